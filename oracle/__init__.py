@@ -1,0 +1,122 @@
+"""fp64 CPU oracle for paged decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never links, loads or calls it, and this package
+never imports the CUDA library.
+
+* ``decode_paged`` -- the paged decode oracle in ``oracle.c`` (plain C,
+  double precision, pthreads over output rows), called through ctypes.
+* ``dense``        -- the literal Lean definitions over unpaged arrays, for
+  tiny cases (see ``dense.py``).
+
+Inputs are numpy arrays: bf16 tensors are passed as their uint16 bit patterns.
+"""
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+ERRORS = {
+    0: "ok",
+    1: "invalid argument",
+    2: "seq_len negative or beyond the block table",
+    3: "a visible position maps to an unmapped or out-of-range page",
+    4: "out of memory",
+}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force=False):
+    """Compile oracle.c with gcc into oracle/_build/liboracle.so."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_libs = {}
+
+
+def _load(lib_path=None):
+    key = lib_path or "default"
+    if key not in _libs:
+        lib = ctypes.CDLL(lib_path or build())
+        fn = lib.oracle_decode_paged
+        fn.restype = ctypes.c_int
+        fn.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q, k_pool, v_pool
+            ctypes.c_void_p, ctypes.c_void_p,                    # block_table, seq_lens
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,  # B Hq Hkv D
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,      # page_size max_blocks num_pages
+            ctypes.c_int32,                                      # window
+            ctypes.c_void_p, ctypes.c_int32,                     # rows, n_rows
+            ctypes.c_void_p, ctypes.c_int32,                     # out, n_threads
+        ]
+        _libs[key] = lib
+    return _libs[key]
+
+
+def _as(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError("expected %s, got %s" % (dtype, a.dtype))
+    return a
+
+
+def decode_paged(q_bits, k_bits, v_bits, block_table, seq_lens, window, page_size=16,
+                 rows=None, threads=1, lib_path=None):
+    """Paged decode attention in fp64.
+
+    q_bits      uint16 [B, Hq, D]                     (bf16 bit patterns)
+    k_bits      uint16 [num_pages, page_size, Hkv, D]
+    v_bits      uint16 [num_pages, page_size, Hkv, D]
+    block_table int32  [B, max_blocks]
+    seq_lens    int32  [B]
+    window      > 0 sliding window, <= 0 none
+    rows        None (all B*Hq rows) or a sequence of flat b*Hq + h indices
+    lib_path    another build of oracle.c to call (the tests' planted-mistake checks)
+    returns     float64 [B, Hq, D], or [len(rows), D] when rows is given
+    """
+    q_bits = _as(q_bits, np.uint16)
+    k_bits = _as(k_bits, np.uint16)
+    v_bits = _as(v_bits, np.uint16)
+    block_table = _as(block_table, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    B, Hq, D = q_bits.shape
+    num_pages, ps, Hkv, Dk = k_bits.shape
+    if ps != page_size or Dk != D or v_bits.shape != k_bits.shape:
+        raise ValueError("pool shape does not match q / page_size")
+    if block_table.ndim != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_table / seq_lens shape")
+    max_blocks = block_table.shape[1]
+    if rows is None:
+        rows_arr, n_rows, out = None, 0, np.zeros((B, Hq, D), dtype=np.float64)
+    else:
+        rows_arr = _as(np.asarray(rows, dtype=np.int32), np.int32)
+        n_rows = len(rows_arr)
+        out = np.zeros((n_rows, D), dtype=np.float64)
+    st = _load(lib_path).oracle_decode_paged(
+        q_bits.ctypes.data, k_bits.ctypes.data, v_bits.ctypes.data,
+        block_table.ctypes.data, seq_lens.ctypes.data,
+        B, Hq, Hkv, D, page_size, max_blocks, num_pages, int(window),
+        None if rows_arr is None else rows_arr.ctypes.data, n_rows,
+        out.ctypes.data, int(threads),
+    )
+    if st != 0:
+        raise OracleError(ERRORS.get(st, "error %d" % st))
+    return out

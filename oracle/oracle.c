@@ -1,0 +1,225 @@
+/*
+ * fp64 CPU oracle for paged decode attention (Gemma-4-12B text path).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * What it computes (one output row per (sequence b, query head h)):
+ *
+ *   Gemma-4-12B model page, "Compute-graph nodes", attn.core rows
+ *   (slidingDecodeGQA and decodeGQA):
+ *       o[b,h] = sum over visible s of softmax_s(1 * <q[b,h], k[b,s,h/G]>) * v[b,s,h/G]
+ *
+ *   Attention.lean, `decodeGQA`: the query of a sequence with L cached tokens
+ *   sits at position L-1, so with no window every cached key l <= L-1 is
+ *   visible, and query head c*G+g reads KV head c.
+ *
+ *   Attention.lean, `slidingGQA`: the query at position p sees key l iff
+ *   l <= p and p < l + window, i.e. p - window < l <= p.  With p = L-1 that is
+ *   the last min(L, window) positions (Op Specs page, NOTE on
+ *   slidingDecodeGQA: "decode attention over the last w cached positions").
+ *
+ *   Attention.lean, `softmax`: exp(s_l) / sum over visible m of exp(s_m) for
+ *   visible l, 0 otherwise.  This oracle subtracts the largest visible logit
+ *   before exponentiating; exp(s_l - M) / sum exp(s_m - M) is the same real
+ *   number, and it keeps exp() finite for logits in the hundreds.
+ *
+ *   Gemma-4-12B model page, "At a glance", shape domain: the KV cache is
+ *   paged with page size 16.  Reading (no layout is printed on the pages): a
+ *   pool holds pages of `page_size` token rows, each row [Hkv, D], so pool
+ *   element (page, slot, c, e) is at ((page*page_size + slot)*Hkv + c)*D + e,
+ *   and logical position l of sequence b lives in physical page
+ *   block_table[b, l / page_size], slot l % page_size.
+ *
+ * Inputs are bf16 bit patterns (uint16); each is widened exactly to double.
+ * Every sum runs in ascending order of its index, in double precision.
+ *
+ * Reading of `window`: window > 0 selects the sliding rule above; window <= 0
+ * means no window (decodeGQA).  L == 0 gives an all-zero row (an empty sum).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum {
+  ORACLE_OK = 0,
+  ORACLE_ERR_ARG = 1,          /* a size or pointer argument is invalid       */
+  ORACLE_ERR_SEQ_LEN = 2,      /* seq_lens[b] < 0 or beyond the block table    */
+  ORACLE_ERR_UNMAPPED = 3,     /* a visible position maps to a page id outside [0, num_pages) */
+  ORACLE_ERR_NOMEM = 4
+};
+
+/* bf16 -> double: a bf16 value is the top 16 bits of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+typedef struct {
+  const uint16_t* q;
+  const uint16_t* k_pool;
+  const uint16_t* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t B, Hq, Hkv, D, page_size, max_blocks;
+  int64_t num_pages;
+  int32_t window;
+  const int32_t* rows; /* flat b*Hq+h indices, or NULL for all rows */
+  int32_t n_rows;
+  double* out;         /* [n_rows, D] */
+  int32_t n_threads;
+  int32_t thread_id;
+  int status;
+} job_t;
+
+/* Index of pool row (token slot) for logical position l of sequence b, or -1. */
+static int64_t pool_row(const job_t* j, int b, int l) {
+  int page = l / j->page_size;
+  if (page >= j->max_blocks) return -1;
+  int64_t phys = j->block_table[(int64_t)b * j->max_blocks + page];
+  if (phys < 0 || phys >= j->num_pages) return -1;
+  return phys * j->page_size + (l % j->page_size);
+}
+
+/* One output row o[b,h,:] (decodeGQA / slidingGQA at position L-1). */
+static int decode_one_row(const job_t* j, int b, int h, double* o, double* logit) {
+  const int G = j->Hq / j->Hkv;
+  const int c = h / G;               /* query head c*G+g reads KV head c */
+  const int D = j->D;
+  const int L = j->seq_lens[b];
+  if (L < 0 || (int64_t)L > (int64_t)j->max_blocks * j->page_size) return ORACLE_ERR_SEQ_LEN;
+
+  /* visible positions: p - window < l <= p with p = L-1 (no lower bound when window <= 0) */
+  int lo = 0;
+  if (j->window > 0 && L > j->window) lo = L - j->window;
+  const int n = L - lo;
+
+  for (int d = 0; d < D; ++d) o[d] = 0.0;
+  if (n <= 0) return ORACLE_OK;
+
+  const uint16_t* qv = j->q + ((int64_t)b * j->Hq + h) * D;
+
+  /* logits s_l = 1 * sum_e q[e] * k[l,c,e]  (scale 1) */
+  double m = -INFINITY;
+  for (int l = lo; l < L; ++l) {
+    int64_t r = pool_row(j, b, l);
+    if (r < 0) return ORACLE_ERR_UNMAPPED;
+    const uint16_t* kv = j->k_pool + (r * j->Hkv + c) * D;
+    double s = 0.0;
+    for (int e = 0; e < D; ++e) s += bf16_bits_to_double(qv[e]) * bf16_bits_to_double(kv[e]);
+    logit[l - lo] = s;
+    if (s > m) m = s;
+  }
+
+  /* softmax over the visible set: w_l = exp(s_l - m), Z = sum w_l */
+  double Z = 0.0;
+  for (int i = 0; i < n; ++i) {
+    logit[i] = exp(logit[i] - m);
+    Z += logit[i];
+  }
+
+  /* o[d] = sum_l w_l * v[l,c,d] / Z */
+  for (int l = lo; l < L; ++l) {
+    int64_t r = pool_row(j, b, l);
+    const uint16_t* vv = j->v_pool + (r * j->Hkv + c) * D;
+    const double w = logit[l - lo];
+    for (int d = 0; d < D; ++d) o[d] += w * bf16_bits_to_double(vv[d]);
+  }
+  for (int d = 0; d < D; ++d) o[d] /= Z;
+  return ORACLE_OK;
+}
+
+static void* worker(void* arg) {
+  job_t* j = (job_t*)arg;
+  int max_L = 0;
+  for (int b = 0; b < j->B; ++b)
+    if (j->seq_lens[b] > max_L) max_L = j->seq_lens[b];
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(max_L > 0 ? max_L : 1));
+  if (!logit) {
+    j->status = ORACLE_ERR_NOMEM;
+    return NULL;
+  }
+  const int total = j->rows ? j->n_rows : j->B * j->Hq;
+  for (int i = j->thread_id; i < total; i += j->n_threads) {
+    const int flat = j->rows ? j->rows[i] : i;
+    const int b = flat / j->Hq, h = flat % j->Hq;
+    int st = decode_one_row(j, b, h, j->out + (int64_t)i * j->D, logit);
+    if (st != ORACLE_OK && j->status == ORACLE_OK) j->status = st;
+  }
+  free(logit);
+  return NULL;
+}
+
+/*
+ * Paged decode attention, fp64.
+ *
+ * q           bf16 bits [B, Hq, D]
+ * k_pool      bf16 bits [num_pages, page_size, Hkv, D]
+ * v_pool      bf16 bits [num_pages, page_size, Hkv, D]
+ * block_table int32 [B, max_blocks]; entries of pages that hold no visible
+ *             position are never read (they may be -1)
+ * seq_lens    int32 [B], 0 <= L <= max_blocks*page_size
+ * window      > 0: sliding window; <= 0: none
+ * rows        NULL for every (b, h) row in b-major order, else n_rows flat
+ *             indices b*Hq + h to compute
+ * out         double [n_rows (or B*Hq), D]
+ * n_threads   worker threads (>= 1); rows are striped over them
+ * returns     ORACLE_OK or an ORACLE_ERR_* code
+ */
+int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                        const int32_t* block_table, const int32_t* seq_lens, int32_t B,
+                        int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                        int32_t max_blocks, int64_t num_pages, int32_t window,
+                        const int32_t* rows, int32_t n_rows, double* out, int32_t n_threads) {
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return ORACLE_ERR_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || page_size < 1 || max_blocks < 1 || num_pages < 1)
+    return ORACLE_ERR_ARG;
+  if (Hq % Hkv != 0) return ORACLE_ERR_ARG;
+  if (rows) {
+    if (n_rows < 0) return ORACLE_ERR_ARG;
+    for (int i = 0; i < n_rows; ++i)
+      if (rows[i] < 0 || rows[i] >= B * Hq) return ORACLE_ERR_ARG;
+  }
+  if (n_threads < 1) n_threads = 1;
+
+  job_t* jobs = (job_t*)calloc((size_t)n_threads, sizeof(job_t));
+  pthread_t* tids = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+  if (!jobs || !tids) {
+    free(jobs);
+    free(tids);
+    return ORACLE_ERR_NOMEM;
+  }
+  for (int t = 0; t < n_threads; ++t) {
+    job_t* j = &jobs[t];
+    j->q = q; j->k_pool = k_pool; j->v_pool = v_pool;
+    j->block_table = block_table; j->seq_lens = seq_lens;
+    j->B = B; j->Hq = Hq; j->Hkv = Hkv; j->D = D; j->page_size = page_size;
+    j->max_blocks = max_blocks; j->num_pages = num_pages; j->window = window;
+    j->rows = rows; j->n_rows = n_rows; j->out = out;
+    j->n_threads = n_threads; j->thread_id = t; j->status = ORACLE_OK;
+  }
+  int status = ORACLE_OK;
+  if (n_threads == 1) {
+    worker(&jobs[0]);
+  } else {
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t) {
+      if (pthread_create(&tids[t], NULL, worker, &jobs[t]) != 0) break;
+      ++started;
+    }
+    for (int t = 0; t < started; ++t) pthread_join(tids[t], NULL);
+    /* rows of threads that never started are computed here */
+    for (int t = started; t < n_threads; ++t) worker(&jobs[t]);
+  }
+  for (int t = 0; t < n_threads; ++t)
+    if (jobs[t].status != ORACLE_OK && status == ORACLE_OK) status = jobs[t].status;
+  free(jobs);
+  free(tids);
+  return status;
+}
