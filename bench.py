@@ -1,0 +1,530 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark on GB300: achieved HBM GB/s and attention calls/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 1|2|3|4|4b|5]
+
+A step is one decode-attention call (for workload 5: one whole decode step,
+40 sliding + 8 global layer calls) over synthetic inputs already resident in
+HBM.  The default workload is the global decode at B=8, seq_lens U[1, 8192].
+Throughput counts algorithmic bytes only: the visible K and V rows, q and o.
+
+Inputs larger than L2 are used as they are; smaller ones are rotated over
+enough distinct copies that every step reads from HBM, not L2.  Calls are
+replayed from a CUDA graph (the decode step of a serving loop); ``e2e`` times
+the same calls through the public API with the per-step inputs (q, block
+table, seq_lens) copied from pinned host memory and o copied back.
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica
+(the attention of different sequences shares nothing): value is the bytes of
+all ranks over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and attention calls/sec"
+UNIT = "GB/s"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (no GPU needed; covered by tests/test_bench_host.py)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(kind, seq_lens, window, Hq=16, out_bytes=2):
+    """Visible K and V rows + q + o of one call (block table and seq_lens not counted)."""
+    Hkv, D = (8, 256) if kind == "sliding" else (1, 512)
+    vis = sum(min(L, window) if window > 0 else L for L in seq_lens)
+    B = len(seq_lens)
+    return vis * Hkv * D * 2 * 2 + B * Hq * D * 2 + B * Hq * D * out_bytes
+
+
+def rotation_count(bytes_per_set, floor=1, cap=16):
+    """Distinct input sets so that consecutive reuse of a set is separated by > 3x L2."""
+    if bytes_per_set <= 0:
+        return floor
+    return max(floor, min(cap, int(math.ceil(4 * L2_BYTES / bytes_per_set))))
+
+
+def aggregate(per_rank, steps, warmup, n_gpus, config, dtype="bf16"):
+    """Combine per-rank results {bytes, ms, calls, ...} into the JSON line (rank 0)."""
+    ms = max(r["ms"] for r in per_rank)
+    total_bytes = sum(r["bytes"] for r in per_rank)
+    total_calls = sum(r["calls"] for r in per_rank)
+    value = total_bytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": n_gpus,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(ms / steps, 6),
+        "calls_per_s": round(total_calls / (ms * 1e-3), 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype,
+        "data": "synthetic",
+        "config": config,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return self.summary()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((t, parts))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        lo = (self.t0 or 0) - 0.15
+        hi = (self.t1 or time.time()) + 0.15
+        inside = [p for t, p in rows if lo <= t <= hi] or [min(rows, key=lambda r: abs(r[0] - lo))[1]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for p in inside if num(p[2]) is not None]
+        smax = [num(p[3]) for p in inside if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def workload_calls(cfg, device, seed_offset=0):
+    """The calls (DecodeCase) of one step of workload `cfg`."""
+    from workloads import config_case, N_LAYERS
+    if cfg == "5":
+        return [config_case(5, device=device, layer=i, poison=False, seed_offset=seed_offset)
+                for i in range(N_LAYERS)]
+    if cfg == "4b":
+        return [config_case(4, device=device, variant="b", poison=False, seed_offset=seed_offset)]
+    return [config_case(int(cfg), device=device, poison=False, seed_offset=seed_offset)]
+
+
+def workload_name(cfg):
+    from workloads import WORKLOADS
+    if cfg == "4b":
+        return "long-context global decode: B=4 x 262144, 16/1 heads, D=512"
+    return WORKLOADS[int(cfg)]
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_decode_attention_gb300 as pda
+    from workloads import config_case, N_LAYERS
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pda.load()
+    stream = torch.cuda.Stream(device=dev)
+
+    # --- inputs: one or more rotating sets of the step's calls ---
+    calls0 = workload_calls(args.config, dev)
+    step_bytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c in calls0)
+    kv_bytes = sum(c.k_pool.numel() * 2 * 2 for c in calls0)
+    n_sets = rotation_count(kv_bytes)
+    sets = [calls0] + [workload_calls(args.config, dev, seed_offset=100000 * k) for k in range(1, n_sets)]
+
+    # per-call buffers: outputs, workspaces, status
+    plans = []
+    for cs in sets:
+        pl = []
+        for c in cs:
+            kind = pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL
+            ws_bytes = pda.attn_decode_workspace_size(kind, c.B, c.max_seq_len, c.window)
+            ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+            o = torch.empty((c.B, c.Hq, c.D), dtype=torch.bfloat16, device=dev)
+            pl.append((c, ws, o))
+        plans.append(pl)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch(pl):
+        for c, ws, o in pl:
+            fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
+            fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
+               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream)
+
+    kernels_per_call = []
+    for c in calls0:
+        kind = pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL
+        ns, _ = pda.attn_decode_plan(kind, c.B, c.max_seq_len, c.window,
+                                     num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+        kernels_per_call.append(2 if ns > 1 else 1)
+
+    # warm-up (direct calls), then capture one rotation as a graph
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            launch(plans[i % n_sets])
+    stream.synchronize()
+    graphs = []
+    if not args.no_graph:
+        for pl in plans:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                launch(pl)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, 3)):
+                graphs[i % n_sets].replay()
+        stream.synchronize()
+
+    def step(i):
+        if graphs:
+            graphs[i % n_sets].replay()
+        else:
+            launch(plans[i % n_sets])
+
+    # --- timed region ---
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-%s" % props.uuid) if getattr(props, "uuid", None) else str(local_rank)
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark(True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+    ev1.synchronize()
+    if sampler:
+        sampler.mark(False)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError("device status %d during the benchmark" % st)
+
+    res = {"bytes": step_bytes * args.steps, "ms": ms, "calls": len(calls0) * args.steps}
+
+    # --- dominant kernel: per-launch duration of the heaviest call, events around it ---
+    heavy = max(range(len(calls0)), key=lambda j: algorithmic_bytes(calls0[j].kind, calls0[j].seq_lens_host,
+                                                                    calls0[j].window))
+    reps = max(8, min(200, args.steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(reps):
+            c, ws, o = plans[i % n_sets][heavy]
+            fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
+            fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
+               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream)
+        e1.record(stream)
+    e1.synchronize()
+    heavy_ms = e0.elapsed_time(e1) / reps
+    hc = calls0[heavy]
+    heavy_bytes = algorithmic_bytes(hc.kind, hc.seq_lens_host, hc.window)
+
+    # --- end to end through the public API with host buffers ---
+    e2e = run_e2e(args, plans, n_sets, stream, status, dev)
+
+    res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
+               heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
+               launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
+    return res
+
+
+def run_e2e(args, plans, n_sets, stream, status, dev):
+    """Per step: H2D of q, block_table, seq_lens from pinned memory; the API call; D2H of o."""
+    import torch
+    import paged_decode_attention_gb300 as pda
+    host = []
+    for pl in plans:
+        hs = []
+        for c, ws, o in pl:
+            hs.append((c.q.cpu().pin_memory(), c.block_table.cpu().pin_memory(),
+                       c.seq_lens.cpu().pin_memory(), torch.empty(o.shape, dtype=o.dtype).pin_memory()))
+        host.append(hs)
+    h2d = sum(q.numel() * 2 + bt.numel() * 4 + sl.numel() * 4 for q, bt, sl, _ in host[0])
+    d2h = sum(oh.numel() * 2 for _, _, _, oh in host[0])
+    steps = max(3, min(args.steps, 200))
+
+    def one(i):
+        pl, hs = plans[i % n_sets], host[i % n_sets]
+        for (c, ws, o), (qh, bth, slh, oh) in zip(pl, hs):
+            c.q.copy_(qh, non_blocking=True)
+            c.block_table.copy_(bth, non_blocking=True)
+            c.seq_lens.copy_(slh, non_blocking=True)
+            fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
+            fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
+               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream)
+            oh.copy_(o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i)
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            one(i)
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    step_bytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c, _, _ in plans[0])
+    return {"value": round(step_bytes * steps / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 6)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(cfg, budget_s=2.0):
+    """A bounded sample of workload `cfg` for the fp64 oracle: (callable, bytes, description)."""
+    import numpy as np
+    import oracle
+    from workloads import bits, config_seq_lens, make_case
+    lens = config_seq_lens(5 if cfg == "5" else (4 if cfg == "4b" else int(cfg)), "b" if cfg == "4b" else None)
+    kind = "sliding" if cfg in ("1", "3") else "global"
+    if cfg == "5":
+        kind = "global"
+    window = 1024 if kind == "sliding" else 0
+    # the first sequences of the workload, as many as fit a per-position budget
+    per_pos_s = 2.0e-7 if kind == "global" else 4.0e-7   # rough fp64 cost per position (16 heads)
+    take, acc = [], 0.0
+    for L in lens:
+        n = min(L, window) if window > 0 else L
+        if take and acc + n * per_pos_s > budget_s:
+            break
+        if n * per_pos_s > budget_s and not take:
+            L = max(1, int(budget_s / per_pos_s))
+            n = L
+        take.append(L)
+        acc += n * per_pos_s
+    case = make_case(kind, take, seed=5150, device="cpu", window=window,
+                     window_only=(kind == "sliding"), poison=False)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    args = (bits(case.q), bits(case.k_pool), bits(case.v_pool), case.block_table.numpy(),
+            case.seq_lens.numpy(), case.window)
+
+    def run():
+        oracle.decode_paged(*args, threads=threads)
+
+    nbytes = algorithmic_bytes(kind, take, window)
+    desc = "%s decode, %d sequence(s) of the workload's seq_lens (%s), all 16 heads" % (
+        kind, len(take), ",".join(str(x) for x in take[:6]) + ("..." if len(take) > 6 else ""))
+    return run, nbytes, desc, threads
+
+
+def cpu_baseline(cfg, budget_s=2.0, reps=3):
+    run, nbytes, desc, threads = oracle_sample(cfg, budget_s)
+    run()
+    t = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        run()
+        t.append(time.perf_counter() - t0)
+    sec = min(t)
+    return {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": desc, "seconds_per_sample": round(sec, 4)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    run, nbytes, desc, threads = oracle_sample(args.config, budget_s=0.5)
+    for _ in range(max(args.warmup, 0)):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    sec = time.perf_counter() - t0
+    value = round(nbytes * args.steps / sec / 1e9, 4)
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(args.config), "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+
+_PG = None
+
+
+def init_dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local_rank
+
+
+def setup_pg(world, backend):
+    global _PG
+    if world > 1 and _PG is None:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+        _PG = dist
+
+
+def barrier(world):
+    if world > 1 and _PG is not None:
+        _PG.barrier()
+
+
+def gather_results(res, world):
+    if world == 1:
+        return [res]
+    out = [None] * world
+    _PG.all_gather_object(out, res)
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4b", "5"])
+    ap.add_argument("--no-graph", action="store_true", help="launch every call directly (no CUDA graph)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = init_dist()
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    setup_pg(world, "nccl")
+    res = run_ours(args, rank, world, local_rank)
+    allres = gather_results(res, world)
+    if rank != 0:
+        return 0
+    peak, peak_src = load_peaks()
+    r0 = allres[0]
+    config = {"workload": workload_name(args.config), "config_id": args.config,
+              "l2": ("inputs %.0f MB > L2; %d set(s)" % (r0["kv_bytes"] / 1e6, r0["n_sets"])
+                     if r0["n_sets"] == 1 else
+                     "rotating %d input sets (%.0f MB in all) so every step reads HBM"
+                     % (r0["n_sets"], r0["n_sets"] * r0["kv_bytes"] / 1e6)),
+              "launch": "cuda graph replay" if not args.no_graph else "direct"}
+    line = aggregate(allres, args.steps, args.warmup, args.gpus, config)
+    achieved = r0["heavy_bytes"] / (r0["heavy_ms"] * 1e-3) / 1e9
+    line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4), "traffic": None,
+                        "peak_source": peak_src,
+                        "kernel": "%s decode (%d launch%s per call, timed together)"
+                        % (r0["heavy_kind"], r0["heavy_kernels"], "es" if r0["heavy_kernels"] > 1 else "")}
+    line["hbm_frac_of_peak"] = round(line["value"] / peak, 4)
+    line["gpu_launches"] = r0["launches_per_step"] * args.steps
+    line["e2e"] = r0["e2e"]
+    line["clocks"] = r0["clocks"]
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * attn_decode.h -- C ABI of the GB300 (sm_103a) paged decode-attention library
+ * for the Gemma-4-12B text path.
+ *
+ * Two operations, one per attention node of the model's compute graph
+ * (Gemma-4-12B model page, "Compute-graph nodes", the two attn.core rows):
+ *
+ *   attn_decode_sliding -- node `slidingDecodeGQA`, the 40 sliding-window layers:
+ *       16 query heads over 8 KV heads (query head h reads KV head h/2),
+ *       head dim 256, window 1024, scale 1.
+ *   attn_decode_global  -- node `decodeGQA`, the 8 global layers:
+ *       16 query heads over 1 KV head (h/16 = 0), head dim 512, scale 1.
+ *
+ * Both compute, for every sequence b and query head h with c = h / G,
+ *
+ *   o[b,h,:] = sum over visible l of softmax_l( <q[b,h,:], k[b,l,c,:]> ) * v[b,l,c,:]
+ *
+ * where the softmax is normalised over the visible positions only
+ * (Attention.lean `softmax`), the query sits at position p = L-1 with
+ * L = seq_lens[b] (Attention.lean `decodeGQA`), and position l is visible iff
+ * l <= p and, when a window w > 0 is given, p < l + w (Attention.lean
+ * `slidingGQA`), i.e. the last min(L, w) positions (Op Specs page, NOTE on
+ * slidingDecodeGQA).  The scale is fixed at 1 ("the q/k norms take its
+ * place", Gemma-4-12B model page, "What to watch for"); there is no logit
+ * soft-cap in attention (only the LM head is capped).  L == 0 gives o = 0.
+ *
+ * KV cache: pages of 16 token positions (Gemma-4-12B model page, "At a
+ * glance", shape domain: page size 16).  A pool is one contiguous array
+ * [num_pages, 16, Hkv, D] of bf16 -- each page holds 16 token rows, each row
+ * the Hkv heads of one position, the token-major order of the attn.core
+ * tensor k[B, S, Hkv, D].  Position l of sequence b lives in page
+ * block_table[b * max_blocks + l / 16], row l % 16.  Entries for pages that
+ * hold no visible position are never read and may be -1.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All array pointers are DEVICE pointers owned by the caller; each must be
+ *   16-byte aligned and the arrays contiguous in the layouts stated.
+ * - The library allocates no memory and never synchronises: work is enqueued
+ *   on `stream` (a cudaStream_t passed as void*; NULL = legacy default stream)
+ *   and the call returns as soon as it is launched.
+ * - Host-side validation runs before anything is launched; on any error
+ *   nothing is enqueued and the call returns a nonzero ATTN_ERR_* code, with
+ *   a message in attn_last_error() (per host thread).
+ * - `status` (optional, may be NULL) is a device int32 that the kernels OR
+ *   ATTN_DEV_* bits into when they detect a contract violation on the device
+ *   (the host cannot see seq_lens or block_table without a synchronisation).
+ *   The caller zeroes it and reads it back when it wants to check.  A page id
+ *   outside [0, num_pages) on a visible position is never dereferenced: the
+ *   copy engine fills that page with zeros and ATTN_DEV_BAD_PAGE is raised.
+ * - The device (SM count) is the CUDA current device of the calling thread.
+ */
+#ifndef ATTN_DECODE_H
+#define ATTN_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_DECODE_ABI_VERSION 1
+
+/* return codes */
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG 1 /* null or misaligned pointer, bad size           */
+#define ATTN_ERR_UNSUPPORTED 2 /* outside the model's shape domain               */
+#define ATTN_ERR_WORKSPACE 3   /* workspace missing or smaller than required     */
+#define ATTN_ERR_CUDA 4        /* a CUDA runtime/driver call or launch failed    */
+
+/* output element type */
+#define ATTN_OUT_BF16 0 /* o is bf16, rounded to nearest even                    */
+#define ATTN_OUT_F32 1  /* o is fp32                                             */
+
+/* operation kinds (for the planning queries) */
+#define ATTN_KIND_SLIDING 0
+#define ATTN_KIND_GLOBAL 1
+
+/* device status bits (OR-ed into *status) */
+#define ATTN_DEV_WAIT_TIMEOUT 1 /* a copy-pipeline wait exceeded its time limit     */
+#define ATTN_DEV_BAD_PAGE 2     /* visible position mapped to page id not in [0,num_pages) */
+#define ATTN_DEV_BAD_SEQ_LEN 4  /* seq_lens[b] < 0 or > max_blocks*16 (clamped)      */
+
+/* Fixed shapes of the two operations (Gemma-4-12B model page, attn.core rows). */
+#define ATTN_SLIDING_HQ 16
+#define ATTN_SLIDING_HKV 8
+#define ATTN_SLIDING_D 256
+#define ATTN_GLOBAL_HQ 16
+#define ATTN_GLOBAL_HKV 1
+#define ATTN_GLOBAL_D 512
+#define ATTN_PAGE_SIZE 16
+
+/* Shape domain (Gemma-4-12B model page, "At a glance"): B in [1,256],
+ * up to 262144 cached positions. */
+#define ATTN_MAX_BATCH 256
+#define ATTN_MAX_SEQ_LEN 262144
+
+/*
+ * attn_decode_sliding -- slidingDecodeGQA (Gemma-4-12B sliding layers).
+ *
+ * q            bf16 [batch, 16, 256]
+ * k_pool       bf16 [num_pages, 16, 8, 256]
+ * v_pool       bf16 [num_pages, 16, 8, 256]
+ * block_table  int32 [batch, max_blocks]
+ * seq_lens     int32 [batch], 0 <= L <= max_blocks*16
+ * o            [batch, 16, 256], bf16 or fp32 per out_dtype (written, never read)
+ * batch        1..256
+ * max_blocks   >= 1, width of block_table
+ * num_pages    >= 1, pages in each pool; num_pages*16 < 2^31
+ * max_seq_len  host-side upper bound on seq_lens (0..max_blocks*16), used only
+ *              to plan the split of the sequence across thread blocks; a
+ *              smaller value than the true maximum is still computed
+ *              correctly, only more slowly
+ * window       > 0; the node's value is 1024
+ * out_dtype    ATTN_OUT_BF16 or ATTN_OUT_F32
+ * num_splits   0 = choose automatically; > 0 forces that many KV splits per
+ *              (sequence, KV head) (clamped to the pages a split can hold)
+ * workspace    device scratch of at least attn_decode_workspace_size(...)
+ *              bytes (may be NULL when that size is 0); contents need no
+ *              initialisation; must not be shared by calls that overlap
+ * status       optional device int32 for ATTN_DEV_* bits, or NULL
+ * stream       cudaStream_t, as void*
+ * returns      ATTN_OK or ATTN_ERR_*
+ */
+int32_t attn_decode_sliding(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_table, const int32_t* seq_lens, void* o,
+                            int32_t batch, int32_t max_blocks, int64_t num_pages,
+                            int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                            int32_t num_splits, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream);
+
+/*
+ * attn_decode_global -- decodeGQA (Gemma-4-12B global layers).
+ *
+ * Same arguments as attn_decode_sliding, with shapes
+ *   q bf16 [batch, 16, 512];  k_pool, v_pool bf16 [num_pages, 16, 1, 512];
+ *   o [batch, 16, 512].
+ * window <= 0 is the node as printed (no window, every cached key visible);
+ * window > 0 applies the slidingGQA visibility rule.
+ * k_pool and v_pool may be the same pointer.
+ */
+int32_t attn_decode_global(const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_table, const int32_t* seq_lens, void* o,
+                           int32_t batch, int32_t max_blocks, int64_t num_pages,
+                           int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                           int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           int32_t* status, void* stream);
+
+/*
+ * attn_decode_plan -- the launch plan, as pure host arithmetic (no CUDA call).
+ *
+ * kind         ATTN_KIND_SLIDING or ATTN_KIND_GLOBAL
+ * batch, max_seq_len, window, num_splits   as for the operations
+ * num_sms      streaming multiprocessors of the target device (>= 1)
+ * out_num_splits        receives the KV splits per (sequence, KV head)
+ * out_workspace_bytes   receives the workspace size the operation requires
+ * returns      ATTN_OK or ATTN_ERR_INVALID_ARG
+ */
+int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
+                         int32_t num_splits, int32_t num_sms, int32_t* out_num_splits,
+                         size_t* out_workspace_bytes);
+
+/*
+ * attn_decode_workspace_size -- attn_decode_plan's workspace size for the
+ * current CUDA device.  Returns 0 (and sets attn_last_error) on bad
+ * arguments or when no device can be queried; 0 is also the valid size of a
+ * call that needs no workspace, so check attn_last_error() when in doubt.
+ */
+size_t attn_decode_workspace_size(int32_t kind, int32_t batch, int32_t max_seq_len,
+                                  int32_t window, int32_t num_splits);
+
+/* Message of the last error on this host thread ("" if none). */
+const char* attn_last_error(void);
+
+/* ATTN_DECODE_ABI_VERSION of the loaded library. */
+int32_t attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_DECODE_H */

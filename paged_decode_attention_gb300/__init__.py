@@ -1,0 +1,188 @@
+"""Paged decode attention for the Gemma-4-12B text path on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/attn_decode.h``; every
+function here only checks and marshals arguments (torch tensors -> device
+pointers) and calls the library of the same name.  All arithmetic runs in
+the CUDA kernels of ``libattn_decode.so``; there is no CPU path.  The library
+is built in-tree by ``_build.build()`` (or ``__graft_entry__.build()``); when
+it is missing, ``load()`` raises instead of falling back to anything.
+
+    attn_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, ...)  -> o
+    attn_decode_global(q, k_pool, v_pool, block_table, seq_lens, ...)   -> o
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "attn_decode_sliding", "attn_decode_global", "attn_decode_plan", "attn_decode_workspace_size",
+    "attn_last_error", "load", "library_path", "AttnDecodeError",
+    "KIND_SLIDING", "KIND_GLOBAL", "DEV_WAIT_TIMEOUT", "DEV_BAD_PAGE", "DEV_BAD_SEQ_LEN",
+]
+
+ATTN_OK = 0
+ERROR_NAMES = {1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_WORKSPACE",
+               4: "ATTN_ERR_CUDA"}
+OUT_BF16, OUT_F32 = 0, 1
+KIND_SLIDING, KIND_GLOBAL = 0, 1
+DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN = 1, 2, 4
+PAGE_SIZE = 16
+SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
+
+EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_plan",
+           "attn_decode_workspace_size", "attn_last_error", "attn_abi_version")
+
+
+class AttnDecodeError(RuntimeError):
+    def __init__(self, code, message):
+        super().__init__("%s: %s" % (ERROR_NAMES.get(code, "error %d" % code), message))
+        self.code = code
+
+
+_lib = None
+
+
+def library_path():
+    return _build.LIB_PATH
+
+
+def load(path=None):
+    """Load libattn_decode.so (built in-tree); raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError("CUDA library %s is not built; run __graft_entry__.build() "
+                           "(there is no CPU fallback)" % p)
+    lib = ctypes.CDLL(p)
+    c_i32, c_i64, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    call = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,       # q k_pool v_pool block_table seq_lens o
+            c_i32, c_i32, c_i64, c_i32, c_i32, c_i32,  # batch max_blocks num_pages max_seq_len window out_dtype
+            c_i32, c_vp, c_sz, c_vp, c_vp]             # num_splits workspace workspace_bytes status stream
+    for name in ("attn_decode_sliding", "attn_decode_global"):
+        fn = getattr(lib, name)
+        fn.restype = c_i32
+        fn.argtypes = call
+    lib.attn_decode_plan.restype = c_i32
+    lib.attn_decode_plan.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                     ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]
+    lib.attn_decode_workspace_size.restype = c_sz
+    lib.attn_decode_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32]
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_last_error.argtypes = []
+    lib.attn_abi_version.restype = c_i32
+    lib.attn_abi_version.argtypes = []
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def attn_last_error():
+    return load().attn_last_error().decode()
+
+
+def attn_decode_plan(kind, batch, max_seq_len, window, num_splits=0, num_sms=152):
+    """(num_splits, workspace_bytes) the library would use; pure host arithmetic."""
+    lib = load()
+    ns = ctypes.c_int32(0)
+    ws = ctypes.c_size_t(0)
+    st = lib.attn_decode_plan(kind, batch, max_seq_len, window, num_splits, num_sms,
+                              ctypes.byref(ns), ctypes.byref(ws))
+    if st != ATTN_OK:
+        raise AttnDecodeError(st, attn_last_error())
+    return ns.value, ws.value
+
+
+def attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits=0):
+    """Workspace bytes for the current CUDA device."""
+    lib = load()
+    n = lib.attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits)
+    err = attn_last_error()
+    if n == 0 and err:
+        raise AttnDecodeError(1, err)
+    return n
+
+
+def _ptr(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor (there is no CPU path)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t.data_ptr()
+
+
+def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len, out_dtype,
+          num_splits, workspace, status, stream):
+    Hq, Hkv, D = SHAPES[kind]
+    if q.dim() != 3:
+        raise ValueError("q must be [batch, %d, %d]" % (Hq, D))
+    batch = q.shape[0]
+    if k_pool.dim() != 4:
+        raise ValueError("k_pool must be [num_pages, 16, %d, %d]" % (Hkv, D))
+    num_pages = k_pool.shape[0]
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    max_blocks = block_table.shape[1]
+    args_q = _ptr(q, "q", torch.bfloat16, (batch, Hq, D))
+    args_k = _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))
+    args_v = _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))
+    args_bt = _ptr(block_table, "block_table", torch.int32, (batch, max_blocks))
+    args_sl = _ptr(seq_lens, "seq_lens", torch.int32, (batch,))
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out_dtype must be torch.bfloat16 or torch.float32")
+    if o is None:
+        o = torch.empty((batch, Hq, D), dtype=out_dtype, device=q.device)
+    args_o = _ptr(o, "o", o.dtype, (batch, Hq, D))
+    if max_seq_len is None:
+        max_seq_len = max_blocks * PAGE_SIZE
+    lib = load()
+    if workspace is None:
+        with torch.cuda.device(q.device):
+            need = attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace, "workspace", torch.uint8)
+    st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    fn = lib.attn_decode_sliding if kind == KIND_SLIDING else lib.attn_decode_global
+    with torch.cuda.device(q.device):
+        st = fn(args_q, args_k, args_v, args_bt, args_sl, args_o, batch, max_blocks, num_pages,
+                int(max_seq_len), int(window), OUT_F32 if o.dtype == torch.float32 else OUT_BF16,
+                int(num_splits), ws_ptr, workspace.numel(), st_ptr, s_ptr)
+    if st != ATTN_OK:
+        raise AttnDecodeError(st, attn_last_error())
+    return o
+
+
+def attn_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=1024,
+                        max_seq_len=None, out_dtype=torch.bfloat16, num_splits=0, workspace=None,
+                        status=None, stream=None):
+    """slidingDecodeGQA: q [B,16,256], pools [P,16,8,256] bf16 -> o [B,16,256].
+
+    max_seq_len: host bound on seq_lens for the split plan (default max_blocks*16).
+    workspace:   uint8 CUDA tensor of at least attn_decode_workspace_size(...) bytes
+                 (allocated per call when None).
+    status:      optional int32 [1] CUDA tensor receiving ATTN_DEV_* bits.
+    """
+    return _call(KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len,
+                 out_dtype, num_splits, workspace, status, stream)
+
+
+def attn_decode_global(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=0,
+                       max_seq_len=None, out_dtype=torch.bfloat16, num_splits=0, workspace=None,
+                       status=None, stream=None):
+    """decodeGQA: q [B,16,512], pools [P,16,1,512] bf16 -> o [B,16,512] (window <= 0: none)."""
+    return _call(KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len,
+                 out_dtype, num_splits, workspace, status, stream)

@@ -1,0 +1,312 @@
+// attn_decode.cu -- host side of the C ABI declared in include/attn_decode.h:
+// argument validation, the split plan, TMA tensor maps and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attn_decode.h"
+#include "combine.cuh"
+#include "global.cuh"
+#include "sliding.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int32_t fail(int32_t code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// Split plan: how many thread blocks share one (sequence, KV head) unit.
+//
+// A unit's visible pages are cut into num_splits runs.  More splits fill the
+// 152 SMs when there are few units (small batch, long sequences); fewer keep
+// the partial-result traffic (one fp32 [Hq_per_unit, D] row per split) and
+// the combine launch off the critical path.  Resident blocks per SM follow
+// from the kernels' shared memory: 3 for the sliding kernel (~66 KB each),
+// 2 for the global kernel (~106 KB each).
+// ---------------------------------------------------------------------------
+struct Plan {
+  int num_splits;
+  int pages_per_split;
+  size_t part_o_bytes;
+  size_t workspace_bytes;
+};
+
+int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
+                  int32_t forced_splits, int32_t num_sms, Plan* out) {
+  if (kind != ATTN_KIND_SLIDING && kind != ATTN_KIND_GLOBAL)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown kind %d", kind);
+  if (batch < 1) return fail(ATTN_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", batch);
+  if (max_seq_len < 0) return fail(ATTN_ERR_INVALID_ARG, "max_seq_len must be >= 0");
+  if (forced_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (num_sms < 1) return fail(ATTN_ERR_INVALID_ARG, "num_sms must be >= 1");
+  const bool sliding = kind == ATTN_KIND_SLIDING;
+  const int D = sliding ? ATTN_SLIDING_D : ATTN_GLOBAL_D;
+  const int Hq = sliding ? ATTN_SLIDING_HQ : ATTN_GLOBAL_HQ;
+  const int units = sliding ? batch * ATTN_SLIDING_HKV : batch;
+  const int blocks_per_sm = sliding ? 3 : 2;
+  const int min_pages = sliding ? 4 : 8;
+
+  int max_pages = (max_seq_len + ATTN_PAGE_SIZE - 1) / ATTN_PAGE_SIZE;
+  if (window > 0) {
+    const int wpages = (window + ATTN_PAGE_SIZE - 1) / ATTN_PAGE_SIZE + 1;
+    if (wpages < max_pages) max_pages = wpages;
+  }
+  int ns = 1;
+  if (max_pages > 0) {
+    if (forced_splits > 0) {
+      ns = forced_splits;
+    } else {
+      const int slots = num_sms * blocks_per_sm;
+      ns = (slots + units - 1) / units;
+      const int cap = max_pages / min_pages > 1 ? max_pages / min_pages : 1;
+      if (ns > cap) ns = cap;
+    }
+    if (ns > max_pages) ns = max_pages;
+    if (ns < 1) ns = 1;
+  }
+  const int pps = max_pages > 0 ? (max_pages + ns - 1) / ns : 1;
+  if (max_pages > 0) ns = (max_pages + pps - 1) / pps;
+  out->num_splits = ns;
+  out->pages_per_split = pps;
+  if (ns > 1) {
+    const size_t rows = static_cast<size_t>(batch) * Hq * ns;
+    out->part_o_bytes = align256(rows * D * sizeof(float));
+    out->workspace_bytes = out->part_o_bytes + align256(rows * sizeof(float2));
+  } else {
+    out->part_o_bytes = 0;
+    out->workspace_bytes = 0;
+  }
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Device facts and TMA descriptors
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+int32_t current_device(int* dev, int* num_sms) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device index %d unsupported", *dev);
+  static int sms[kMaxDevices] = {0};
+  if (sms[*dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev);
+    if (e != cudaSuccess || n < 1)
+      return fail(ATTN_ERR_CUDA, "cudaDeviceGetAttribute(SM count): %s", cudaGetErrorString(e));
+    sms[*dev] = n;
+  }
+  *num_sms = sms[*dev];
+  return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The pool [num_pages, 16, Hkv, D] viewed as a 2-D tensor of num_pages*16
+// token rows by Hkv*D bf16 elements; boxes of 16 rows x box_cols.
+int32_t encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, int row_elems,
+                        int box_cols, CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems),
+                              static_cast<cuuint64_t>(num_pages) * ATTN_PAGE_SIZE};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), ATTN_PAGE_SIZE};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
+                   elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return ATTN_OK;
+}
+
+template <typename Kernel>
+int32_t ensure_smem(Kernel kernel, size_t bytes, int dev, bool* done) {
+  if (done[dev]) return ATTN_OK;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  done[dev] = true;
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Common validation + launch
+// ---------------------------------------------------------------------------
+int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* v_pool,
+                   const int32_t* block_table, const int32_t* seq_lens, void* o, int32_t batch,
+                   int32_t max_blocks, int64_t num_pages, int32_t max_seq_len, int32_t window,
+                   int32_t out_dtype, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                   int32_t* status, void* stream) {
+  g_err[0] = '\0';
+  const bool sliding = kind == ATTN_KIND_SLIDING;
+  const char* name = sliding ? "attn_decode_sliding" : "attn_decode_global";
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !o)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: null array pointer", name);
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(block_table) ||
+      !aligned16(seq_lens) || !aligned16(o))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: every array must be 16-byte aligned", name);
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: status must be 4-byte aligned", name);
+  if (batch < 1) return fail(ATTN_ERR_INVALID_ARG, "%s: batch must be >= 1 (got %d)", name, batch);
+  if (batch > ATTN_MAX_BATCH)
+    return fail(ATTN_ERR_UNSUPPORTED, "%s: batch %d outside the model's domain [1, %d]", name, batch,
+                ATTN_MAX_BATCH);
+  if (max_blocks < 1) return fail(ATTN_ERR_INVALID_ARG, "%s: max_blocks must be >= 1", name);
+  if (num_pages < 1) return fail(ATTN_ERR_INVALID_ARG, "%s: num_pages must be >= 1", name);
+  if (num_pages > (int64_t{1} << 31) / ATTN_PAGE_SIZE - 1)
+    return fail(ATTN_ERR_UNSUPPORTED, "%s: num_pages %lld too large (row index must fit in int32)", name,
+                static_cast<long long>(num_pages));
+  if (max_seq_len < 0 || static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * ATTN_PAGE_SIZE)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: max_seq_len %d not in [0, max_blocks*16 = %lld]", name,
+                max_seq_len, static_cast<long long>(max_blocks) * ATTN_PAGE_SIZE);
+  if (max_seq_len > ATTN_MAX_SEQ_LEN)
+    return fail(ATTN_ERR_UNSUPPORTED, "%s: max_seq_len %d beyond the model's domain (%d)", name,
+                max_seq_len, ATTN_MAX_SEQ_LEN);
+  if (sliding && window <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: window must be > 0 (the node's is 1024)", name);
+  if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: out_dtype must be ATTN_OUT_BF16 or ATTN_OUT_F32", name);
+  if (num_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "%s: num_splits must be >= 0", name);
+
+  int dev = 0, num_sms = 0;
+  int32_t st = current_device(&dev, &num_sms);
+  if (st != ATTN_OK) return st;
+  Plan plan;
+  st = make_plan(kind, batch, max_seq_len, window, num_splits, num_sms, &plan);
+  if (st != ATTN_OK) return st;
+  if (plan.workspace_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+      return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes required (got %zu)", name,
+                  plan.workspace_bytes, workspace ? workspace_bytes : size_t{0});
+    if (!aligned16(workspace)) return fail(ATTN_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
+  }
+
+  pda::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.o = o;
+  p.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
+  p.part_ml = plan.workspace_bytes
+                  ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + plan.part_o_bytes)
+                  : nullptr;
+  p.status = status;
+  p.num_pages = num_pages;
+  p.batch = batch;
+  p.max_blocks = max_blocks;
+  p.window = window;
+  p.num_splits = plan.num_splits;
+  p.pages_per_split = plan.pages_per_split;
+  p.out_f32 = out_dtype == ATTN_OUT_F32;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tm_k, tm_v;
+  if (sliding) {
+    const int row = ATTN_SLIDING_HKV * ATTN_SLIDING_D;
+    if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, ATTN_SLIDING_D, CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+    if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, ATTN_SLIDING_D, CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+    static bool smem_set[kMaxDevices] = {false};
+    if ((st = ensure_smem(pda::sliding::decode_kernel, pda::sliding::kSmemBytes, dev, smem_set))) return st;
+    const dim3 grid(plan.num_splits, ATTN_SLIDING_HKV, batch);
+    pda::sliding::decode_kernel<<<grid, pda::sliding::kThreads, pda::sliding::kSmemBytes, s>>>(tm_k, tm_v, p);
+    if (plan.num_splits > 1)
+      pda::combine_kernel<ATTN_SLIDING_D>
+          <<<dim3(ATTN_SLIDING_HQ, batch), ATTN_SLIDING_D / 4, 0, s>>>(p);
+  } else {
+    const int row = ATTN_GLOBAL_HKV * ATTN_GLOBAL_D;
+    if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
+    if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
+    static bool smem_set[kMaxDevices] = {false};
+    if ((st = ensure_smem(pda::global::decode_kernel, pda::global::kSmemBytes, dev, smem_set))) return st;
+    const dim3 grid(plan.num_splits, batch);
+    pda::global::decode_kernel<<<grid, pda::global::kThreads, pda::global::kSmemBytes, s>>>(tm_k, tm_v, p);
+    if (plan.num_splits > 1)
+      pda::combine_kernel<ATTN_GLOBAL_D><<<dim3(ATTN_GLOBAL_HQ, batch), ATTN_GLOBAL_D / 4, 0, s>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t attn_decode_sliding(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_table, const int32_t* seq_lens, void* o,
+                            int32_t batch, int32_t max_blocks, int64_t num_pages,
+                            int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                            int32_t num_splits, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream) {
+  return run_decode(ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, o, batch, max_blocks,
+                    num_pages, max_seq_len, window, out_dtype, num_splits, workspace, workspace_bytes,
+                    status, stream);
+}
+
+int32_t attn_decode_global(const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_table, const int32_t* seq_lens, void* o,
+                           int32_t batch, int32_t max_blocks, int64_t num_pages,
+                           int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                           int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           int32_t* status, void* stream) {
+  return run_decode(ATTN_KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, o, batch, max_blocks,
+                    num_pages, max_seq_len, window, out_dtype, num_splits, workspace, workspace_bytes,
+                    status, stream);
+}
+
+int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
+                         int32_t num_splits, int32_t num_sms, int32_t* out_num_splits,
+                         size_t* out_workspace_bytes) {
+  g_err[0] = '\0';
+  Plan plan;
+  const int32_t st = make_plan(kind, batch, max_seq_len, window, num_splits, num_sms, &plan);
+  if (st != ATTN_OK) return st;
+  if (out_num_splits) *out_num_splits = plan.num_splits;
+  if (out_workspace_bytes) *out_workspace_bytes = plan.workspace_bytes;
+  return ATTN_OK;
+}
+
+size_t attn_decode_workspace_size(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
+                                  int32_t num_splits) {
+  g_err[0] = '\0';
+  int dev = 0, num_sms = 0;
+  if (current_device(&dev, &num_sms) != ATTN_OK) return 0;
+  Plan plan;
+  if (make_plan(kind, batch, max_seq_len, window, num_splits, num_sms, &plan) != ATTN_OK) return 0;
+  return plan.workspace_bytes;
+}
+
+const char* attn_last_error(void) { return g_err; }
+
+int32_t attn_abi_version(void) { return ATTN_DECODE_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,280 @@
+// global.cuh -- split-KV decode kernel for the Gemma-4-12B global layers
+// (decodeGQA: 16 query heads over 1 KV head, D = 512, G = 16, scale 1).
+//
+// With G = 16 every K/V byte feeds 16 query heads (16 flop per byte), which
+// is more than the CUDA cores sustain at HBM speed, so both contractions run
+// on tensor cores (bf16 in, fp32 accumulate):
+//   S[h, l]  = sum_d q[h, d] K[l, d]     A = q (16 x 512), B = K^T per page
+//   O[h, d] += sum_l P[h, l] V[l, d]     A = P (16 x 16),  B = V per page
+//
+// One thread block per (split, sequence b):
+//   * warp 4 (producer) issues, per page, 8 TMA tensor copies for K and 8
+//     for V: boxes of 16 rows x 64 dims (2 KB) of the pool viewed as
+//     [num_pages*16 rows, 512], written with the 128-byte swizzle so that the
+//     ldmatrix reads below are free of bank conflicts;
+//   * warps 0..3 (consumers) each own 128 of the 512 dims: a warp computes
+//     its partial S over its dims, the four partials are summed through
+//     shared memory in a fixed order (so every warp holds the bitwise-same
+//     S), each warp runs the same online softmax, and accumulates P*V for its
+//     own 128 output dims.
+// Masking selects: logits of rows outside [lo, L) become -inf, and V rows
+// outside [lo, L) of a partial page are overwritten with zeros in shared
+// memory before the P*V product (0 * NaN would be NaN).
+#pragma once
+
+#include "common.cuh"
+
+namespace pda {
+namespace global {
+
+constexpr int kHq = ATTN_GLOBAL_HQ;  // 16
+constexpr int kD = ATTN_GLOBAL_D;    // 512
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDimsPerWarp = kD / kConsumerWarps;  // 128
+constexpr int kChunk = 64;                          // dims per TMA box (128-byte rows)
+constexpr int kChunks = kD / kChunk;                // 8
+constexpr int kChunkBytes = kPage * kChunk * 2;     // 2 KB
+constexpr int kPageBytes = kPage * kD * 2;          // 16 KB
+constexpr int kStages = 3;
+
+static_assert(kHq == 16, "the m16n8k16 tiling uses the 16 query heads as the M dimension");
+
+struct Smem {
+  alignas(1024) uint8_t k[kStages][kPageBytes];  // kChunks tiles of [16 rows][64 dims], swizzled
+  alignas(1024) uint8_t v[kStages][kPageBytes];
+  alignas(16) float xs[2][kConsumerWarps][32][8];  // partial-S exchange, double-buffered
+  alignas(8) uint64_t full[kStages];
+  alignas(8) uint64_t empty[kStages];
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
+
+// byte offset of 16-byte unit `unit` of row `row` in a 128B-swizzled [16][64] tile
+__device__ __forceinline__ uint32_t swz(int row, int unit) {
+  return row * 128 + ((unit ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int split = blockIdx.x;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const SplitRange r = split_range(p, b, split);
+  const int n_pages = r.page_end - r.page_begin;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tensor_map(&tm_k);
+      prefetch_tensor_map(&tm_v);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    produce_pages<kStages, 2 * kPageBytes>(p, b, r, s.full, s.empty, [&](int stage, int32_t y) {
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch)
+        tma_load_2d_hint(s.k[stage] + ch * kChunkBytes, &tm_k, ch * kChunk, y, &s.full[stage], policy);
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch)
+        tma_load_2d_hint(s.v[stage] + ch * kChunkBytes, &tm_v, ch * kChunk, y, &s.full[stage], policy);
+    });
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int g = lane >> 2;  // fragment row: query heads g and g + 8
+  const int t = lane & 3;   // fragment column pair
+  const int dim0 = warp * kDimsPerWarp;
+
+  // q as m16n8k16 A fragments over this warp's 128 dims (8 k-steps of 16)
+  uint32_t qa[8][4];
+  {
+    const uint32_t* q_g = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * kHq + g) * kD);
+    const uint32_t* q_g8 = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * kHq + g + 8) * kD);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d = dim0 + ks * 16 + 2 * t;
+      qa[ks][0] = __ldg(q_g + d / 2);
+      qa[ks][1] = __ldg(q_g8 + d / 2);
+      qa[ks][2] = __ldg(q_g + (d + 8) / 2);
+      qa[ks][3] = __ldg(q_g8 + (d + 8) / 2);
+    }
+  }
+
+  float m[2] = {-INFINITY, -INFINITY};  // rows g, g+8 (log2 units)
+  float l[2] = {0.f, 0.f};              // this thread's share of the row sums
+  float acc[16][4];                     // 16 n-tiles of 8 dims
+#pragma unroll
+  for (int n = 0; n < 16; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+
+  // ldmatrix lane roles
+  const int mi = lane >> 3;
+  const int lr = lane & 7;
+  bool ok = true;
+
+  for (int i = 0; i < n_pages; ++i) {
+    const int stage = i % kStages;
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kStages) & 1));
+      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+    }
+    const int pos0 = (r.page_begin + i) * kPage;
+    const uint32_t kst = smem_addr(s.k[stage]);
+    const uint32_t vst = smem_addr(s.v[stage]);
+
+    // ---- partial S over this warp's dims: two n-tiles of 8 positions ----
+    float sp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int ch = 2 * warp + (ks >> 2);
+      const int row = ((mi >> 1) << 3) + lr;
+      const int unit = 2 * (ks & 3) + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(kst + ch * kChunkBytes + swz(row, unit), b0, b1, b2, b3);
+      mma_bf16_16816(sp[0], qa[ks], b0, b1);
+      mma_bf16_16816(sp[1], qa[ks], b2, b3);
+    }
+
+    // ---- sum the four partials in a fixed order ----
+    const int buf = i & 1;
+    {
+      float4* dst = reinterpret_cast<float4*>(&s.xs[buf][warp][lane][0]);
+      dst[0] = make_float4(sp[0][0], sp[0][1], sp[0][2], sp[0][3]);
+      dst[1] = make_float4(sp[1][0], sp[1][1], sp[1][2], sp[1][3]);
+    }
+    named_barrier_sync(1, kConsumerWarps * 32);
+    float sc[2][4];
+    {
+      const float4* src = reinterpret_cast<const float4*>(&s.xs[buf][0][lane][0]);
+      float4 a0 = src[0], a1 = src[1];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) {
+        const float4* sw = reinterpret_cast<const float4*>(&s.xs[buf][w][lane][0]);
+        const float4 c0 = sw[0], c1 = sw[1];
+        a0.x += c0.x; a0.y += c0.y; a0.z += c0.z; a0.w += c0.w;
+        a1.x += c1.x; a1.y += c1.y; a1.z += c1.z; a1.w += c1.w;
+      }
+      sc[0][0] = a0.x; sc[0][1] = a0.y; sc[0][2] = a0.z; sc[0][3] = a0.w;
+      sc[1][0] = a1.x; sc[1][1] = a1.y; sc[1][2] = a1.z; sc[1][3] = a1.w;
+    }
+
+    // ---- masked online softmax (log2 units) ----
+    // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*t + (e&1)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int pos = pos0 + 8 * nt + 2 * t + (e & 1);
+        sc[nt][e] = (pos >= r.lo && pos < r.L) ? sc[nt][e] * kLog2e : -INFINITY;
+      }
+    float mx[2];
+    mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+    float m_use[2], scale[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+      const float m_new = fmaxf(m[rr], mx[rr]);
+      m_use[rr] = m_new == -INFINITY ? 0.f : m_new;
+      scale[rr] = exp2f(m[rr] - m_use[rr]);
+      m[rr] = m_new;
+    }
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(sc[nt][e] - m_use[e >> 1]);
+    l[0] = l[0] * scale[0] + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+    l[1] = l[1] * scale[1] + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      acc[n][0] *= scale[0];
+      acc[n][1] *= scale[0];
+      acc[n][2] *= scale[1];
+      acc[n][3] *= scale[1];
+    }
+    // P as the A fragment of one k16 step (k = the page's 16 positions)
+    const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
+                            pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
+
+    // ---- zero V rows outside [lo, L) in this warp's two chunks ----
+    if (pos0 < r.lo || pos0 + kPage > r.L) {
+#pragma unroll 1
+      for (int rr = 0; rr < kPage; ++rr) {
+        const int pos = pos0 + rr;
+        if ((pos < r.lo || pos >= r.L) && lane < 16) {
+          const int ch = 2 * warp + (lane >> 3);
+          st_shared_v4(vst + ch * kChunkBytes + rr * 128 + (lane & 7) * 16, make_uint4(0, 0, 0, 0));
+        }
+      }
+      fence_proxy_async_smem();  // before TMA rewrites this stage
+      __syncwarp();
+    }
+
+    // ---- O += P V over this warp's 128 dims ----
+#pragma unroll
+    for (int np = 0; np < 8; ++np) {
+      const int ch = 2 * warp + (np >> 2);
+      const int row = ((mi & 1) << 3) + lr;
+      const int unit = 2 * (np & 3) + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4_trans(vst + ch * kChunkBytes + swz(row, unit), b0, b1, b2, b3);
+      mma_bf16_16816(acc[2 * np], pa, b0, b1);
+      mma_bf16_16816(acc[2 * np + 1], pa, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[stage]);
+  }
+
+  // ---------------- epilogue ----------------
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+  }
+  const size_t row0 = static_cast<size_t>(b) * kHq + g;
+  const size_t row1 = row0 + 8;
+  if (p.num_splits == 1) {
+    const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
+    const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const int d = dim0 + 8 * n + 2 * t;
+      store_out2(p, row0 * kD + d, acc[n][0] * inv0, acc[n][1] * inv0);
+      store_out2(p, row1 * kD + d, acc[n][2] * inv1, acc[n][3] * inv1);
+    }
+  } else {
+    const size_t slot0 = row0 * p.num_splits + split;
+    const size_t slot1 = row1 * p.num_splits + split;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const int d = dim0 + 8 * n + 2 * t;
+      *reinterpret_cast<float2*>(p.part_o + slot0 * kD + d) = make_float2(acc[n][0], acc[n][1]);
+      *reinterpret_cast<float2*>(p.part_o + slot1 * kD + d) = make_float2(acc[n][2], acc[n][3]);
+    }
+    if (warp == 0 && t == 0) {
+      p.part_ml[slot0] = make_float2(m[0], l[0]);
+      p.part_ml[slot1] = make_float2(m[1], l[1]);
+    }
+  }
+}
+
+}  // namespace global
+}  // namespace pda

@@ -1,0 +1,276 @@
+// sliding.cuh -- split-KV decode kernel for the Gemma-4-12B sliding-window
+// layers (slidingDecodeGQA: 16 query heads over 8 KV heads, D = 256,
+// G = 2, scale 1), on CUDA cores.
+//
+// One thread block per (split, KV head c, sequence b) handles query heads
+// 2c and 2c+1 against the visible pages of its split:
+//   * warp 4 (producer) reads block-table entries and issues one 2-D TMA
+//     tensor copy per page for K and one for V: a 16-row x 256-column box
+//     (8 KB) of the pool viewed as [num_pages*16 rows, 8*256], so the
+//     KV-head slice of a page lands dense in shared memory;
+//   * warps 0..3 (consumers) each own 4 of the 16 rows of every page and run
+//     their own online softmax over them; lane j holds dims 8j..8j+7 of q,
+//     of the K row and of the output accumulator (packed fp32x2 FMAs);
+//   * after the last page the four warps' (max, sum, accumulator) are
+//     merged through shared memory and either written as o (one split) or
+//     as a partial (output, log-sum-exp) for the combine kernel.
+// Masking selects, never multiplies: rows outside [lo, L) get logit -inf
+// and their V row is skipped, so NaN in unused slots cannot leak.
+#pragma once
+
+#include "common.cuh"
+
+namespace pda {
+namespace sliding {
+
+constexpr int kHq = ATTN_SLIDING_HQ;    // 16
+constexpr int kHkv = ATTN_SLIDING_HKV;  // 8
+constexpr int kD = ATTN_SLIDING_D;      // 256
+constexpr int kG = kHq / kHkv;          // 2
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRowsPerWarp = kPage / kConsumerWarps;  // 4
+constexpr int kRowBytes = kD * 2;                      // 512
+constexpr int kTileBytes = kPage * kRowBytes;          // 8 KB per K (or V) page-head
+constexpr int kStages = 4;
+
+static_assert(kG == 2, "the lane mapping below assumes two query heads per KV head");
+
+struct Smem {
+  alignas(128) uint8_t k[kStages][kTileBytes];
+  alignas(128) uint8_t v[kStages][kTileBytes];
+  alignas(8) uint64_t full[kStages];
+  alignas(8) uint64_t empty[kStages];
+};
+// the post-loop merge reuses the K stages: [warps][G][D] accumulators + m, l
+static_assert(kStages * kTileBytes >= (kConsumerWarps * kG * kD + 4 * kConsumerWarps * kG) * 4,
+              "merge scratch does not fit");
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 128;  // + alignment slack
+
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+
+  const int split = blockIdx.x;
+  const int c = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const SplitRange r = split_range(p, b, split);
+  const int n_pages = r.page_end - r.page_begin;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tensor_map(&tm_k);
+      prefetch_tensor_map(&tm_v);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    const int x = c * kD;
+    produce_pages<kStages, 2 * kTileBytes>(p, b, r, s.full, s.empty, [&](int stage, int32_t y) {
+      tma_load_2d_hint(s.k[stage], &tm_k, x, y, &s.full[stage], policy);
+      tma_load_2d_hint(s.v[stage], &tm_v, x, y, &s.full[stage], policy);
+    });
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int hq0 = c * kG;
+  float2 qf[kG][4];
+#pragma unroll
+  for (int h = 0; h < kG; ++h) {
+    const uint4 w = ld_global_nc_v4(p.q + (static_cast<size_t>(b) * kHq + hq0 + h) * kD + 8 * lane);
+    qf[h][0] = bf16x2_to_float2(w.x);
+    qf[h][1] = bf16x2_to_float2(w.y);
+    qf[h][2] = bf16x2_to_float2(w.z);
+    qf[h][3] = bf16x2_to_float2(w.w);
+  }
+
+  float m[kG] = {-INFINITY, -INFINITY};  // running max (log2 units), same in every lane
+  float l[kG] = {0.f, 0.f};              // running sum, same in every lane
+  float2 acc[kG][4];
+#pragma unroll
+  for (int h = 0; h < kG; ++h)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[h][k] = make_float2(0.f, 0.f);
+
+  // after the reduce-scatter, lane holds the logit of (row r_mine, head h_mine)
+  const int j_mine = (lane >> 2) & 7;
+  const int r_mine = j_mine >> 1;
+  const int h_mine = j_mine & 1;
+  bool ok = true;
+
+  for (int i = 0; i < n_pages; ++i) {
+    const int stage = i % kStages;
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kStages) & 1));
+      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+    }
+    const int pos0 = (r.page_begin + i) * kPage + warp * kRowsPerWarp;
+    const uint32_t kbase = smem_addr(s.k[stage]) + warp * kRowsPerWarp * kRowBytes + lane * 16;
+    const uint32_t vbase = smem_addr(s.v[stage]) + warp * kRowsPerWarp * kRowBytes + lane * 16;
+
+    // partial logits over this lane's 8 dims: part[row*2 + head]
+    float part[8];
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const uint4 kw = ld_shared_v4(kbase + rr * kRowBytes);
+      const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
+      const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        float2 t = __fmul2_rn(qf[h][0], k0);
+        t = __ffma2_rn(qf[h][1], k1, t);
+        t = __ffma2_rn(qf[h][2], k2, t);
+        t = __ffma2_rn(qf[h][3], k3, t);
+        part[rr * 2 + h] = t.x + t.y;
+      }
+    }
+    // reduce-scatter over 32 lanes: 4 + 2 + 1 exchanges, then an all-reduce
+    // over the remaining 4-lane group
+    {
+      const bool up = lane & 16;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float send = up ? part[k] : part[k + 4];
+        const float keep = up ? part[k + 4] : part[k];
+        part[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+    }
+    {
+      const bool up = lane & 8;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float send = up ? part[k] : part[k + 2];
+        const float keep = up ? part[k + 2] : part[k];
+        part[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+    }
+    {
+      const bool up = lane & 4;
+      const float send = up ? part[0] : part[1];
+      const float keep = up ? part[1] : part[0];
+      part[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    part[0] += __shfl_xor_sync(0xffffffffu, part[0], 2);
+    part[0] += __shfl_xor_sync(0xffffffffu, part[0], 1);
+
+    // masked online softmax, in log2 units (exp(x) = exp2(x * log2 e))
+    const int pos_mine = pos0 + r_mine;
+    const bool vis_mine = pos_mine >= r.lo && pos_mine < r.L;
+    const float s2 = vis_mine ? part[0] * kLog2e : -INFINITY;
+    float pm = fmaxf(s2, __shfl_xor_sync(0xffffffffu, s2, 8));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));  // max over the 4 rows of head h_mine
+    const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 4);
+    const float page_max[kG] = {h_mine ? pm_other : pm, h_mine ? pm : pm_other};
+    float m_use[kG], scale[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      const float m_new = fmaxf(m[h], page_max[h]);
+      m_use[h] = m_new == -INFINITY ? 0.f : m_new;
+      scale[h] = exp2f(m[h] - m_use[h]);
+      m[h] = m_new;
+    }
+    const float pv = exp2f(s2 - (h_mine ? m_use[1] : m_use[0]));
+    float ps = pv + __shfl_xor_sync(0xffffffffu, pv, 8);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+    const float ps_other = __shfl_xor_sync(0xffffffffu, ps, 4);
+    l[0] = l[0] * scale[0] + (h_mine ? ps_other : ps);
+    l[1] = l[1] * scale[1] + (h_mine ? ps : ps_other);
+
+    float pj[8];  // probability of (row, head) j = row*2 + head; lanes 4j..4j+3 hold it
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pj[j] = __shfl_sync(0xffffffffu, pv, 4 * j);
+
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      const float2 sc = make_float2(scale[h], scale[h]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[h][k] = __fmul2_rn(acc[h][k], sc);
+    }
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const int pos = pos0 + rr;
+      if (pos >= r.lo && pos < r.L) {  // warp-uniform
+        const uint4 vw = ld_shared_v4(vbase + rr * kRowBytes);
+        const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
+        const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          const float2 pp = make_float2(pj[rr * 2 + h], pj[rr * 2 + h]);
+          acc[h][0] = __ffma2_rn(pp, v0, acc[h][0]);
+          acc[h][1] = __ffma2_rn(pp, v1, acc[h][1]);
+          acc[h][2] = __ffma2_rn(pp, v2, acc[h][2]);
+          acc[h][3] = __ffma2_rn(pp, v3, acc[h][3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[stage]);
+  }
+
+  // ---------------- merge the four warps ----------------
+  named_barrier_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse K stages as scratch
+  float* mo = reinterpret_cast<float*>(&s.k[0][0]);    // [warp][h][D]
+  float* mm = mo + kConsumerWarps * kG * kD;           // [warp][h]
+  float* ml = mm + kConsumerWarps * kG;                // [warp][h]
+#pragma unroll
+  for (int h = 0; h < kG; ++h) {
+    float4* dst = reinterpret_cast<float4*>(mo + (warp * kG + h) * kD + 8 * lane);
+    dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+    dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      mm[warp * kG + h] = m[h];
+      ml[warp * kG + h] = l[h];
+    }
+  }
+  named_barrier_sync(1, kConsumerWarps * 32);
+
+  const int t = threadIdx.x;        // 0..127: 2 heads x 64 groups of 4 dims
+  const int h = t >> 6;
+  const int d0 = (t & 63) * 4;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * kG + h]);
+  float Lsum = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = exp2f(mm[w * kG + h] - M);
+      Lsum += f * ml[w * kG + h];
+      const float4 a = *reinterpret_cast<const float4*>(mo + (w * kG + h) * kD + d0);
+      O.x += f * a.x;
+      O.y += f * a.y;
+      O.z += f * a.z;
+      O.w += f * a.w;
+    }
+  }
+  const size_t row = static_cast<size_t>(b) * kHq + hq0 + h;
+  if (p.num_splits == 1) {
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    store_out4(p, row * kD + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+  } else {
+    const size_t slot = row * p.num_splits + split;
+    *reinterpret_cast<float4*>(p.part_o + slot * kD + d0) = O;
+    if (d0 == 0) p.part_ml[slot] = make_float2(M, Lsum);
+  }
+}
+
+}  // namespace sliding
+}  // namespace pda

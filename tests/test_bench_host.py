@@ -1,0 +1,91 @@
+"""Host logic of bench.py, without a GPU: byte model, L2 rotation, and the
+multi-rank aggregation (world size 2 over gloo on the CPU)."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_algorithmic_bytes_per_position():
+    # sliding: 8 KV heads x 256 dims x 2 bytes x (K and V) = 8192 bytes per visible position
+    assert bench.algorithmic_bytes("sliding", [1], 1024) - bench.algorithmic_bytes("sliding", [0], 1024) == 8192
+    # global: 1 x 512 x 2 x 2 = 2048 bytes per position
+    assert bench.algorithmic_bytes("global", [10], 0) - bench.algorithmic_bytes("global", [9], 0) == 2048
+    # the window caps the visible positions
+    assert bench.algorithmic_bytes("sliding", [5000], 1024) == bench.algorithmic_bytes("sliding", [1024], 1024)
+    # q and o: B x 16 x D x 2 bytes each (bf16 out)
+    assert bench.algorithmic_bytes("global", [0, 0], 0) == 2 * 16 * 512 * 2 * 2
+
+
+def test_rotation_exceeds_l2():
+    n = bench.rotation_count(67 * 10**6)
+    assert n * 67 * 10**6 > 3 * bench.L2_BYTES
+    assert bench.rotation_count(4 * 10**9) == 1
+
+
+def test_aggregate_single_rank():
+    line = bench.aggregate([{"bytes": 2e9, "ms": 1000.0, "calls": 10}], 10, 3, 1, {"workload": "x"})
+    assert line["value"] == 2.0 and line["unit"] == "GB/s" and line["calls_per_s"] == 10.0
+    assert line["ms_per_step"] == 100.0 and line["higher_is_better"] is True
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench as b
+    r, w, lr = b.init_dist()
+    b.setup_pg(w, "gloo")
+    res = {"bytes": 1e9 * (rank + 1), "ms": 100.0 * (rank + 1), "calls": 5}
+    b.barrier(w)
+    allres = b.gather_results(res, w)
+    if r == 0:
+        q.put(b.aggregate(allres, 5, 3, w, {"workload": "x"}))
+    b._PG.destroy_process_group()
+
+
+def test_two_rank_aggregation_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    line = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # bytes of both ranks over the slowest rank's time: 3e9 B / 0.2 s = 15 GB/s
+    assert line["value"] == 15.0
+    assert line["n_gpus"] == 2 and line["scaling"] == "weak"
+    assert line["calls_per_s"] == 50.0
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "0", "--config", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

@@ -1,0 +1,141 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares,
+plans splits by plain arithmetic, and rejects bad arguments before launching.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_decode_attention_gb300 as pda
+from paged_decode_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pda.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_operations():
+    names = declared_functions()
+    for n in ("attn_decode_sliding", "attn_decode_global", "attn_decode_plan",
+              "attn_decode_workspace_size", "attn_last_error", "attn_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), "symbol %s declared in attn_decode.h but not exported" % n
+
+
+def test_binding_covers_the_exports(lib):
+    assert set(pda.EXPORTS) <= set(declared_functions())
+
+
+def test_abi_version(lib):
+    assert lib.attn_abi_version() == 1
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "attn_decode.h"\nint main(void){return ATTN_OK;}\n')
+    import subprocess
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-c", str(src), "-o", str(tmp_path / "use.o")], check=True)
+
+
+# ---------------------------------------------------------------------------
+# split plan (pure host arithmetic)
+# ---------------------------------------------------------------------------
+
+def test_plan_no_split_when_units_fill_the_gpu(lib):
+    # 256 sequences x 8 KV heads = 2048 blocks >= 3 per SM x 152
+    assert pda.attn_decode_plan(pda.KIND_SLIDING, 256, 32768, 1024) == (1, 0)
+
+
+def test_plan_splits_small_batches(lib):
+    ns, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 4, 1100, 1024)
+    assert ns > 1
+    assert ws >= 4 * 16 * ns * 256 * 4 + 4 * 16 * ns * 8
+    ns, ws = pda.attn_decode_plan(pda.KIND_GLOBAL, 4, 262144, 0)
+    assert ns >= 76  # fills 2 blocks x 152 SMs
+    assert ws >= 4 * 16 * ns * 512 * 4
+
+
+def test_plan_respects_forced_splits_and_page_count(lib):
+    ns, _ = pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0, num_splits=7)
+    assert ns == 5  # 10 pages: 7 requested -> 2 pages per split -> 5 splits
+    ns, _ = pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0, num_splits=1)
+    assert ns == 1
+    ns, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 2, 0, 1024)
+    assert (ns, ws) == (1, 0)
+    # a window bounds the pages of a sliding unit at ceil(w/16)+1
+    ns, _ = pda.attn_decode_plan(pda.KIND_SLIDING, 1, 262144, 1024, num_splits=1000)
+    assert ns == 65
+
+
+def test_plan_rejects_bad_arguments(lib):
+    with pytest.raises(pda.AttnDecodeError):
+        pda.attn_decode_plan(7, 1, 16, 0)
+    with pytest.raises(pda.AttnDecodeError):
+        pda.attn_decode_plan(pda.KIND_GLOBAL, 0, 16, 0)
+    with pytest.raises(pda.AttnDecodeError):
+        pda.attn_decode_plan(pda.KIND_GLOBAL, 1, 16, 0, num_sms=0)
+
+
+# ---------------------------------------------------------------------------
+# host validation: returns an error code and launches nothing
+# ---------------------------------------------------------------------------
+
+FAKE = 1 << 20  # an aligned, never dereferenced address
+
+
+def call(lib, name="attn_decode_sliding", **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, o=FAKE, batch=4, max_blocks=70,
+             num_pages=300, max_seq_len=1100, window=1024, out_dtype=0, num_splits=0,
+             ws=None, ws_bytes=0, status=None, stream=None)
+    a.update(kw)
+    fn = getattr(lib, name)
+    return fn(a["q"], a["k"], a["v"], a["bt"], a["sl"], a["o"], a["batch"], a["max_blocks"],
+              a["num_pages"], a["max_seq_len"], a["window"], a["out_dtype"], a["num_splits"],
+              a["ws"], a["ws_bytes"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("name", ["attn_decode_sliding", "attn_decode_global"])
+@pytest.mark.parametrize("bad,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(bt=None), 1), (dict(sl=None), 1),
+    (dict(o=None), 1), (dict(q=FAKE + 8), 1), (dict(o=FAKE + 2), 1), (dict(status=FAKE + 2), 1),
+    (dict(batch=0), 1), (dict(batch=257), 2), (dict(max_blocks=0), 1), (dict(num_pages=0), 1),
+    (dict(num_pages=1 << 27), 2), (dict(max_seq_len=-1), 1), (dict(max_seq_len=70 * 16 + 1), 1),
+    (dict(max_blocks=20000, max_seq_len=262145), 2), (dict(out_dtype=2), 1), (dict(num_splits=-1), 1),
+])
+def test_invalid_arguments_are_rejected_before_launch(lib, name, bad, code):
+    assert call(lib, name, **bad) == code
+    assert pda.attn_last_error() != ""
+
+
+def test_sliding_requires_a_positive_window(lib):
+    assert call(lib, "attn_decode_sliding", window=0) == 1
+    assert call(lib, "attn_decode_sliding", window=-5) == 1
+    assert "window" in pda.attn_last_error()
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 16, 256, dtype=torch.bfloat16)
+    pool = torch.zeros(2, 16, 8, 256, dtype=torch.bfloat16)
+    bt = torch.zeros(1, 1, dtype=torch.int32)
+    sl = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        pda.attn_decode_sliding(q, pool, pool, bt, sl)

@@ -253,10 +253,13 @@ def config_seq_lens(cfg, variant=None):
     raise ValueError("unknown workload %r" % (cfg,))
 
 
-def config_case(cfg, device="cpu", variant=None, layer=0, poison=True):
-    """One call of workload `cfg`.  For cfg 5, `layer` picks the layer (0..47)."""
+def config_case(cfg, device="cpu", variant=None, layer=0, poison=True, seed_offset=0):
+    """One call of workload `cfg`.  For cfg 5, `layer` picks the layer (0..47).
+
+    seed_offset draws a different cache and query with the same lengths (the
+    benchmark's rotating input sets)."""
     L = config_seq_lens(cfg, variant)
-    seed = 1000 * cfg + layer
+    seed = 1000 * cfg + layer + seed_offset
     if cfg == 1:
         return make_case("sliding", L, seed, device, poison=poison)
     if cfg == 2:
