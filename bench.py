@@ -41,6 +41,7 @@ METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and attention cal
 UNIT = "GB/s"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 
 
 # ---------------------------------------------------------------------------
@@ -218,7 +219,7 @@ def run_ours(args, rank, world, local_rank):
         pl = []
         for c in cs:
             kind = pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL
-            ws_bytes = pda.attn_decode_workspace_size(kind, c.B, c.max_seq_len, c.window)
+            ws_bytes = pda.attn_decode_workspace_size(kind, c.B, c.max_seq_len, c.window, NUM_SPLITS)
             ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
             o = torch.empty((c.B, c.Hq, c.D), dtype=torch.bfloat16, device=dev)
             pl.append((c, ws, o))
@@ -229,14 +230,11 @@ def run_ours(args, rank, world, local_rank):
         for c, ws, o in pl:
             fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
             fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
-               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream)
+               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
+               num_splits=NUM_SPLITS)
 
-    kernels_per_call = []
-    for c in calls0:
-        kind = pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL
-        ns, _ = pda.attn_decode_plan(kind, c.B, c.max_seq_len, c.window,
-                                     num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
-        kernels_per_call.append(2 if ns > 1 else 1)
+    # every call launches the decode kernel and its combine kernel
+    kernels_per_call = [2 for _ in calls0]
 
     # warm-up (direct calls), then capture one rotation as a graph
     with torch.cuda.stream(stream):
@@ -303,7 +301,8 @@ def run_ours(args, rank, world, local_rank):
             c, ws, o = plans[i % n_sets][heavy]
             fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
             fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
-               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream)
+               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
+               num_splits=NUM_SPLITS)
         e1.record(stream)
     e1.synchronize()
     heavy_ms = e0.elapsed_time(e1) / reps
@@ -342,7 +341,8 @@ def run_e2e(args, plans, n_sets, stream, status, dev):
             c.seq_lens.copy_(slh, non_blocking=True)
             fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
             fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
-               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream)
+               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
+               num_splits=NUM_SPLITS)
             oh.copy_(o, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -485,7 +485,11 @@ def main(argv=None):
     ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4b", "5"])
     ap.add_argument("--no-graph", action="store_true", help="launch every call directly (no CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="thread blocks per KV head (0 = the library's automatic plan)")
     args = ap.parse_args(argv)
+    global NUM_SPLITS
+    NUM_SPLITS = args.num_splits
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = init_dist()

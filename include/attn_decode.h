@@ -108,17 +108,21 @@ extern "C" {
  * batch        1..256
  * max_blocks   >= 1, width of block_table
  * num_pages    >= 1, pages in each pool; num_pages*16 < 2^31
- * max_seq_len  host-side upper bound on seq_lens (0..max_blocks*16), used only
- *              to plan the split of the sequence across thread blocks; a
- *              smaller value than the true maximum is still computed
- *              correctly, only more slowly
+ * max_seq_len  host-side upper bound on seq_lens (0..max_blocks*16); it only
+ *              caps how many thread blocks are launched for small problems
+ *              and never changes which positions are read
  * window       > 0; the node's value is 1024
  * out_dtype    ATTN_OUT_BF16 or ATTN_OUT_F32
- * num_splits   0 = choose automatically; > 0 forces that many KV splits per
- *              (sequence, KV head) (clamped to the pages a split can hold)
+ * num_splits   0 = automatic (one wave of resident thread blocks); > 0 forces
+ *              that many thread blocks per KV head (at most 1024).  The
+ *              visible pages of all sequences, concatenated, are cut into
+ *              that many equal spans; a sequence cut by a span boundary is
+ *              finished by a second kernel that merges the partial softmax
+ *              results.  The result does not depend on this value beyond
+ *              floating-point regrouping.
  * workspace    device scratch of at least attn_decode_workspace_size(...)
- *              bytes (may be NULL when that size is 0); contents need no
- *              initialisation; must not be shared by calls that overlap
+ *              bytes for those partial results; contents need no
+ *              initialisation; must not be shared by calls that may overlap
  * status       optional device int32 for ATTN_DEV_* bits, or NULL
  * stream       cudaStream_t, as void*
  * returns      ATTN_OK or ATTN_ERR_*
@@ -153,7 +157,7 @@ int32_t attn_decode_global(const void* q, const void* k_pool, const void* v_pool
  * kind         ATTN_KIND_SLIDING or ATTN_KIND_GLOBAL
  * batch, max_seq_len, window, num_splits   as for the operations
  * num_sms      streaming multiprocessors of the target device (>= 1)
- * out_num_splits        receives the KV splits per (sequence, KV head)
+ * out_num_splits        receives the thread blocks per KV head (see num_splits)
  * out_workspace_bytes   receives the workspace size the operation requires
  * returns      ATTN_OK or ATTN_ERR_INVALID_ARG
  */
@@ -164,8 +168,7 @@ int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32
 /*
  * attn_decode_workspace_size -- attn_decode_plan's workspace size for the
  * current CUDA device.  Returns 0 (and sets attn_last_error) on bad
- * arguments or when no device can be queried; 0 is also the valid size of a
- * call that needs no workspace, so check attn_last_error() when in doubt.
+ * arguments or when no device can be queried.
  */
 size_t attn_decode_workspace_size(int32_t kind, int32_t batch, int32_t max_seq_len,
                                   int32_t window, int32_t num_splits);

@@ -31,67 +31,61 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ---------------------------------------------------------------------------
-// Split plan: how many thread blocks share one (sequence, KV head) unit.
+// Launch plan: how many thread blocks share the pages of one KV head.
 //
-// A unit's visible pages are cut into num_splits runs.  More splits fill the
-// 152 SMs when there are few units (small batch, long sequences); fewer keep
-// the partial-result traffic (one fp32 [Hq_per_unit, D] row per split) and
-// the combine launch off the critical path.  Resident blocks per SM follow
-// from the kernels' shared memory: 3 for the sliding kernel (~66 KB each),
-// 2 for the global kernel (~106 KB each).
+// The decode kernels cut the concatenated visible pages of all sequences
+// into grid_x equal spans (the balanced schedule in common.cuh), so grid_x
+// only has to fill the GPU once: one wave of resident blocks, 3 per SM for
+// the sliding kernel (~75 KB of shared memory each, 8 KV-head columns) and
+// 2 per SM for the global kernel (~107 KB each).  max_seq_len bounds the
+// total pages, so small problems launch fewer blocks; it never changes
+// which positions are read.  The workspace holds one partial row per
+// (block, sequence) pair that a span boundary can cut: grid_x + batch slots.
 // ---------------------------------------------------------------------------
 struct Plan {
-  int num_splits;
-  int pages_per_split;
+  int grid_x;
+  int min_pages;
   size_t part_o_bytes;
   size_t workspace_bytes;
 };
 
 int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
-                  int32_t forced_splits, int32_t num_sms, Plan* out) {
+                  int32_t forced_blocks, int32_t num_sms, Plan* out) {
   if (kind != ATTN_KIND_SLIDING && kind != ATTN_KIND_GLOBAL)
     return fail(ATTN_ERR_INVALID_ARG, "unknown kind %d", kind);
   if (batch < 1) return fail(ATTN_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", batch);
   if (max_seq_len < 0) return fail(ATTN_ERR_INVALID_ARG, "max_seq_len must be >= 0");
-  if (forced_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (forced_blocks < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
   if (num_sms < 1) return fail(ATTN_ERR_INVALID_ARG, "num_sms must be >= 1");
   const bool sliding = kind == ATTN_KIND_SLIDING;
   const int D = sliding ? ATTN_SLIDING_D : ATTN_GLOBAL_D;
   const int Hq = sliding ? ATTN_SLIDING_HQ : ATTN_GLOBAL_HQ;
-  const int units = sliding ? batch * ATTN_SLIDING_HKV : batch;
-  const int blocks_per_sm = sliding ? 3 : 2;
-  const int min_pages = sliding ? 4 : 8;
+  const int columns = sliding ? ATTN_SLIDING_HKV : 1;
+  const int blocks_per_sm = sliding ? pda::sliding::kBlocksPerSm : pda::global::kBlocksPerSm;
+  const int min_pages = sliding ? pda::sliding::kMinPages : pda::global::kMinPages;
 
-  int max_pages = (max_seq_len + ATTN_PAGE_SIZE - 1) / ATTN_PAGE_SIZE;
+  // visible pages of one sequence, at most
+  int64_t max_pages = (max_seq_len + ATTN_PAGE_SIZE - 1) / ATTN_PAGE_SIZE;
   if (window > 0) {
-    const int wpages = (window + ATTN_PAGE_SIZE - 1) / ATTN_PAGE_SIZE + 1;
+    const int64_t wpages = (window + ATTN_PAGE_SIZE - 1) / ATTN_PAGE_SIZE + 1;
     if (wpages < max_pages) max_pages = wpages;
   }
-  int ns = 1;
-  if (max_pages > 0) {
-    if (forced_splits > 0) {
-      ns = forced_splits;
-    } else {
-      const int slots = num_sms * blocks_per_sm;
-      ns = (slots + units - 1) / units;
-      const int cap = max_pages / min_pages > 1 ? max_pages / min_pages : 1;
-      if (ns > cap) ns = cap;
-    }
-    if (ns > max_pages) ns = max_pages;
-    if (ns < 1) ns = 1;
-  }
-  const int pps = max_pages > 0 ? (max_pages + ns - 1) / ns : 1;
-  if (max_pages > 0) ns = (max_pages + pps - 1) / pps;
-  out->num_splits = ns;
-  out->pages_per_split = pps;
-  if (ns > 1) {
-    const size_t rows = static_cast<size_t>(batch) * Hq * ns;
-    out->part_o_bytes = align256(rows * D * sizeof(float));
-    out->workspace_bytes = out->part_o_bytes + align256(rows * sizeof(float2));
+  const int64_t total_max = max_pages * batch;
+  int64_t gx;
+  if (forced_blocks > 0) {
+    gx = forced_blocks;
   } else {
-    out->part_o_bytes = 0;
-    out->workspace_bytes = 0;
+    gx = static_cast<int64_t>(num_sms) * blocks_per_sm / columns;
+    const int64_t useful = (total_max + min_pages - 1) / min_pages;
+    if (gx > useful) gx = useful;
   }
+  if (gx > pda::kMaxSplits) gx = pda::kMaxSplits;
+  if (gx < 1) gx = 1;
+  out->grid_x = static_cast<int>(gx);
+  out->min_pages = min_pages;
+  const size_t rows = (static_cast<size_t>(gx) + batch) * Hq;
+  out->part_o_bytes = align256(rows * D * sizeof(float));
+  out->workspace_bytes = out->part_o_bytes + align256(rows * sizeof(float2));
   return ATTN_OK;
 }
 
@@ -158,6 +152,26 @@ int32_t ensure_smem(Kernel kernel, size_t bytes, int dev, bool* done) {
   return ATTN_OK;
 }
 
+// The combine grid is a programmatic dependent of the decode grid: it may be
+// scheduled while the decode kernel runs (which calls
+// griddepcontrol.launch_dependents at entry) and waits in
+// griddepcontrol.wait for the decode grid's results, so its launch latency
+// overlaps the decode kernel instead of following it.
+template <typename Kernel>
+cudaError_t launch_combine(Kernel kernel, dim3 grid, int threads, cudaStream_t s, const pda::DecodeParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // ---------------------------------------------------------------------------
 // Common validation + launch
 // ---------------------------------------------------------------------------
@@ -203,56 +217,51 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
   Plan plan;
   st = make_plan(kind, batch, max_seq_len, window, num_splits, num_sms, &plan);
   if (st != ATTN_OK) return st;
-  if (plan.workspace_bytes > 0) {
-    if (!workspace || workspace_bytes < plan.workspace_bytes)
-      return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes required (got %zu)", name,
-                  plan.workspace_bytes, workspace ? workspace_bytes : size_t{0});
-    if (!aligned16(workspace)) return fail(ATTN_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
-  }
+  if (!workspace || workspace_bytes < plan.workspace_bytes)
+    return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes required (got %zu)", name,
+                plan.workspace_bytes, workspace ? workspace_bytes : size_t{0});
+  if (!aligned16(workspace)) return fail(ATTN_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
 
   pda::DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.o = o;
-  p.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
-  p.part_ml = plan.workspace_bytes
-                  ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + plan.part_o_bytes)
-                  : nullptr;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + plan.part_o_bytes);
   p.status = status;
   p.num_pages = num_pages;
   p.batch = batch;
   p.max_blocks = max_blocks;
   p.window = window;
-  p.num_splits = plan.num_splits;
-  p.pages_per_split = plan.pages_per_split;
+  p.grid_x = plan.grid_x;
+  p.min_pages = plan.min_pages;
   p.out_f32 = out_dtype == ATTN_OUT_F32;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tm_k, tm_v;
+  cudaError_t e;
   if (sliding) {
     const int row = ATTN_SLIDING_HKV * ATTN_SLIDING_D;
     if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, ATTN_SLIDING_D, CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, ATTN_SLIDING_D, CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     static bool smem_set[kMaxDevices] = {false};
     if ((st = ensure_smem(pda::sliding::decode_kernel, pda::sliding::kSmemBytes, dev, smem_set))) return st;
-    const dim3 grid(plan.num_splits, ATTN_SLIDING_HKV, batch);
+    const dim3 grid(plan.grid_x, ATTN_SLIDING_HKV);
     pda::sliding::decode_kernel<<<grid, pda::sliding::kThreads, pda::sliding::kSmemBytes, s>>>(tm_k, tm_v, p);
-    if (plan.num_splits > 1)
-      pda::combine_kernel<ATTN_SLIDING_D>
-          <<<dim3(ATTN_SLIDING_HQ, batch), ATTN_SLIDING_D / 4, 0, s>>>(p);
+    e = launch_combine(pda::combine_kernel<ATTN_SLIDING_D>,
+                       dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), 32, s, p);
   } else {
     const int row = ATTN_GLOBAL_HKV * ATTN_GLOBAL_D;
     if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
     if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
     static bool smem_set[kMaxDevices] = {false};
     if ((st = ensure_smem(pda::global::decode_kernel, pda::global::kSmemBytes, dev, smem_set))) return st;
-    const dim3 grid(plan.num_splits, batch);
-    pda::global::decode_kernel<<<grid, pda::global::kThreads, pda::global::kSmemBytes, s>>>(tm_k, tm_v, p);
-    if (plan.num_splits > 1)
-      pda::combine_kernel<ATTN_GLOBAL_D><<<dim3(ATTN_GLOBAL_HQ, batch), ATTN_GLOBAL_D / 4, 0, s>>>(p);
+    pda::global::decode_kernel<<<plan.grid_x, pda::global::kThreads, pda::global::kSmemBytes, s>>>(tm_k, tm_v, p);
+    e = launch_combine(pda::combine_kernel<ATTN_GLOBAL_D>,
+                       dim3(ATTN_GLOBAL_HQ * (ATTN_GLOBAL_D / pda::kCombineCols), batch), 32, s, p);
   }
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
   return ATTN_OK;
 }
@@ -290,7 +299,7 @@ int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32
   Plan plan;
   const int32_t st = make_plan(kind, batch, max_seq_len, window, num_splits, num_sms, &plan);
   if (st != ATTN_OK) return st;
-  if (out_num_splits) *out_num_splits = plan.num_splits;
+  if (out_num_splits) *out_num_splits = plan.grid_x;
   if (out_workspace_bytes) *out_workspace_bytes = plan.workspace_bytes;
   return ATTN_OK;
 }

@@ -1,5 +1,5 @@
-// common.cuh -- launch parameters and the per-(sequence, split) visible range
-// shared by the decode kernels.
+// common.cuh -- launch parameters, the balanced page schedule and the TMA
+// page producer shared by the decode kernels.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -10,7 +10,9 @@
 
 namespace pda {
 
-constexpr int kPage = ATTN_PAGE_SIZE;       // token rows per cache page
+constexpr int kPage = ATTN_PAGE_SIZE;  // token rows per cache page
+constexpr int kMaxBatch = ATTN_MAX_BATCH;
+constexpr int kMaxSplits = 1024;       // blocks per KV head the host plan may launch
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -18,56 +20,110 @@ struct DecodeParams {
   const int32_t* block_table;  // [batch, max_blocks]
   const int32_t* seq_lens;     // [batch]
   void* o;                     // [batch, Hq, D], bf16 or fp32
-  float* part_o;               // [batch, Hq, num_splits, D]  (num_splits > 1)
-  float2* part_ml;             // [batch, Hq, num_splits]: (running max in log2 units, sum)
+  float* part_o;               // [grid_x + batch, Hq, D]: partial outputs, slot = block + sequence
+  float2* part_ml;             // [grid_x + batch, Hq]: (running max in log2 units, sum)
   int32_t* status;             // optional ATTN_DEV_* word
   int64_t num_pages;
   int32_t batch;
   int32_t max_blocks;
   int32_t window;              // > 0 sliding rule, <= 0 none
-  int32_t num_splits;
-  int32_t pages_per_split;
+  int32_t grid_x;              // blocks sharing the pages of one KV head
+  int32_t min_pages;           // smallest span a block is given
   int32_t out_f32;
 };
 
-// Visible positions [lo, L) of sequence b and the page range [page_begin,
-// page_end) of one split.  Decode query at p = L-1 (Attention.lean
-// decodeGQA); with a window w the visible keys are p-w < l <= p
-// (Attention.lean slidingGQA).  Splits cut the visible pages into runs of
-// pages_per_split, counted from the first visible page; the last split takes
-// whatever remains, so an understated max_seq_len costs speed, not results.
-struct SplitRange {
-  int L;
-  int lo;
-  int page_begin;
-  int page_end;
+// ---------------------------------------------------------------------------
+// Balanced schedule.
+//
+// Sequence b's visible positions are [lo_b, L_b) with the query at
+// p = L_b - 1 (Attention.lean decodeGQA) and, for a window w, lo_b =
+// max(0, L_b - w) (Attention.lean slidingGQA: p - w < l <= p).  They occupy
+// logical pages lo_b/16 .. (L_b-1)/16.  Concatenating every sequence's
+// visible pages gives N pages; block g of grid_x takes the contiguous span
+// [g*per, min((g+1)*per, N)) with per = max(min_pages, ceil(N / grid_x)), so
+// every block streams the same number of pages whatever the mix of
+// lengths.  A sequence that lies inside one span is finished by that block;
+// one that straddles spans leaves a partial result in slot (block + b), an
+// injective numbering because spans and sequences are both in order, and
+// the combine kernel merges them.
+// ---------------------------------------------------------------------------
+struct SeqTable {
+  int32_t prefix[kMaxBatch + 1];  // prefix[b] = visible pages of sequences < b
+  int32_t len[kMaxBatch];         // L_b, clamped to [0, max_blocks*16]
 };
 
-__device__ __forceinline__ SplitRange split_range(const DecodeParams& p, int b, int split) {
-  SplitRange r;
-  int L = p.seq_lens[b];
-  const int L_cap = p.max_blocks * kPage;
-  if (L < 0 || L > L_cap) {
-    if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
-    L = L < 0 ? 0 : L_cap;
-  }
-  r.L = L;
-  r.lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
-  r.page_begin = r.page_end = 0;
-  if (L > 0) {
-    const int first = r.lo / kPage;
-    const int last = (L - 1) / kPage;  // inclusive
-    const int begin = first + split * p.pages_per_split;
-    int end = (split == p.num_splits - 1) ? last + 1 : begin + p.pages_per_split;
-    if (end > last + 1) end = last + 1;
-    if (begin <= last) {
-      r.page_begin = begin;
-      r.page_end = end;
-    }
-  }
-  return r;
+__device__ __forceinline__ int first_visible(int L, int window) {
+  return (window > 0 && L > window) ? L - window : 0;
 }
 
+__device__ __forceinline__ int visible_pages(int L, int window) {
+  return L > 0 ? (L - 1) / kPage - first_visible(L, window) / kPage + 1 : 0;
+}
+
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int L, bool report_it) {
+  const int cap = p.max_blocks * kPage;
+  if (L < 0 || L > cap) {
+    if (report_it) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
+    return L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+// Fills the table; called by every thread of the block (contains __syncthreads).
+__device__ __forceinline__ void build_seq_table(const DecodeParams& p, SeqTable& t) {
+  const int tid = threadIdx.x;
+  for (int b = tid; b < p.batch; b += blockDim.x) t.len[b] = clamp_len(p, p.seq_lens[b], true);
+  __syncthreads();
+  if (tid < 32) {
+    int carry = 0;
+    if (tid == 0) t.prefix[0] = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      const int b = b0 + tid;
+      int v = b < p.batch ? visible_pages(t.len[b], p.window) : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (tid >= o) v += u;
+      }
+      if (b < p.batch) t.prefix[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// The sequence holding flattened page f: the largest b < batch with prefix[b] <= f.
+__device__ __forceinline__ int seq_of(const SeqTable& t, int batch, int f) {
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.prefix[mid] <= f) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Span {
+  int begin, end;  // flattened pages of this block
+};
+
+__device__ __forceinline__ int span_pages(int total, int grid_x, int min_pages) {
+  const int per = (total + grid_x - 1) / grid_x;
+  return per > min_pages ? per : min_pages;
+}
+
+__device__ __forceinline__ Span block_span(const DecodeParams& p, const SeqTable& t, int g) {
+  const int total = t.prefix[p.batch];
+  const int per = span_pages(total, p.grid_x, p.min_pages);
+  Span s;
+  const long long b0 = static_cast<long long>(g) * per;
+  s.begin = b0 < total ? static_cast<int>(b0) : total;
+  s.end = s.begin + per < total ? s.begin + per : total;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// Output stores
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, float4 v) {
   if (p.out_f32) {
     *reinterpret_cast<float4*>(static_cast<float*>(p.o) + idx) = v;
@@ -87,29 +143,36 @@ __device__ __forceinline__ void store_out2(const DecodeParams& p, size_t idx, fl
   }
 }
 
-// Producer side of the page pipeline, run by one whole warp: walks the pages
-// of a split, reads their block-table entries 32 at a time (one coalesced
-// load per 32 pages, fetched a batch ahead), and has lane 0 issue the TMA
-// copies `issue(stage, y)` for page row coordinate y.  A page id outside
+// ---------------------------------------------------------------------------
+// Producer side of the page pipeline, run by one whole warp.  Walks the
+// block's span of flattened pages, reads their block-table entries 32 at a
+// time (one entry per lane, fetched a batch ahead), and has lane 0 issue the
+// TMA copies `issue(stage, y)` for page row coordinate y.  A page id outside
 // [0, num_pages) is replaced by a fully out-of-range coordinate, which the
 // copy engine fills with zeros, and ATTN_DEV_BAD_PAGE is raised.  Before it
 // returns, the warp waits (bounded) until every copy it issued has landed,
 // so no copy is in flight when the block retires.
+// ---------------------------------------------------------------------------
 template <int kStages, int kTxBytes, typename Issue>
-__device__ __forceinline__ void produce_pages(const DecodeParams& p, int b, const SplitRange& r,
+__device__ __forceinline__ void produce_pages(const DecodeParams& p, const SeqTable& t, const Span& sp,
                                               uint64_t* full, uint64_t* empty, Issue issue) {
   const int lane = threadIdx.x & 31;
-  const int n_pages = r.page_end - r.page_begin;
-  const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.max_blocks + r.page_begin;
-  int nxt = lane < n_pages ? bt[lane] : 0;
+  const int n_pages = sp.end - sp.begin;
+  auto entry = [&](int i) -> int {
+    if (i >= n_pages) return 0;
+    const int f = sp.begin + i;
+    const int b = seq_of(t, p.batch, f);
+    const int lp = first_visible(t.len[b], p.window) / kPage + (f - t.prefix[b]);
+    return p.block_table[static_cast<int64_t>(b) * p.max_blocks + lp];
+  };
+  int nxt = entry(lane);
   int cur = 0;
   int issued = 0;
   bool ok = true;
   for (int i = 0; i < n_pages; ++i) {
     if ((i & 31) == 0) {
       cur = nxt;
-      const int j = i + 32 + lane;
-      nxt = j < n_pages ? bt[j] : 0;
+      nxt = entry(i + 32 + lane);
     }
     const int phys = __shfl_sync(0xffffffffu, cur, i & 31);
     const int stage = i % kStages;
@@ -142,6 +205,50 @@ __device__ __forceinline__ void produce_pages(const DecodeParams& p, int b, cons
       if (!mbar_wait(&full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     }
   }
+}
+
+// Consumer-side walk over the span: which sequence the current page belongs
+// to, its first position, and whether it closes a segment (the last page of
+// its sequence inside this span).
+struct PageCursor {
+  int b;        // current sequence
+  int L, lo;    // its visible positions [lo, L)
+  int seg_end;  // flattened index one past its last page in this span
+
+  __device__ __forceinline__ void start(const DecodeParams& p, const SeqTable& t, const Span& sp) {
+    b = seq_of(t, p.batch, sp.begin);
+    load(p, t, sp);
+  }
+  __device__ __forceinline__ void load(const DecodeParams& p, const SeqTable& t, const Span& sp) {
+    L = t.len[b];
+    lo = first_visible(L, p.window);
+    seg_end = t.prefix[b + 1] < sp.end ? t.prefix[b + 1] : sp.end;
+  }
+  // position of row 0 of flattened page f (f within sequence b)
+  __device__ __forceinline__ int pos0(const SeqTable& t, int f) const {
+    return (lo / kPage + (f - t.prefix[b])) * kPage;
+  }
+  // move to the sequence of flattened page f (skipping empty sequences)
+  __device__ __forceinline__ void advance(const DecodeParams& p, const SeqTable& t, const Span& sp, int f) {
+    if (f >= t.prefix[b + 1]) {
+      do { ++b; } while (f >= t.prefix[b + 1]);
+      load(p, t, sp);
+    }
+  }
+  // true when this block holds every visible page of sequence b
+  __device__ __forceinline__ bool whole(const SeqTable& t, const Span& sp) const {
+    return t.prefix[b] >= sp.begin && t.prefix[b + 1] <= sp.end;
+  }
+};
+
+// Lets the dependent (combine) grid launch while this grid runs.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grid this one depends on has completed and its writes are visible.
+__device__ __forceinline__ void wait_for_primary_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace pda

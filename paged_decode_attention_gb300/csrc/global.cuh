@@ -1,13 +1,14 @@
-// global.cuh -- split-KV decode kernel for the Gemma-4-12B global layers
-// (decodeGQA: 16 query heads over 1 KV head, D = 512, G = 16, scale 1).
+// global.cuh -- decode kernel for the Gemma-4-12B global layers (decodeGQA:
+// 16 query heads over 1 KV head, D = 512, G = 16, scale 1).
 //
-// With G = 16 every K/V byte feeds 16 query heads (16 flop per byte), which
-// is more than the CUDA cores sustain at HBM speed, so both contractions run
-// on tensor cores (bf16 in, fp32 accumulate):
+// With G = 16 every K/V byte feeds 16 query heads (16 flop per byte), more
+// than the CUDA cores sustain at HBM speed, so both contractions run on
+// tensor cores (bf16 in, fp32 accumulate):
 //   S[h, l]  = sum_d q[h, d] K[l, d]     A = q (16 x 512), B = K^T per page
 //   O[h, d] += sum_l P[h, l] V[l, d]     A = P (16 x 16),  B = V per page
 //
-// One thread block per (split, sequence b):
+// Grid (grid_x): block g streams its span of the flattened visible pages
+// (balanced schedule, common.cuh):
 //   * warp 4 (producer) issues, per page, 8 TMA tensor copies for K and 8
 //     for V: boxes of 16 rows x 64 dims (2 KB) of the pool viewed as
 //     [num_pages*16 rows, 512], written with the 128-byte swizzle so that the
@@ -16,7 +17,8 @@
 //     its partial S over its dims, the four partials are summed through
 //     shared memory in a fixed order (so every warp holds the bitwise-same
 //     S), each warp runs the same online softmax, and accumulates P*V for its
-//     own 128 output dims.
+//     own 128 output dims; since all warps share (max, sum), each writes its
+//     slice of o (or of the partial) with no further merge.
 // Masking selects: logits of rows outside [lo, L) become -inf, and V rows
 // outside [lo, L) of a partial page are overwritten with zeros in shared
 // memory before the P*V product (0 * NaN would be NaN).
@@ -37,13 +39,16 @@ constexpr int kChunks = kD / kChunk;                // 8
 constexpr int kChunkBytes = kPage * kChunk * 2;     // 2 KB
 constexpr int kPageBytes = kPage * kD * 2;          // 16 KB
 constexpr int kStages = 3;
+constexpr int kBlocksPerSm = 2;
+constexpr int kMinPages = 4;
 
 static_assert(kHq == 16, "the m16n8k16 tiling uses the 16 query heads as the M dimension");
 
 struct Smem {
   alignas(1024) uint8_t k[kStages][kPageBytes];  // kChunks tiles of [16 rows][64 dims], swizzled
   alignas(1024) uint8_t v[kStages][kPageBytes];
-  alignas(16) float xs[2][kConsumerWarps][32][8];  // partial-S exchange, double-buffered
+  alignas(16) float4 xs[2][kConsumerWarps][2][32];  // partial-S exchange, double-buffered
+  SeqTable table;
   alignas(8) uint64_t full[kStages];
   alignas(8) uint64_t empty[kStages];
 };
@@ -61,13 +66,11 @@ __global__ void __launch_bounds__(kThreads)
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int split = blockIdx.x;
-  const int b = blockIdx.y;
+  const int gb = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SplitRange r = split_range(p, b, split);
-  const int n_pages = r.page_end - r.page_begin;
 
+  allow_dependent_launch();
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
@@ -75,7 +78,11 @@ __global__ void __launch_bounds__(kThreads)
     }
     fence_mbar_init();
   }
-  __syncthreads();
+  build_seq_table(p, s.table);  // ends with __syncthreads
+  const SeqTable& t = s.table;
+  const Span sp = block_span(p, t, gb);
+  const int n_pages = sp.end - sp.begin;
+  if (n_pages <= 0) return;
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kThreads)
       prefetch_tensor_map(&tm_v);
     }
     const uint64_t policy = l2_policy_evict_first();
-    produce_pages<kStages, 2 * kPageBytes>(p, b, r, s.full, s.empty, [&](int stage, int32_t y) {
+    produce_pages<kStages, 2 * kPageBytes>(p, t, sp, s.full, s.empty, [&](int stage, int32_t y) {
 #pragma unroll
       for (int ch = 0; ch < kChunks; ++ch)
         tma_load_2d_hint(s.k[stage] + ch * kChunkBytes, &tm_k, ch * kChunk, y, &s.full[stage], policy);
@@ -97,49 +104,60 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---------------- consumers ----------------
   const int g = lane >> 2;  // fragment row: query heads g and g + 8
-  const int t = lane & 3;   // fragment column pair
+  const int tq = lane & 3;  // fragment column pair
   const int dim0 = warp * kDimsPerWarp;
+  const int mi = lane >> 3;  // ldmatrix: which 8x8 matrix this lane addresses
+  const int lr = lane & 7;
+
+  PageCursor cur;
+  cur.start(p, t, sp);
 
   // q as m16n8k16 A fragments over this warp's 128 dims (8 k-steps of 16)
   uint32_t qa[8][4];
-  {
-    const uint32_t* q_g = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * kHq + g) * kD);
-    const uint32_t* q_g8 = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * kHq + g + 8) * kD);
+  auto load_q = [&]() {
+    const uint32_t* q_g = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(cur.b) * kHq + g) * kD);
+    const uint32_t* q_g8 = q_g + 8 * kD / 2;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int d = dim0 + ks * 16 + 2 * t;
+      const int d = dim0 + ks * 16 + 2 * tq;
       qa[ks][0] = __ldg(q_g + d / 2);
       qa[ks][1] = __ldg(q_g8 + d / 2);
       qa[ks][2] = __ldg(q_g + (d + 8) / 2);
       qa[ks][3] = __ldg(q_g8 + (d + 8) / 2);
     }
-  }
+  };
+  load_q();
 
-  float m[2] = {-INFINITY, -INFINITY};  // rows g, g+8 (log2 units)
-  float l[2] = {0.f, 0.f};              // this thread's share of the row sums
-  float acc[16][4];                     // 16 n-tiles of 8 dims
+  float m[2], l[2];  // rows g, g+8: running max (log2 units), this thread's share of the sum
+  float acc[16][4];  // 16 n-tiles of 8 dims
+  auto reset = [&]() {
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
 #pragma unroll
-  for (int n = 0; n < 16; ++n)
+    for (int n = 0; n < 16; ++n)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-
-  // ldmatrix lane roles
-  const int mi = lane >> 3;
-  const int lr = lane & 7;
+      for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+  };
+  reset();
   bool ok = true;
 
   for (int i = 0; i < n_pages; ++i) {
+    const int f = sp.begin + i;
+    if (f >= t.prefix[cur.b + 1]) {
+      cur.advance(p, t, sp, f);
+      load_q();
+    }
     const int stage = i % kStages;
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kStages) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     }
-    const int pos0 = (r.page_begin + i) * kPage;
+    const int pos0 = cur.pos0(t, f);
     const uint32_t kst = smem_addr(s.k[stage]);
     const uint32_t vst = smem_addr(s.v[stage]);
 
     // ---- partial S over this warp's dims: two n-tiles of 8 positions ----
-    float sp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float sp_[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int ch = 2 * warp + (ks >> 2);
@@ -147,26 +165,21 @@ __global__ void __launch_bounds__(kThreads)
       const int unit = 2 * (ks & 3) + (mi & 1);
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4(kst + ch * kChunkBytes + swz(row, unit), b0, b1, b2, b3);
-      mma_bf16_16816(sp[0], qa[ks], b0, b1);
-      mma_bf16_16816(sp[1], qa[ks], b2, b3);
+      mma_bf16_16816(sp_[0], qa[ks], b0, b1);
+      mma_bf16_16816(sp_[1], qa[ks], b2, b3);
     }
 
     // ---- sum the four partials in a fixed order ----
     const int buf = i & 1;
-    {
-      float4* dst = reinterpret_cast<float4*>(&s.xs[buf][warp][lane][0]);
-      dst[0] = make_float4(sp[0][0], sp[0][1], sp[0][2], sp[0][3]);
-      dst[1] = make_float4(sp[1][0], sp[1][1], sp[1][2], sp[1][3]);
-    }
+    s.xs[buf][warp][0][lane] = make_float4(sp_[0][0], sp_[0][1], sp_[0][2], sp_[0][3]);
+    s.xs[buf][warp][1][lane] = make_float4(sp_[1][0], sp_[1][1], sp_[1][2], sp_[1][3]);
     named_barrier_sync(1, kConsumerWarps * 32);
     float sc[2][4];
     {
-      const float4* src = reinterpret_cast<const float4*>(&s.xs[buf][0][lane][0]);
-      float4 a0 = src[0], a1 = src[1];
+      float4 a0 = s.xs[buf][0][0][lane], a1 = s.xs[buf][0][1][lane];
 #pragma unroll
       for (int w = 1; w < kConsumerWarps; ++w) {
-        const float4* sw = reinterpret_cast<const float4*>(&s.xs[buf][w][lane][0]);
-        const float4 c0 = sw[0], c1 = sw[1];
+        const float4 c0 = s.xs[buf][w][0][lane], c1 = s.xs[buf][w][1][lane];
         a0.x += c0.x; a0.y += c0.y; a0.z += c0.z; a0.w += c0.w;
         a1.x += c1.x; a1.y += c1.y; a1.z += c1.z; a1.w += c1.w;
       }
@@ -175,13 +188,13 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---- masked online softmax (log2 units) ----
-    // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*t + (e&1)
+    // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*tq + (e&1)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int pos = pos0 + 8 * nt + 2 * t + (e & 1);
-        sc[nt][e] = (pos >= r.lo && pos < r.L) ? sc[nt][e] * kLog2e : -INFINITY;
+        const int pos = pos0 + 8 * nt + 2 * tq + (e & 1);
+        sc[nt][e] = (pos >= cur.lo && pos < cur.L) ? sc[nt][e] * kLog2e : -INFINITY;
       }
     float mx[2];
     mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
@@ -215,11 +228,11 @@ __global__ void __launch_bounds__(kThreads)
                             pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
 
     // ---- zero V rows outside [lo, L) in this warp's two chunks ----
-    if (pos0 < r.lo || pos0 + kPage > r.L) {
+    if (pos0 < cur.lo || pos0 + kPage > cur.L) {
 #pragma unroll 1
       for (int rr = 0; rr < kPage; ++rr) {
         const int pos = pos0 + rr;
-        if ((pos < r.lo || pos >= r.L) && lane < 16) {
+        if ((pos < cur.lo || pos >= cur.L) && lane < 16) {
           const int ch = 2 * warp + (lane >> 3);
           st_shared_v4(vst + ch * kChunkBytes + rr * 128 + (lane & 7) * 16, make_uint4(0, 0, 0, 0));
         }
@@ -241,37 +254,40 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[stage]);
-  }
 
-  // ---------------- epilogue ----------------
+    if (f + 1 == cur.seg_end) {
+      // ---------------- finish this sequence's segment ----------------
+      float lt[2];
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
-    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
-  }
-  const size_t row0 = static_cast<size_t>(b) * kHq + g;
-  const size_t row1 = row0 + 8;
-  if (p.num_splits == 1) {
-    const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
-    const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+      for (int rr = 0; rr < 2; ++rr) {
+        lt[rr] = l[rr] + __shfl_xor_sync(0xffffffffu, l[rr], 1);
+        lt[rr] += __shfl_xor_sync(0xffffffffu, lt[rr], 2);
+      }
+      if (cur.whole(t, sp)) {
+        const size_t row0 = static_cast<size_t>(cur.b) * kHq + g;
+        const float inv0 = lt[0] > 0.f ? 1.f / lt[0] : 0.f;
+        const float inv1 = lt[1] > 0.f ? 1.f / lt[1] : 0.f;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int d = dim0 + 8 * n + 2 * t;
-      store_out2(p, row0 * kD + d, acc[n][0] * inv0, acc[n][1] * inv0);
-      store_out2(p, row1 * kD + d, acc[n][2] * inv1, acc[n][3] * inv1);
-    }
-  } else {
-    const size_t slot0 = row0 * p.num_splits + split;
-    const size_t slot1 = row1 * p.num_splits + split;
+        for (int n = 0; n < 16; ++n) {
+          const int d = dim0 + 8 * n + 2 * tq;
+          store_out2(p, row0 * kD + d, acc[n][0] * inv0, acc[n][1] * inv0);
+          store_out2(p, (row0 + 8) * kD + d, acc[n][2] * inv1, acc[n][3] * inv1);
+        }
+      } else {
+        const size_t slot0 = (static_cast<size_t>(gb) + cur.b) * kHq + g;
+        const size_t slot1 = slot0 + 8;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int d = dim0 + 8 * n + 2 * t;
-      *reinterpret_cast<float2*>(p.part_o + slot0 * kD + d) = make_float2(acc[n][0], acc[n][1]);
-      *reinterpret_cast<float2*>(p.part_o + slot1 * kD + d) = make_float2(acc[n][2], acc[n][3]);
-    }
-    if (warp == 0 && t == 0) {
-      p.part_ml[slot0] = make_float2(m[0], l[0]);
-      p.part_ml[slot1] = make_float2(m[1], l[1]);
+        for (int n = 0; n < 16; ++n) {
+          const int d = dim0 + 8 * n + 2 * tq;
+          *reinterpret_cast<float2*>(p.part_o + slot0 * kD + d) = make_float2(acc[n][0], acc[n][1]);
+          *reinterpret_cast<float2*>(p.part_o + slot1 * kD + d) = make_float2(acc[n][2], acc[n][3]);
+        }
+        if (warp == 0 && tq == 0) {
+          p.part_ml[slot0] = make_float2(m[0], lt[0]);
+          p.part_ml[slot1] = make_float2(m[1], lt[1]);
+        }
+      }
+      reset();
     }
   }
 }

@@ -1,19 +1,20 @@
-// sliding.cuh -- split-KV decode kernel for the Gemma-4-12B sliding-window
-// layers (slidingDecodeGQA: 16 query heads over 8 KV heads, D = 256,
-// G = 2, scale 1), on CUDA cores.
+// sliding.cuh -- decode kernel for the Gemma-4-12B sliding-window layers
+// (slidingDecodeGQA: 16 query heads over 8 KV heads, D = 256, G = 2,
+// scale 1), on CUDA cores.
 //
-// One thread block per (split, KV head c, sequence b) handles query heads
-// 2c and 2c+1 against the visible pages of its split:
+// Grid (grid_x, 8): column c serves KV head c (query heads 2c, 2c+1); block
+// g of a column streams its span of the flattened visible pages (see the
+// balanced schedule in common.cuh):
 //   * warp 4 (producer) reads block-table entries and issues one 2-D TMA
 //     tensor copy per page for K and one for V: a 16-row x 256-column box
 //     (8 KB) of the pool viewed as [num_pages*16 rows, 8*256], so the
 //     KV-head slice of a page lands dense in shared memory;
 //   * warps 0..3 (consumers) each own 4 of the 16 rows of every page and run
 //     their own online softmax over them; lane j holds dims 8j..8j+7 of q,
-//     of the K row and of the output accumulator (packed fp32x2 FMAs);
-//   * after the last page the four warps' (max, sum, accumulator) are
-//     merged through shared memory and either written as o (one split) or
-//     as a partial (output, log-sum-exp) for the combine kernel.
+//     of the K/V rows and of the output accumulator (packed fp32x2 FMAs);
+//   * when a sequence's pages in the span end, the four warps' (max, sum,
+//     accumulator) are merged through shared memory and written as o (the
+//     span holds the whole sequence) or as a partial for the combine kernel.
 // Masking selects, never multiplies: rows outside [lo, L) get logit -inf
 // and their V row is skipped, so NaN in unused slots cannot leak.
 #pragma once
@@ -33,18 +34,21 @@ constexpr int kRowsPerWarp = kPage / kConsumerWarps;  // 4
 constexpr int kRowBytes = kD * 2;                      // 512
 constexpr int kTileBytes = kPage * kRowBytes;          // 8 KB per K (or V) page-head
 constexpr int kStages = 4;
+constexpr int kBlocksPerSm = 3;
+constexpr int kMinPages = 4;
 
 static_assert(kG == 2, "the lane mapping below assumes two query heads per KV head");
 
 struct Smem {
   alignas(128) uint8_t k[kStages][kTileBytes];
   alignas(128) uint8_t v[kStages][kTileBytes];
+  alignas(16) float merge_o[kConsumerWarps][kG][kD];
+  float merge_m[kConsumerWarps][kG];
+  float merge_l[kConsumerWarps][kG];
+  SeqTable table;
   alignas(8) uint64_t full[kStages];
   alignas(8) uint64_t empty[kStages];
 };
-// the post-loop merge reuses the K stages: [warps][G][D] accumulators + m, l
-static_assert(kStages * kTileBytes >= (kConsumerWarps * kG * kD + 4 * kConsumerWarps * kG) * 4,
-              "merge scratch does not fit");
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 128;  // + alignment slack
 
@@ -54,14 +58,12 @@ __global__ void __launch_bounds__(kThreads)
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
-  const int split = blockIdx.x;
+  const int g = blockIdx.x;
   const int c = blockIdx.y;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SplitRange r = split_range(p, b, split);
-  const int n_pages = r.page_end - r.page_begin;
 
+  allow_dependent_launch();
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
@@ -69,7 +71,11 @@ __global__ void __launch_bounds__(kThreads)
     }
     fence_mbar_init();
   }
-  __syncthreads();
+  build_seq_table(p, s.table);  // ends with __syncthreads
+  const SeqTable& t = s.table;
+  const Span sp = block_span(p, t, g);
+  const int n_pages = sp.end - sp.begin;
+  if (n_pages <= 0) return;
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
@@ -79,7 +85,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     const uint64_t policy = l2_policy_evict_first();
     const int x = c * kD;
-    produce_pages<kStages, 2 * kTileBytes>(p, b, r, s.full, s.empty, [&](int stage, int32_t y) {
+    produce_pages<kStages, 2 * kTileBytes>(p, t, sp, s.full, s.empty, [&](int stage, int32_t y) {
       tma_load_2d_hint(s.k[stage], &tm_k, x, y, &s.full[stage], policy);
       tma_load_2d_hint(s.v[stage], &tm_v, x, y, &s.full[stage], policy);
     });
@@ -88,37 +94,52 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---------------- consumers ----------------
   const int hq0 = c * kG;
-  float2 qf[kG][4];
-#pragma unroll
-  for (int h = 0; h < kG; ++h) {
-    const uint4 w = ld_global_nc_v4(p.q + (static_cast<size_t>(b) * kHq + hq0 + h) * kD + 8 * lane);
-    qf[h][0] = bf16x2_to_float2(w.x);
-    qf[h][1] = bf16x2_to_float2(w.y);
-    qf[h][2] = bf16x2_to_float2(w.z);
-    qf[h][3] = bf16x2_to_float2(w.w);
-  }
-
-  float m[kG] = {-INFINITY, -INFINITY};  // running max (log2 units), same in every lane
-  float l[kG] = {0.f, 0.f};              // running sum, same in every lane
-  float2 acc[kG][4];
-#pragma unroll
-  for (int h = 0; h < kG; ++h)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[h][k] = make_float2(0.f, 0.f);
-
   // after the reduce-scatter, lane holds the logit of (row r_mine, head h_mine)
   const int j_mine = (lane >> 2) & 7;
   const int r_mine = j_mine >> 1;
   const int h_mine = j_mine & 1;
+
+  PageCursor cur;
+  cur.start(p, t, sp);
+  float2 qf[kG][4];
+  auto load_q = [&]() {
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      const uint4 w = ld_global_nc_v4(p.q + (static_cast<size_t>(cur.b) * kHq + hq0 + h) * kD + 8 * lane);
+      qf[h][0] = bf16x2_to_float2(w.x);
+      qf[h][1] = bf16x2_to_float2(w.y);
+      qf[h][2] = bf16x2_to_float2(w.z);
+      qf[h][3] = bf16x2_to_float2(w.w);
+    }
+  };
+  load_q();
+
+  float m[kG], l[kG];  // running max (log2 units) and sum, identical in every lane
+  float2 acc[kG][4];
+  auto reset = [&]() {
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[h][k] = make_float2(0.f, 0.f);
+    }
+  };
+  reset();
   bool ok = true;
 
   for (int i = 0; i < n_pages; ++i) {
+    const int f = sp.begin + i;
+    if (f >= t.prefix[cur.b + 1]) {
+      cur.advance(p, t, sp, f);
+      load_q();
+    }
     const int stage = i % kStages;
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kStages) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     }
-    const int pos0 = (r.page_begin + i) * kPage + warp * kRowsPerWarp;
+    const int pos0 = cur.pos0(t, f) + warp * kRowsPerWarp;
     const uint32_t kbase = smem_addr(s.k[stage]) + warp * kRowsPerWarp * kRowBytes + lane * 16;
     const uint32_t vbase = smem_addr(s.v[stage]) + warp * kRowsPerWarp * kRowBytes + lane * 16;
 
@@ -131,11 +152,11 @@ __global__ void __launch_bounds__(kThreads)
       const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
-        float2 t = __fmul2_rn(qf[h][0], k0);
-        t = __ffma2_rn(qf[h][1], k1, t);
-        t = __ffma2_rn(qf[h][2], k2, t);
-        t = __ffma2_rn(qf[h][3], k3, t);
-        part[rr * 2 + h] = t.x + t.y;
+        float2 u = __fmul2_rn(qf[h][0], k0);
+        u = __ffma2_rn(qf[h][1], k1, u);
+        u = __ffma2_rn(qf[h][2], k2, u);
+        u = __ffma2_rn(qf[h][3], k3, u);
+        part[rr * 2 + h] = u.x + u.y;
       }
     }
     // reduce-scatter over 32 lanes: 4 + 2 + 1 exchanges, then an all-reduce
@@ -169,7 +190,7 @@ __global__ void __launch_bounds__(kThreads)
 
     // masked online softmax, in log2 units (exp(x) = exp2(x * log2 e))
     const int pos_mine = pos0 + r_mine;
-    const bool vis_mine = pos_mine >= r.lo && pos_mine < r.L;
+    const bool vis_mine = pos_mine >= cur.lo && pos_mine < cur.L;
     const float s2 = vis_mine ? part[0] * kLog2e : -INFINITY;
     float pm = fmaxf(s2, __shfl_xor_sync(0xffffffffu, s2, 8));
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));  // max over the 4 rows of head h_mine
@@ -203,7 +224,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int pos = pos0 + rr;
-      if (pos >= r.lo && pos < r.L) {  // warp-uniform
+      if (pos >= cur.lo && pos < cur.L) {  // warp-uniform
         const uint4 vw = ld_shared_v4(vbase + rr * kRowBytes);
         const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
         const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
@@ -219,56 +240,55 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[stage]);
-  }
 
-  // ---------------- merge the four warps ----------------
-  named_barrier_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse K stages as scratch
-  float* mo = reinterpret_cast<float*>(&s.k[0][0]);    // [warp][h][D]
-  float* mm = mo + kConsumerWarps * kG * kD;           // [warp][h]
-  float* ml = mm + kConsumerWarps * kG;                // [warp][h]
+    if (f + 1 == cur.seg_end) {
+      // ---------------- finish this sequence's segment ----------------
 #pragma unroll
-  for (int h = 0; h < kG; ++h) {
-    float4* dst = reinterpret_cast<float4*>(mo + (warp * kG + h) * kD + 8 * lane);
-    dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
-    dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
-  }
-  if (lane == 0) {
+      for (int h = 0; h < kG; ++h) {
+        float4* dst = reinterpret_cast<float4*>(&s.merge_o[warp][h][8 * lane]);
+        dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+        dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+      }
+      if (lane == 0) {
 #pragma unroll
-    for (int h = 0; h < kG; ++h) {
-      mm[warp * kG + h] = m[h];
-      ml[warp * kG + h] = l[h];
+        for (int h = 0; h < kG; ++h) {
+          s.merge_m[warp][h] = m[h];
+          s.merge_l[warp][h] = l[h];
+        }
+      }
+      named_barrier_sync(1, kConsumerWarps * 32);
+      const int tt = threadIdx.x;  // 0..127: 2 heads x 64 groups of 4 dims
+      const int h = tt >> 6;
+      const int d0 = (tt & 63) * 4;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s.merge_m[w][h]);
+      float Lsum = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float fw = exp2f(s.merge_m[w][h] - M);
+          Lsum += fw * s.merge_l[w][h];
+          const float4 a = *reinterpret_cast<const float4*>(&s.merge_o[w][h][d0]);
+          O.x += fw * a.x;
+          O.y += fw * a.y;
+          O.z += fw * a.z;
+          O.w += fw * a.w;
+        }
+      }
+      if (cur.whole(t, sp)) {
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const size_t row = static_cast<size_t>(cur.b) * kHq + hq0 + h;
+        store_out4(p, row * kD + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+      } else {
+        const size_t slot = (static_cast<size_t>(g) + cur.b) * kHq + hq0 + h;
+        *reinterpret_cast<float4*>(p.part_o + slot * kD + d0) = O;
+        if (d0 == 0) p.part_ml[slot] = make_float2(M, Lsum);
+      }
+      named_barrier_sync(1, kConsumerWarps * 32);  // merge buffers free again
+      reset();
     }
-  }
-  named_barrier_sync(1, kConsumerWarps * 32);
-
-  const int t = threadIdx.x;        // 0..127: 2 heads x 64 groups of 4 dims
-  const int h = t >> 6;
-  const int d0 = (t & 63) * 4;
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * kG + h]);
-  float Lsum = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = exp2f(mm[w * kG + h] - M);
-      Lsum += f * ml[w * kG + h];
-      const float4 a = *reinterpret_cast<const float4*>(mo + (w * kG + h) * kD + d0);
-      O.x += f * a.x;
-      O.y += f * a.y;
-      O.z += f * a.z;
-      O.w += f * a.w;
-    }
-  }
-  const size_t row = static_cast<size_t>(b) * kHq + hq0 + h;
-  if (p.num_splits == 1) {
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    store_out4(p, row * kD + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
-  } else {
-    const size_t slot = row * p.num_splits + split;
-    *reinterpret_cast<float4*>(p.part_o + slot * kD + d0) = O;
-    if (d0 == 0) p.part_ml[slot] = make_float2(M, Lsum);
   }
 }
 

@@ -59,30 +59,40 @@ def test_header_compiles_as_c(tmp_path):
 # split plan (pure host arithmetic)
 # ---------------------------------------------------------------------------
 
-def test_plan_no_split_when_units_fill_the_gpu(lib):
-    # 256 sequences x 8 KV heads = 2048 blocks >= 3 per SM x 152
-    assert pda.attn_decode_plan(pda.KIND_SLIDING, 256, 32768, 1024) == (1, 0)
+def _workspace(gx, batch, D):
+    def a256(x):
+        return (x + 255) // 256 * 256
+    rows = (gx + batch) * 16
+    return a256(rows * D * 4) + a256(rows * 8)
 
 
-def test_plan_splits_small_batches(lib):
-    ns, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 4, 1100, 1024)
-    assert ns > 1
-    assert ws >= 4 * 16 * ns * 256 * 4 + 4 * 16 * ns * 8
-    ns, ws = pda.attn_decode_plan(pda.KIND_GLOBAL, 4, 262144, 0)
-    assert ns >= 76  # fills 2 blocks x 152 SMs
-    assert ws >= 4 * 16 * ns * 512 * 4
+def test_plan_fills_one_wave(lib):
+    # sliding: 3 blocks per SM x 152 SMs over 8 KV-head columns; global: 2 per SM
+    gx, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 256, 32768, 1024)
+    assert gx == 152 * 3 // 8
+    assert ws == _workspace(gx, 256, 256)
+    gx, ws = pda.attn_decode_plan(pda.KIND_GLOBAL, 4, 262144, 0)
+    assert gx == 304
+    assert ws == _workspace(304, 4, 512)
 
 
-def test_plan_respects_forced_splits_and_page_count(lib):
-    ns, _ = pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0, num_splits=7)
-    assert ns == 5  # 10 pages: 7 requested -> 2 pages per split -> 5 splits
-    ns, _ = pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0, num_splits=1)
-    assert ns == 1
-    ns, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 2, 0, 1024)
-    assert (ns, ws) == (1, 0)
-    # a window bounds the pages of a sliding unit at ceil(w/16)+1
-    ns, _ = pda.attn_decode_plan(pda.KIND_SLIDING, 1, 262144, 1024, num_splits=1000)
-    assert ns == 65
+def test_plan_small_problems_launch_fewer_blocks(lib):
+    # 2 sequences of at most 10 pages, 4 pages per block at least -> 5 blocks
+    gx, _ = pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0)
+    assert gx == 5
+    # a window bounds a sequence's visible pages at ceil(w/16) + 1 = 65
+    gx, _ = pda.attn_decode_plan(pda.KIND_SLIDING, 1, 262144, 1024)
+    assert gx == 17  # ceil(65 / 4)
+    gx, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 2, 0, 1024)
+    assert gx == 1 and ws == _workspace(1, 2, 256)
+
+
+def test_plan_respects_forced_block_counts(lib):
+    assert pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0, num_splits=7)[0] == 7
+    assert pda.attn_decode_plan(pda.KIND_GLOBAL, 2, 160, 0, num_splits=1)[0] == 1
+    assert pda.attn_decode_plan(pda.KIND_SLIDING, 1, 262144, 1024, num_splits=1000)[0] == 1000
+    # the combine kernel merges at most 1024 partials per row
+    assert pda.attn_decode_plan(pda.KIND_GLOBAL, 1, 262144, 0, num_splits=5000)[0] == 1024
 
 
 def test_plan_rejects_bad_arguments(lib):
