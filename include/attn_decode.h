@@ -81,6 +81,7 @@ extern "C" {
 #define ATTN_DEV_WAIT_TIMEOUT 1 /* a copy-pipeline wait exceeded its time limit     */
 #define ATTN_DEV_BAD_PAGE 2     /* visible position mapped to page id not in [0,num_pages) */
 #define ATTN_DEV_BAD_SEQ_LEN 4  /* seq_lens[b] < 0 or > max_blocks*16 (clamped)      */
+#define ATTN_DEV_INTERNAL 8     /* an internal index check failed; the access was skipped */
 
 /* Fixed shapes of the two operations (Gemma-4-12B model page, attn.core rows). */
 #define ATTN_SLIDING_HQ 16

@@ -29,7 +29,7 @@ ERROR_NAMES = {1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ER
                4: "ATTN_ERR_CUDA"}
 OUT_BF16, OUT_F32 = 0, 1
 KIND_SLIDING, KIND_GLOBAL = 0, 1
-DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN = 1, 2, 4
+DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN, DEV_INTERNAL = 1, 2, 4, 8
 PAGE_SIZE = 16
 SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
 

@@ -236,6 +236,8 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
   p.window = window;
   p.grid_x = plan.grid_x;
   p.min_pages = plan.min_pages;
+  p.part_rows = (static_cast<int64_t>(plan.grid_x) + batch) *
+                (sliding ? ATTN_SLIDING_HQ : ATTN_GLOBAL_HQ);
   p.out_f32 = out_dtype == ATTN_OUT_F32;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -61,6 +61,10 @@ __global__ void __launch_bounds__(32) combine_kernel(const __grid_constant__ Dec
   const int g1 = (before + mine - 1) / per;
   if (g0 == g1) return;  // one block held the whole sequence and wrote o
   const int ns = g1 - g0 + 1;
+  if (ns > kMaxSplits || (static_cast<int64_t>(g1) + b + 1) * Hq > p.part_rows) {
+    if (lane == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: partials beyond the workspace
+    return;
+  }
 
   wait_for_primary_grid();
 

@@ -30,6 +30,7 @@ struct DecodeParams {
   int32_t grid_x;              // blocks sharing the pages of one KV head
   int32_t min_pages;           // smallest span a block is given
   int32_t out_f32;
+  int64_t part_rows;           // rows [Hq-row granularity] the workspace holds: (grid_x + batch) * Hq
 };
 
 // ---------------------------------------------------------------------------
@@ -163,6 +164,10 @@ __device__ __forceinline__ void produce_pages(const DecodeParams& p, const SeqTa
     const int f = sp.begin + i;
     const int b = seq_of(t, p.batch, f);
     const int lp = first_visible(t.len[b], p.window) / kPage + (f - t.prefix[b]);
+    if (lp < 0 || lp >= p.max_blocks) {  // cannot happen for a consistent schedule
+      report(p.status, ATTN_DEV_INTERNAL);
+      return -1;
+    }
     return p.block_table[static_cast<int64_t>(b) * p.max_blocks + lp];
   };
   int nxt = entry(lane);

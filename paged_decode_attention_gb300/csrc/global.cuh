@@ -273,6 +273,8 @@ __global__ void __launch_bounds__(kThreads)
           store_out2(p, row0 * kD + d, acc[n][0] * inv0, acc[n][1] * inv0);
           store_out2(p, (row0 + 8) * kD + d, acc[n][2] * inv1, acc[n][3] * inv1);
         }
+      } else if ((static_cast<int64_t>(gb) + cur.b + 1) * kHq > p.part_rows) {
+        if (lane == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: slot beyond the workspace
       } else {
         const size_t slot0 = (static_cast<size_t>(gb) + cur.b) * kHq + g;
         const size_t slot1 = slot0 + 8;

@@ -174,6 +174,10 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void report(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }

@@ -281,6 +281,8 @@ __global__ void __launch_bounds__(kThreads)
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         const size_t row = static_cast<size_t>(cur.b) * kHq + hq0 + h;
         store_out4(p, row * kD + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+      } else if ((static_cast<int64_t>(g) + cur.b + 1) * kHq > p.part_rows) {
+        if (tt == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: slot beyond the workspace
       } else {
         const size_t slot = (static_cast<size_t>(g) + cur.b) * kHq + hq0 + h;
         *reinterpret_cast<float4*>(p.part_o + slot * kD + d0) = O;
