@@ -174,6 +174,43 @@ int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32
 size_t attn_decode_workspace_size(int32_t kind, int32_t batch, int32_t max_seq_len,
                                   int32_t window, int32_t num_splits);
 
+/*
+ * attn_decode_sliding_noalloc -- attn_decode_sliding for callers that cannot
+ * allocate device memory.  The pages this library follows have no
+ * counterpart for it: it exists for integration, not for the method.
+ *
+ * Some callers have no way to hand over a workspace: a plugin in a serving
+ * runtime that gets device pointers for its inputs and outputs but no
+ * allocator, code whose device memory is fixed by a budget set up front, or
+ * a caller that must not touch the CUDA allocator on its hot path
+ * (cudaMalloc can synchronise the device and stall other streams).  This
+ * entry point takes the same arguments as
+ * attn_decode_sliding minus the workspace, and keeps the partial results of
+ * split sequences in a fixed 8 MiB array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  It calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - The first call on a device (with that device current) looks up the
+ *   array's device address with cudaGetSymbolAddress; make that first call
+ *   before any stream capture.
+ * - Calls whose plan needs more than 8 MiB of scratch are rejected with
+ *   ATTN_ERR_UNSUPPORTED and a message; nothing is launched.  The automatic
+ *   plan (num_splits = 0) fits for every batch up to ATTN_MAX_BATCH; large
+ *   forced num_splits may not.
+ * - All calls share the one array, which keeps whatever the last call left
+ *   there.  Nothing in it needs to start at zero: each call writes the
+ *   partial rows it reads.  Calls that may overlap on the GPU (concurrent
+ *   streams, or several host threads) race on the array and must be
+ *   serialised by the caller.
+ * - Everything else (arguments, layouts, errors, status bits, results) is as
+ *   for attn_decode_sliding.
+ */
+int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                    const int32_t* block_table, const int32_t* seq_lens, void* o,
+                                    int32_t batch, int32_t max_blocks, int64_t num_pages,
+                                    int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                                    int32_t num_splits, int32_t* status, void* stream);
+
 /* Message of the last error on this host thread ("" if none). */
 const char* attn_last_error(void);
 

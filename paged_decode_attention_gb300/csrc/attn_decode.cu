@@ -321,3 +321,67 @@ const char* attn_last_error(void) { return g_err; }
 int32_t attn_abi_version(void) { return ATTN_DECODE_ABI_VERSION; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Sliding-window decode with built-in scratch, for callers that cannot
+// allocate device memory themselves.
+//
+// The partial softmax rows that the split sequences leave for the combine
+// kernel live in one file-scope device array instead of a caller-provided
+// workspace.  Every GPU that loads this library keeps the array for the life
+// of the process.  In host code the array's name is only a host-side stand-in
+// for the device object and must never be handed to a kernel; the device
+// address comes from cudaGetSymbolAddress, taken once per device on the first
+// call made with that device current.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t{8} << 20;  // 8 MiB per device
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+int32_t noalloc_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(ATTN_ERR_CUDA, "attn_decode_sliding_noalloc: cudaGetSymbolAddress of the scratch failed: %s",
+                  cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                               const int32_t* block_table, const int32_t* seq_lens, void* o,
+                                               int32_t batch, int32_t max_blocks, int64_t num_pages,
+                                               int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                                               int32_t num_splits, int32_t* status, void* stream) {
+  g_err[0] = '\0';
+  int dev = 0, num_sms = 0;
+  int32_t st = current_device(&dev, &num_sms);
+  if (st != ATTN_OK) return st;
+  // Size check first; every other argument is validated by the common path below.
+  if (window > 0 && batch >= 1 && max_seq_len >= 0 && num_splits >= 0) {
+    Plan plan;
+    st = make_plan(ATTN_KIND_SLIDING, batch, max_seq_len, window, num_splits, num_sms, &plan);
+    if (st != ATTN_OK) return st;
+    if (plan.workspace_bytes > kNoAllocScratchBytes)
+      return fail(ATTN_ERR_UNSUPPORTED,
+                  "attn_decode_sliding_noalloc: this call needs %zu bytes of scratch but the built-in "
+                  "scratch holds %zu (batch %d, num_splits %d); use attn_decode_sliding with a workspace",
+                  plan.workspace_bytes, kNoAllocScratchBytes, batch, num_splits);
+  }
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(dev, &scratch)) != ATTN_OK) return st;
+  return run_decode(ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, o, batch, max_blocks,
+                    num_pages, max_seq_len, window, out_dtype, num_splits, scratch, kNoAllocScratchBytes,
+                    status, stream);
+}
