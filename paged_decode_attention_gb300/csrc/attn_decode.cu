@@ -76,6 +76,10 @@ int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t wind
     gx = forced_blocks;
   } else {
     gx = static_cast<int64_t>(num_sms) * blocks_per_sm / columns;
+    // Short spans (few pages per block) are latency-bound and leave a partial
+    // per block; there one global block per SM streams as fast and halves the
+    // partials the combine kernel reads.
+    if (!sliding && total_max < gx * pda::global::kShortSpanPages) gx = num_sms;
     const int64_t useful = (total_max + min_pages - 1) / min_pages;
     if (gx > useful) gx = useful;
   }
@@ -252,7 +256,7 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
     const dim3 grid(plan.grid_x, ATTN_SLIDING_HKV);
     pda::sliding::decode_kernel<<<grid, pda::sliding::kThreads, pda::sliding::kSmemBytes, s>>>(tm_k, tm_v, p);
     e = launch_combine(pda::combine_kernel<ATTN_SLIDING_D>,
-                       dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), 32, s, p);
+                       dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, s, p);
   } else {
     const int row = ATTN_GLOBAL_HKV * ATTN_GLOBAL_D;
     if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
@@ -261,7 +265,7 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
     if ((st = ensure_smem(pda::global::decode_kernel, pda::global::kSmemBytes, dev, smem_set))) return st;
     pda::global::decode_kernel<<<plan.grid_x, pda::global::kThreads, pda::global::kSmemBytes, s>>>(tm_k, tm_v, p);
     e = launch_combine(pda::combine_kernel<ATTN_GLOBAL_D>,
-                       dim3(ATTN_GLOBAL_HQ * (ATTN_GLOBAL_D / pda::kCombineCols), batch), 32, s, p);
+                       dim3(ATTN_GLOBAL_HQ * (ATTN_GLOBAL_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, s, p);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));

@@ -11,11 +11,13 @@
 // never read.  Rows of sequences with no visible position are written as 0
 // (the empty sum); rows finished whole by one block are left untouched.
 //
-// One single-warp block per (row b*Hq + h, slice of 128 dims): each lane owns
-// 4 dims and keeps 16 partial rows in flight, so a row with tens of
-// partials costs a couple of L2 round trips.  The schedule arithmetic runs
-// before griddepcontrol.wait, overlapping the decode kernel (the combine is
-// launched as its programmatic dependent).
+// One 4-warp block per (row b*Hq + h, slice of 128 dims).  Warp w takes the
+// partials i = w, w+4, ...; each lane owns 4 dims and issues the (m, l) pair
+// and the 16-byte slice of up to kPerWarp partials in one go, so a row costs
+// one memory round trip (more only beyond 4*kPerWarp partials).  The maxima
+// and the weighted sums are then merged across the warps in shared memory.
+// The schedule arithmetic runs before griddepcontrol.wait, overlapping the
+// decode kernel (the combine is launched as its programmatic dependent).
 #pragma once
 
 #include "common.cuh"
@@ -23,18 +25,22 @@
 namespace pda {
 
 constexpr int kCombineCols = 128;  // dims per combine block
-constexpr int kCombineInFlight = 16;
+constexpr int kCombineWarps = 4;
+constexpr int kPerWarp = 12;       // partials a warp keeps in flight per round
 
 template <int kD>
-__global__ void __launch_bounds__(32) combine_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kSlices = kD / kCombineCols;
-  __shared__ float w_s[kMaxSplits];
+  __shared__ float s_max[kCombineWarps];
+  __shared__ float s_l[kCombineWarps];
+  __shared__ float4 s_o[kCombineWarps][32];
 
   const int h = blockIdx.x / kSlices;
   const int slice = blockIdx.x % kSlices;
   const int b = blockIdx.y;
   const int Hq = gridDim.x / kSlices;
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const size_t row = static_cast<size_t>(b) * Hq + h;
   const int d0 = slice * kCombineCols + lane * 4;
 
@@ -53,7 +59,7 @@ __global__ void __launch_bounds__(32) combine_kernel(const __grid_constant__ Dec
     total += __shfl_xor_sync(0xffffffffu, total, o);
   }
   if (mine == 0) {
-    store_out4(p, row * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
+    if (warp == 0) store_out4(p, row * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
   const int per = span_pages(total, p.grid_x, p.min_pages);
@@ -62,56 +68,70 @@ __global__ void __launch_bounds__(32) combine_kernel(const __grid_constant__ Dec
   if (g0 == g1) return;  // one block held the whole sequence and wrote o
   const int ns = g1 - g0 + 1;
   if (ns > kMaxSplits || (static_cast<int64_t>(g1) + b + 1) * Hq > p.part_rows) {
-    if (lane == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: partials beyond the workspace
+    if (threadIdx.x == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: partials beyond the workspace
     return;
   }
 
   wait_for_primary_grid();
 
-  // weights 2^{m_g - M} over the partials that saw a visible position
-  const float2* ml = p.part_ml + (static_cast<size_t>(g0) + b) * Hq + h;
-  float mx = -INFINITY;
-  for (int i = lane; i < ns; i += 32) {
-    const float2 e = ml[static_cast<size_t>(i) * Hq];
-    w_s[i] = e.y > 0.f ? e.x : -INFINITY;
-    mx = fmaxf(mx, w_s[i]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float ls = 0.f;
-  for (int i = lane; i < ns; i += 32) {
-    const float wi = (mx == -INFINITY || w_s[i] == -INFINITY) ? 0.f : exp2f(w_s[i] - mx);
-    ls += wi * ml[static_cast<size_t>(i) * Hq].y;
-    w_s[i] = wi;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-  __syncwarp();
-
-  // o = sum_g w_g O_g / sum_g w_g l_g
   const size_t stride = static_cast<size_t>(Hq) * kD;
+  const float2* ml = p.part_ml + (static_cast<size_t>(g0) + b) * Hq + h;
   const float* base = p.part_o + ((static_cast<size_t>(g0) + b) * Hq + h) * kD + d0;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < ns; i0 += kCombineInFlight) {
-    float4 a[kCombineInFlight];
+
+  // This warp's partials, kPerWarp per round: running (max, sum, output) of
+  // the rounds so far, in the same log2 units as the decode kernels.
+  float wm = -INFINITY, wl = 0.f;
+  float4 wo = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r0 = warp; r0 < ns; r0 += kCombineWarps * kPerWarp) {
+    float2 e[kPerWarp];
+    float4 a[kPerWarp];
 #pragma unroll
-    for (int j = 0; j < kCombineInFlight; ++j) {
-      const int i = i0 + j;
-      a[j] = (i < ns && w_s[i] != 0.f) ? *reinterpret_cast<const float4*>(base + i * stride)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < kPerWarp; ++j) {
+      const int i = r0 + j * kCombineWarps;
+      e[j] = i < ns ? ml[static_cast<size_t>(i) * Hq] : make_float2(-INFINITY, 0.f);
+      a[j] = i < ns ? *reinterpret_cast<const float4*>(base + i * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float rm = wm;
 #pragma unroll
-    for (int j = 0; j < kCombineInFlight; ++j) {
-      const int i = i0 + j;
-      const float wi = i < ns ? w_s[i] : 0.f;
-      O.x += wi * a[j].x;
-      O.y += wi * a[j].y;
-      O.z += wi * a[j].z;
-      O.w += wi * a[j].w;
+    for (int j = 0; j < kPerWarp; ++j)
+      if (e[j].y > 0.f) rm = fmaxf(rm, e[j].x);
+    if (rm == -INFINITY) continue;
+    const float cw = wm == -INFINITY ? 0.f : exp2f(wm - rm);
+    wl *= cw;
+    wo.x *= cw; wo.y *= cw; wo.z *= cw; wo.w *= cw;
+#pragma unroll
+    for (int j = 0; j < kPerWarp; ++j) {
+      if (e[j].y > 0.f) {  // partials without a visible position are skipped, whatever they hold
+        const float w = exp2f(e[j].x - rm);
+        wl += w * e[j].y;
+        wo.x += w * a[j].x; wo.y += w * a[j].y; wo.z += w * a[j].z; wo.w += w * a[j].w;
+      }
     }
+    wm = rm;
   }
-  const float inv = ls > 0.f ? 1.f / ls : 0.f;
-  store_out4(p, row * kD + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+
+  // merge the warps
+  if (lane == 0) s_max[warp] = wm;
+  __syncthreads();
+  float M = s_max[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, s_max[w]);
+  const float f = (M == -INFINITY || wm == -INFINITY) ? 0.f : exp2f(wm - M);
+  if (lane == 0) s_l[warp] = f * wl;
+  s_o[warp][lane] = make_float4(f * wo.x, f * wo.y, f * wo.z, f * wo.w);
+  __syncthreads();
+  if (warp == 0) {
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+      L += s_l[w];
+      const float4 v = s_o[w][lane];
+      O.x += v.x; O.y += v.y; O.z += v.z; O.w += v.w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    store_out4(p, row * kD + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+  }
 }
 
 }  // namespace pda

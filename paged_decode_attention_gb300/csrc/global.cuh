@@ -41,6 +41,7 @@ constexpr int kPageBytes = kPage * kD * 2;          // 16 KB
 constexpr int kStages = 3;
 constexpr int kBlocksPerSm = 2;
 constexpr int kMinPages = 4;
+constexpr int kShortSpanPages = 32;  // below this many pages per block the plan uses one block per SM
 
 static_assert(kHq == 16, "the m16n8k16 tiling uses the 16 query heads as the M dimension");
 
@@ -156,8 +157,10 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t kst = smem_addr(s.k[stage]);
     const uint32_t vst = smem_addr(s.v[stage]);
 
-    // ---- partial S over this warp's dims: two n-tiles of 8 positions ----
-    float sp_[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- partial S over this warp's dims: two n-tiles of 8 positions; even
+    //      and odd k-steps accumulate separately (two chains of 4 MMAs) ----
+    float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int ch = 2 * warp + (ks >> 2);
@@ -165,14 +168,18 @@ __global__ void __launch_bounds__(kThreads)
       const int unit = 2 * (ks & 3) + (mi & 1);
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4(kst + ch * kChunkBytes + swz(row, unit), b0, b1, b2, b3);
-      mma_bf16_16816(sp_[0], qa[ks], b0, b1);
-      mma_bf16_16816(sp_[1], qa[ks], b2, b3);
+      float (&s0)[4] = (ks & 1) ? so[0] : se[0];
+      float (&s1)[4] = (ks & 1) ? so[1] : se[1];
+      mma_bf16_16816(s0, qa[ks], b0, b1);
+      mma_bf16_16816(s1, qa[ks], b2, b3);
     }
 
     // ---- sum the four partials in a fixed order ----
     const int buf = i & 1;
-    s.xs[buf][warp][0][lane] = make_float4(sp_[0][0], sp_[0][1], sp_[0][2], sp_[0][3]);
-    s.xs[buf][warp][1][lane] = make_float4(sp_[1][0], sp_[1][1], sp_[1][2], sp_[1][3]);
+    s.xs[buf][warp][0][lane] =
+        make_float4(se[0][0] + so[0][0], se[0][1] + so[0][1], se[0][2] + so[0][2], se[0][3] + so[0][3]);
+    s.xs[buf][warp][1][lane] =
+        make_float4(se[1][0] + so[1][0], se[1][1] + so[1][1], se[1][2] + so[1][2], se[1][3] + so[1][3]);
     named_barrier_sync(1, kConsumerWarps * 32);
     float sc[2][4];
     {
@@ -216,12 +223,15 @@ __global__ void __launch_bounds__(kThreads)
       for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(sc[nt][e] - m_use[e >> 1]);
     l[0] = l[0] * scale[0] + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
     l[1] = l[1] * scale[1] + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+    // rescale only when some row's running max moved (multiplying by 1 is exact)
+    if (__any_sync(0xffffffffu, scale[0] != 1.f || scale[1] != 1.f)) {
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      acc[n][0] *= scale[0];
-      acc[n][1] *= scale[0];
-      acc[n][2] *= scale[1];
-      acc[n][3] *= scale[1];
+      for (int n = 0; n < 16; ++n) {
+        acc[n][0] *= scale[0];
+        acc[n][1] *= scale[0];
+        acc[n][2] *= scale[1];
+        acc[n][3] *= scale[1];
+      }
     }
     // P as the A fragment of one k16 step (k = the page's 16 positions)
     const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),

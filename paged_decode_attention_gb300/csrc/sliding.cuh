@@ -215,11 +215,13 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < 8; ++j) pj[j] = __shfl_sync(0xffffffffu, pv, 4 * j);
 
+    if (scale[0] != 1.f || scale[1] != 1.f) {  // same in every lane; multiplying by 1 is exact
 #pragma unroll
-    for (int h = 0; h < kG; ++h) {
-      const float2 sc = make_float2(scale[h], scale[h]);
+      for (int h = 0; h < kG; ++h) {
+        const float2 sc = make_float2(scale[h], scale[h]);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc[h][k] = __fmul2_rn(acc[h][k], sc);
+        for (int k = 0; k < 4; ++k) acc[h][k] = __fmul2_rn(acc[h][k], sc);
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
