@@ -246,6 +246,14 @@ struct PageCursor {
   }
 };
 
+// The first sequence after b with a visible page inside the span, or -1.
+// It is the sequence PageCursor::advance moves to when b's pages end.
+__device__ __forceinline__ int next_seq_in_span(const DecodeParams& p, const SeqTable& t, const Span& sp, int b) {
+  int nb = b + 1;
+  while (nb < p.batch && t.prefix[nb + 1] == t.prefix[nb]) ++nb;  // skip empty sequences
+  return (nb < p.batch && t.prefix[nb] < sp.end) ? nb : -1;
+}
+
 // Lets the dependent (combine) grid launch while this grid runs.
 __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

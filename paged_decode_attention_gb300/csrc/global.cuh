@@ -127,7 +127,16 @@ __global__ void __launch_bounds__(kThreads)
       qa[ks][3] = __ldg(q_g8 + (d + 8) / 2);
     }
   };
+  // Pull q of the span's next sequence into L2 while this one runs, so its
+  // reload at the sequence boundary is an L2 hit (16 KB = 128 lines of 128
+  // bytes; the 128 consumer threads take one line each).
+  auto prefetch_next_q = [&]() {
+    const int nb = next_seq_in_span(p, t, sp, cur.b);
+    if (nb >= 0)
+      prefetch_l2(reinterpret_cast<const uint8_t*>(p.q + static_cast<size_t>(nb) * kHq * kD) + threadIdx.x * 128);
+  };
   load_q();
+  prefetch_next_q();
 
   float m[2], l[2];  // rows g, g+8: running max (log2 units), this thread's share of the sum
   float acc[16][4];  // 16 n-tiles of 8 dims
@@ -147,6 +156,7 @@ __global__ void __launch_bounds__(kThreads)
     if (f >= t.prefix[cur.b + 1]) {
       cur.advance(p, t, sp, f);
       load_q();
+      prefetch_next_q();
     }
     const int stage = i % kStages;
     if (ok) {

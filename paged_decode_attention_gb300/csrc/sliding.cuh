@@ -101,18 +101,28 @@ __global__ void __launch_bounds__(kThreads)
 
   PageCursor cur;
   cur.start(p, t, sp);
+  // q of the current sequence as fp32 pairs; qn holds the raw bf16 words of
+  // the next sequence of the span, loaded one segment ahead
   float2 qf[kG][4];
-  auto load_q = [&]() {
+  uint4 qn[kG];
+  auto load_q_raw = [&](int b) {
+#pragma unroll
+    for (int h = 0; h < kG; ++h)
+      qn[h] = ld_global_nc_v4(p.q + (static_cast<size_t>(b) * kHq + hq0 + h) * kD + 8 * lane);
+  };
+  auto take_q = [&]() {
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
-      const uint4 w = ld_global_nc_v4(p.q + (static_cast<size_t>(cur.b) * kHq + hq0 + h) * kD + 8 * lane);
-      qf[h][0] = bf16x2_to_float2(w.x);
-      qf[h][1] = bf16x2_to_float2(w.y);
-      qf[h][2] = bf16x2_to_float2(w.z);
-      qf[h][3] = bf16x2_to_float2(w.w);
+      qf[h][0] = bf16x2_to_float2(qn[h].x);
+      qf[h][1] = bf16x2_to_float2(qn[h].y);
+      qf[h][2] = bf16x2_to_float2(qn[h].z);
+      qf[h][3] = bf16x2_to_float2(qn[h].w);
     }
   };
-  load_q();
+  load_q_raw(cur.b);
+  take_q();
+  int nb = next_seq_in_span(p, t, sp, cur.b);
+  if (nb >= 0) load_q_raw(nb);
 
   float m[kG], l[kG];  // running max (log2 units) and sum, identical in every lane
   float2 acc[kG][4];
@@ -131,8 +141,10 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = 0; i < n_pages; ++i) {
     const int f = sp.begin + i;
     if (f >= t.prefix[cur.b + 1]) {
-      cur.advance(p, t, sp, f);
-      load_q();
+      cur.advance(p, t, sp, f);  // lands on nb, whose q is already in qn
+      take_q();
+      nb = next_seq_in_span(p, t, sp, cur.b);
+      if (nb >= 0) load_q_raw(nb);
     }
     const int stage = i % kStages;
     if (ok) {
