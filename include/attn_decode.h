@@ -211,6 +211,17 @@ int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool, const voi
                                     int32_t max_seq_len, int32_t window, int32_t out_dtype,
                                     int32_t num_splits, int32_t* status, void* stream);
 
+/*
+ * attn_selftest_wait_timeout -- exercises the device-side failure path of the
+ * copy pipeline.  It launches one warp that waits, with the same bounded
+ * wait and time limit as the decode kernels (1 s), on a shared-memory
+ * barrier that nothing arrives at.  The wait gives up, ATTN_DEV_WAIT_TIMEOUT
+ * is OR-ed into *status (a device int32, required) and the kernel returns;
+ * the CUDA context stays usable.  Asynchronous on `stream`.  For tests of
+ * failure detection; the pages have no counterpart for it.
+ */
+int32_t attn_selftest_wait_timeout(int32_t* status, void* stream);
+
 /* Message of the last error on this host thread ("" if none). */
 const char* attn_last_error(void);
 

@@ -326,6 +326,30 @@ int32_t attn_abi_version(void) { return ATTN_DECODE_ABI_VERSION; }
 
 }  // extern "C"
 
+// One warp waits, with the decode kernels' bounded wait and time limit, on a
+// barrier that nothing arrives at; the wait gives up, the timeout bit is
+// raised and the kernel returns.  No copy is ever issued.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int32_t* status) {
+  __shared__ alignas(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    pda::mbar_init(&bar, 1);
+    pda::fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, pda::mbar_wait(&bar, 0));
+  if (!ok && threadIdx.x == 0) pda::report(status, ATTN_DEV_WAIT_TIMEOUT);
+}
+
+extern "C" int32_t attn_selftest_wait_timeout(int32_t* status, void* stream) {
+  g_err[0] = '\0';
+  if (!status || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_selftest_wait_timeout: status must be a 4-byte aligned device int32");
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attn_selftest_wait_timeout: launch failed: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Sliding-window decode with built-in scratch, for callers that cannot
 // allocate device memory themselves.

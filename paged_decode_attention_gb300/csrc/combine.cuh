@@ -44,20 +44,44 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   const size_t row = static_cast<size_t>(b) * Hq + h;
   const int d0 = slice * kCombineCols + lane * 4;
 
-  // the schedule: pages before sequence b, its own pages, and the total
-  int before = 0, mine = 0, total = 0;
-  for (int j = lane; j < p.batch; j += 32) {
-    const int n = visible_pages(clamp_len(p, p.seq_lens[j], false), p.window);
-    total += n;
-    before += j < b ? n : 0;
-    mine += j == b ? n : 0;
-  }
+  // The schedule: pages before sequence b, its own pages, and the total.
+  // Warp 0 reads seq_lens four at a time and shares the three sums.
+  __shared__ int s_sched[3];
+  if (warp == 0) {
+    int before = 0, mine = 0, total = 0;
+    const int nvec = p.batch >> 2;  // seq_lens is 16-byte aligned
+    for (int v = lane; v <= nvec; v += 32) {
+      int L[4];
+      if (v < nvec) {
+        const int4 w = reinterpret_cast<const int4*>(p.seq_lens)[v];
+        L[0] = w.x; L[1] = w.y; L[2] = w.z; L[3] = w.w;
+      } else {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    mine += __shfl_xor_sync(0xffffffffu, mine, o);
-    total += __shfl_xor_sync(0xffffffffu, total, o);
+        for (int k = 0; k < 4; ++k) L[k] = 4 * v + k < p.batch ? p.seq_lens[4 * v + k] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = 4 * v + k;
+        const int n = j < p.batch ? visible_pages(clamp_len(p, L[k], false), p.window) : 0;
+        total += n;
+        before += j < b ? n : 0;
+        mine += j == b ? n : 0;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      mine += __shfl_xor_sync(0xffffffffu, mine, o);
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    if (lane == 0) {
+      s_sched[0] = before;
+      s_sched[1] = mine;
+      s_sched[2] = total;
+    }
   }
+  __syncthreads();
+  const int before = s_sched[0], mine = s_sched[1], total = s_sched[2];
   if (mine == 0) {
     if (warp == 0) store_out4(p, row * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
     return;

@@ -89,3 +89,12 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_recorded_traffic_tracks_the_kernel_sources():
+    # a capture is reported only while the kernel sources hash to the recorded value
+    for (kind, cfg), (nbytes, sha) in bench.NCU_TRAFFIC.items():
+        got = bench.recorded_traffic(kind, cfg)
+        assert got in (None, nbytes)
+        assert (got is not None) == (bench.kernel_source_hash(kind) == sha)
+    assert bench.recorded_traffic("global", "no-such-workload") is None
