@@ -20,6 +20,7 @@ from . import _build
 
 __all__ = [
     "attn_decode_sliding", "attn_decode_global", "attn_decode_plan", "attn_decode_workspace_size",
+    "PreparedDecode", "prepare_decode_sliding", "prepare_decode_global",
     "attn_last_error", "load", "library_path", "AttnDecodeError",
     "KIND_SLIDING", "KIND_GLOBAL", "DEV_WAIT_TIMEOUT", "DEV_BAD_PAGE", "DEV_BAD_SEQ_LEN",
 ]
@@ -164,6 +165,63 @@ def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len
     if st != ATTN_OK:
         raise AttnDecodeError(st, attn_last_error())
     return o
+
+
+class PreparedDecode:
+    """A decode call whose arguments are checked and marshalled once.
+
+    For a serving loop that calls the same buffers every step: construction
+    validates the tensors exactly as the one-shot functions do and keeps their
+    device pointers; ``run(stream)`` then costs one C call.  The tensors must
+    stay alive and in place (the object keeps references to them); their
+    contents may change between runs.
+    """
+
+    def __init__(self, kind, q, k_pool, v_pool, block_table, seq_lens, o=None, *, window, max_seq_len=None,
+                 out_dtype=torch.bfloat16, num_splits=0, workspace=None, status=None):
+        Hq, Hkv, D = SHAPES[kind]
+        batch, num_pages, max_blocks = q.shape[0], k_pool.shape[0], block_table.shape[1]
+        ptrs = [_ptr(q, "q", torch.bfloat16, (batch, Hq, D)),
+                _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
+                _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
+                _ptr(block_table, "block_table", torch.int32, (batch, max_blocks)),
+                _ptr(seq_lens, "seq_lens", torch.int32, (batch,))]
+        if o is None:
+            o = torch.empty((batch, Hq, D), dtype=out_dtype, device=q.device)
+        ptrs.append(_ptr(o, "o", o.dtype, (batch, Hq, D)))
+        if max_seq_len is None:
+            max_seq_len = max_blocks * PAGE_SIZE
+        lib = load()
+        if workspace is None:
+            with torch.cuda.device(q.device):
+                need = attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits)
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        ws_ptr = _ptr(workspace, "workspace", torch.uint8)
+        st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
+        self._keep = (q, k_pool, v_pool, block_table, seq_lens, o, workspace, status)
+        self.o = o
+        self._fn = lib.attn_decode_sliding if kind == KIND_SLIDING else lib.attn_decode_global
+        self._args = tuple(ptrs) + (batch, max_blocks, num_pages, int(max_seq_len), int(window),
+                                    OUT_F32 if o.dtype == torch.float32 else OUT_BF16, int(num_splits),
+                                    ws_ptr, workspace.numel(), st_ptr)
+
+    def run(self, stream):
+        """Enqueue the call on `stream` (a torch.cuda.Stream or a raw cudaStream_t); returns o."""
+        s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        st = self._fn(*self._args, s_ptr)
+        if st != ATTN_OK:
+            raise AttnDecodeError(st, attn_last_error())
+        return self.o
+
+
+def prepare_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=1024, **kw):
+    """PreparedDecode for attn_decode_sliding (same arguments, minus the stream)."""
+    return PreparedDecode(KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, o, window=window, **kw)
+
+
+def prepare_decode_global(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=0, **kw):
+    """PreparedDecode for attn_decode_global (same arguments, minus the stream)."""
+    return PreparedDecode(KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, o, window=window, **kw)
 
 
 def attn_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=1024,

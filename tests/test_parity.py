@@ -242,3 +242,17 @@ def test_long_context_global_full_size(cuda_lib, variant):
 def test_decode_step_mix_layers_full_size(cuda_lib, layer):
     case = config_case(5, device=DEV, layer=layer)
     _full_size(case, 48, 3, "mix layer %d" % layer)
+
+
+def test_prepared_call_matches_the_one_shot_call(cuda_lib):
+    for kind in ("sliding", "global"):
+        case = make_case(kind, [17, 1500, 300], seed=92).to(DEV)
+        ref, _ = run(case)
+        prep = (pda.prepare_decode_sliding if kind == "sliding" else pda.prepare_decode_global)(
+            case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, window=case.window,
+            max_seq_len=case.max_seq_len, out_dtype=torch.float32)
+        s = torch.cuda.Stream()
+        for _ in range(2):  # a prepared call is reusable
+            o = prep.run(s)
+            s.synchronize()
+            assert torch.equal(o, ref)
