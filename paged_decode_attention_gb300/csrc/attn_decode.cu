@@ -76,10 +76,6 @@ int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t wind
     gx = forced_blocks;
   } else {
     gx = static_cast<int64_t>(num_sms) * blocks_per_sm / columns;
-    // Short spans (few pages per block) are latency-bound and leave a partial
-    // per block; there one global block per SM streams as fast and halves the
-    // partials the combine kernel reads.
-    if (!sliding && total_max < gx * pda::global::kShortSpanPages) gx = num_sms;
     const int64_t useful = (total_max + min_pages - 1) / min_pages;
     if (gx > useful) gx = useful;
   }
@@ -149,31 +145,40 @@ int32_t encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, i
 template <typename Kernel>
 int32_t ensure_smem(Kernel kernel, size_t bytes, int dev, bool* done) {
   if (done[dev]) return ATTN_OK;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
+  cudaError_t e = cudaSuccess;
+  if (bytes > 0)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  // Every kernel of the library asks for the largest shared-memory carveout,
+  // so consecutive launches never wait for an SM to change its L1/shared split.
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   done[dev] = true;
   return ATTN_OK;
 }
 
-// The combine grid is a programmatic dependent of the decode grid: it may be
-// scheduled while the decode kernel runs (which calls
-// griddepcontrol.launch_dependents at entry) and waits in
-// griddepcontrol.wait for the decode grid's results, so its launch latency
-// overlaps the decode kernel instead of following it.
-template <typename Kernel>
-cudaError_t launch_combine(Kernel kernel, dim3 grid, int threads, cudaStream_t s, const pda::DecodeParams& p) {
+// Every kernel is launched as a programmatic dependent of the kernel before
+// it in the stream.  A decode grid may then be scheduled while that kernel
+// finishes: it sets up its shared memory, then waits in griddepcontrol.wait
+// before it reads any input or writes any output, and lets its own dependent
+// (the combine) launch only after that wait.  The combine runs its schedule
+// arithmetic while the decode grid streams, waits for the decode grid's
+// results the same way, and lets the next kernel launch once it is merging.
+// Following anything but a kernel, the attribute has no effect.
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, int threads, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ---------------------------------------------------------------------------
@@ -231,6 +236,8 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.o = o;
+  p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+  p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
   p.part_o = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + plan.part_o_bytes);
   p.status = status;
@@ -253,19 +260,28 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
     if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, ATTN_SLIDING_D, CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     static bool smem_set[kMaxDevices] = {false};
     if ((st = ensure_smem(pda::sliding::decode_kernel, pda::sliding::kSmemBytes, dev, smem_set))) return st;
-    const dim3 grid(plan.grid_x, ATTN_SLIDING_HKV);
-    pda::sliding::decode_kernel<<<grid, pda::sliding::kThreads, pda::sliding::kSmemBytes, s>>>(tm_k, tm_v, p);
-    e = launch_combine(pda::combine_kernel<ATTN_SLIDING_D>,
-                       dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, s, p);
+    static bool comb_set[kMaxDevices] = {false};
+    if ((st = ensure_smem(pda::combine_kernel<ATTN_SLIDING_D>, 0, dev, comb_set))) return st;
+    e = launch_pdl(pda::sliding::decode_kernel, dim3(plan.grid_x, ATTN_SLIDING_HKV), pda::sliding::kThreads,
+                   pda::sliding::kSmemBytes, s, tm_k, tm_v, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(pda::combine_kernel<ATTN_SLIDING_D>,
+                     dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, 0,
+                     s, p);
   } else {
     const int row = ATTN_GLOBAL_HKV * ATTN_GLOBAL_D;
     if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
     if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
     static bool smem_set[kMaxDevices] = {false};
     if ((st = ensure_smem(pda::global::decode_kernel, pda::global::kSmemBytes, dev, smem_set))) return st;
-    pda::global::decode_kernel<<<plan.grid_x, pda::global::kThreads, pda::global::kSmemBytes, s>>>(tm_k, tm_v, p);
-    e = launch_combine(pda::combine_kernel<ATTN_GLOBAL_D>,
-                       dim3(ATTN_GLOBAL_HQ * (ATTN_GLOBAL_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, s, p);
+    static bool comb_set[kMaxDevices] = {false};
+    if ((st = ensure_smem(pda::combine_kernel<ATTN_GLOBAL_D>, 0, dev, comb_set))) return st;
+    e = launch_pdl(pda::global::decode_kernel, dim3(plan.grid_x), pda::global::kThreads, pda::global::kSmemBytes, s,
+                   tm_k, tm_v, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(pda::combine_kernel<ATTN_GLOBAL_D>,
+                     dim3(ATTN_GLOBAL_HQ * (ATTN_GLOBAL_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, 0,
+                     s, p);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));

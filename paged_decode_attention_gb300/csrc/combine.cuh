@@ -44,8 +44,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   const size_t row = static_cast<size_t>(b) * Hq + h;
   const int d0 = slice * kCombineCols + lane * 4;
 
-  // The schedule: pages before sequence b, its own pages, and the total.
-  // Warp 0 reads seq_lens four at a time and shares the three sums.
+  // The schedule, on the decode kernels' weighted page list (kSeqWeight
+  // virtual pages before every non-empty sequence): weighted pages before
+  // sequence b, its own real pages, and the weighted total.  Warp 0 reads
+  // seq_lens four at a time and shares the three sums.
   __shared__ int s_sched[3];
   if (warp == 0) {
     int before = 0, mine = 0, total = 0;
@@ -63,8 +65,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
       for (int k = 0; k < 4; ++k) {
         const int j = 4 * v + k;
         const int n = j < p.batch ? visible_pages(clamp_len(p, L[k], false), p.window) : 0;
-        total += n;
-        before += j < b ? n : 0;
+        const int wn = n > 0 ? n + kSeqWeight : 0;
+        total += wn;
+        before += j < b ? wn : 0;
         mine += j == b ? n : 0;
       }
     }
@@ -87,8 +90,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     return;
   }
   const int per = span_pages(total, p.grid_x, p.min_pages);
-  const int g0 = before / per;
-  const int g1 = (before + mine - 1) / per;
+  const int g0 = (before + kSeqWeight) / per;
+  const int g1 = (before + kSeqWeight + mine - 1) / per;
   if (g0 == g1) return;  // one block held the whole sequence and wrote o
   const int ns = g1 - g0 + 1;
   if (ns > kMaxSplits || (static_cast<int64_t>(g1) + b + 1) * Hq > p.part_rows) {
@@ -97,6 +100,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   }
 
   wait_for_primary_grid();
+  allow_dependent_launch();  // the next kernel may start its prologue
 
   const size_t stride = static_cast<size_t>(Hq) * kD;
   const float2* ml = p.part_ml + (static_cast<size_t>(g0) + b) * Hq + h;

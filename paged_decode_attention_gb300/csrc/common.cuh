@@ -17,6 +17,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
   const __nv_bfloat16* q;      // [batch, Hq, D]
+  const __nv_bfloat16* k_pool; // [num_pages, 16, Hkv, D] (read through the tensor maps; raw for L2 prefetches)
+  const __nv_bfloat16* v_pool;
   const int32_t* block_table;  // [batch, max_blocks]
   const int32_t* seq_lens;     // [batch]
   void* o;                     // [batch, Hq, D], bf16 or fp32
@@ -40,17 +42,29 @@ struct DecodeParams {
 // p = L_b - 1 (Attention.lean decodeGQA) and, for a window w, lo_b =
 // max(0, L_b - w) (Attention.lean slidingGQA: p - w < l <= p).  They occupy
 // logical pages lo_b/16 .. (L_b-1)/16.  Concatenating every sequence's
-// visible pages gives N pages; block g of grid_x takes the contiguous span
-// [g*per, min((g+1)*per, N)) with per = max(min_pages, ceil(N / grid_x)), so
-// every block streams the same number of pages whatever the mix of
-// lengths.  A sequence that lies inside one span is finished by that block;
-// one that straddles spans leaves a partial result in slot (block + b), an
-// injective numbering because spans and sequences are both in order, and
-// the combine kernel merges them.
+// visible pages gives N pages.  Each sequence a block starts also costs it a
+// fixed amount of work (loading its q, closing its segment), so spans are cut
+// on a weighted list in which every non-empty sequence is preceded by
+// kSeqWeight virtual pages.  With W weighted pages in all, block g of grid_x
+// takes the weighted range [g*per, min((g+1)*per, W)), per = max(min_pages,
+// ceil(W / grid_x)), mapped back to a contiguous range of real pages (a
+// virtual page maps to the first page of its sequence), so every block gets
+// the same amount of work whatever the mix of lengths.  A sequence that lies
+// inside one span is finished by that block; one that straddles spans leaves
+// a partial result in slot (block + b), an injective numbering because spans
+// and sequences are both in order, and the combine kernel merges them.
 // ---------------------------------------------------------------------------
+constexpr int kSeqWeight = 1;  // virtual pages charged per sequence start
+
+struct Span {
+  int begin, end;  // flattened real pages of this block
+};
+
 struct SeqTable {
   int32_t prefix[kMaxBatch + 1];  // prefix[b] = visible pages of sequences < b
-  int32_t len[kMaxBatch];         // L_b, clamped to [0, max_blocks*16]
+  int32_t len[kMaxBatch];         // L_b, clamped (clamp_len)
+  Span span;                      // this block's pages
+  int32_t rebuilt;                // confirm_seq_table found seq_lens changed since the hint pass
 };
 
 __device__ __forceinline__ int first_visible(int L, int window) {
@@ -61,8 +75,11 @@ __device__ __forceinline__ int visible_pages(int L, int window) {
   return L > 0 ? (L - 1) / kPage - first_visible(L, window) / kPage + 1 : 0;
 }
 
+// L_b clamped to [0, min(max_blocks*16, ATTN_MAX_SEQ_LEN)]: the block table
+// holds no more positions, and the bound keeps every page count and prefix
+// sum well inside int32.  A length outside is reported once per block.
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int L, bool report_it) {
-  const int cap = p.max_blocks * kPage;
+  const int cap = p.max_blocks < ATTN_MAX_SEQ_LEN / kPage ? p.max_blocks * kPage : ATTN_MAX_SEQ_LEN;
   if (L < 0 || L > cap) {
     if (report_it) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
     return L < 0 ? 0 : cap;
@@ -70,30 +87,109 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int L, bool repo
   return L;
 }
 
-// Fills the table; called by every thread of the block (contains __syncthreads).
-__device__ __forceinline__ void build_seq_table(const DecodeParams& p, SeqTable& t) {
-  const int tid = threadIdx.x;
-  for (int b = tid; b < p.batch; b += blockDim.x) t.len[b] = clamp_len(p, p.seq_lens[b], true);
-  __syncthreads();
-  if (tid < 32) {
-    int carry = 0;
-    if (tid == 0) t.prefix[0] = 0;
+__device__ __forceinline__ int span_pages(int total, int grid_x, int min_pages) {
+  const int per = (total + grid_x - 1) / grid_x;
+  return per > min_pages ? per : min_pages;
+}
+
+// Fills the table and block g's span; run by warp 0 alone.  kHint: the pass
+// that runs before griddepcontrol.wait, whose results only aim prefetches.
+// Its seq_lens reads go through ld.global.cg, so no line that might still
+// change is kept in L1, and it reports nothing.
+template <bool kHint>
+__device__ __forceinline__ void scan_seq_lens(const DecodeParams& p, SeqTable& t, int g) {
+  const int lane = threadIdx.x;
+  {
+    // pass 1: lengths, prefix sums of visible pages, non-empty sequences
+    int carry = 0, nonempty = 0;
+    if (lane == 0) t.prefix[0] = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
-      const int b = b0 + tid;
-      int v = b < p.batch ? visible_pages(t.len[b], p.window) : 0;
+      const int b = b0 + lane;
+      const int L = b < p.batch ? clamp_len(p, kHint ? __ldcg(p.seq_lens + b) : p.seq_lens[b], !kHint) : 0;
+      int v = visible_pages(L, p.window);
+      nonempty += __popc(__ballot_sync(0xffffffffu, v > 0));
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
-        if (tid >= o) v += u;
+        if (lane >= o) v += u;
       }
-      if (b < p.batch) t.prefix[b + 1] = carry + v;
+      if (b < p.batch) {
+        t.len[b] = L;
+        t.prefix[b + 1] = carry + v;
+      }
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
+    __syncwarp();
+    // block g's weighted range [w0, w1) and the real pages it maps to
+    const int total = carry + kSeqWeight * nonempty;
+    const int per = span_pages(total, p.grid_x, p.min_pages);
+    const long long u0 = static_cast<long long>(g) * per;
+    const int w0 = u0 < total ? static_cast<int>(u0) : total;
+    const int w1 = w0 + per < total ? w0 + per : total;
+    // pass 2: weighted prefix wprefix[b] = prefix[b] + kSeqWeight * (non-empty
+    // sequences before b); for u < total the owner of weighted position u is
+    // the largest b with wprefix[b] <= u (on a run of equal values, the
+    // non-empty sequence that ends it).
+    int own0 = 0, wp0 = 0, own1 = 0, wp1 = 0, before = 0;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      const int b = b0 + lane;
+      const bool in = b < p.batch;
+      const unsigned ne = __ballot_sync(0xffffffffu, in && t.len[b] > 0);
+      const int wp = in ? t.prefix[b] + kSeqWeight * (before + __popc(ne & lt)) : 0;
+      const unsigned c0 = __ballot_sync(0xffffffffu, in && wp <= w0);
+      const unsigned c1 = __ballot_sync(0xffffffffu, in && wp <= w1);
+      if (c0) {
+        const int l = 31 - __clz(c0);
+        own0 = b0 + l;
+        wp0 = __shfl_sync(0xffffffffu, wp, l);
+      }
+      if (c1) {
+        const int l = 31 - __clz(c1);
+        own1 = b0 + l;
+        wp1 = __shfl_sync(0xffffffffu, wp, l);
+      }
+      before += __popc(ne);
+    }
+    if (lane == 0) {
+      const int o0 = w0 - wp0 - kSeqWeight, o1 = w1 - wp1 - kSeqWeight;
+      t.span.begin = w0 >= total ? carry : t.prefix[own0] + (o0 > 0 ? o0 : 0);
+      t.span.end = w1 >= total ? carry : t.prefix[own1] + (o1 > 0 ? o1 : 0);
+    }
+  }
+  __syncwarp();
+}
+
+// Before griddepcontrol.wait: the table from hint reads.  Called by every
+// thread of the block; ends with __syncthreads.
+__device__ __forceinline__ void build_seq_table_hint(const DecodeParams& p, SeqTable& t, int g) {
+  if (threadIdx.x < 32) scan_seq_lens<true>(p, t, g);
+  __syncthreads();
+}
+
+// After griddepcontrol.wait: re-reads seq_lens and rebuilds the table only if
+// a length differs from the hint pass (t.rebuilt tells the producer), so in
+// the usual case the schedule costs one read here.  Called by every thread of
+// the block; ends with a __syncthreads that also publishes anything written
+// before it.  From here on the table is exact.
+__device__ __forceinline__ void confirm_seq_table(const DecodeParams& p, SeqTable& t, int g) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    bool differ = false;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      const int b = b0 + lane;
+      const int L = b < p.batch ? clamp_len(p, p.seq_lens[b], true) : 0;
+      differ |= __any_sync(0xffffffffu, b < p.batch && L != t.len[b]);
+    }
+    __syncwarp();
+    if (differ) scan_seq_lens<false>(p, t, g);
+    if (lane == 0) t.rebuilt = differ;
   }
   __syncthreads();
 }
 
-// The sequence holding flattened page f: the largest b < batch with prefix[b] <= f.
+// The sequence holding flattened page f: the largest b < batch with
+// prefix[b] <= f (on a run of equal values, the non-empty sequence that ends it).
 __device__ __forceinline__ int seq_of(const SeqTable& t, int batch, int f) {
   int lo = 0, hi = batch - 1;
   while (lo < hi) {
@@ -103,23 +199,34 @@ __device__ __forceinline__ int seq_of(const SeqTable& t, int batch, int f) {
   return lo;
 }
 
-struct Span {
-  int begin, end;  // flattened pages of this block
-};
-
-__device__ __forceinline__ int span_pages(int total, int grid_x, int min_pages) {
-  const int per = (total + grid_x - 1) / grid_x;
-  return per > min_pages ? per : min_pages;
+// Run by one warp before griddepcontrol.wait, on a table built with kHint:
+// lane i looks up page i of the span (i < n) and calls warm(y) with its row
+// coordinate in the pools, to pull it into L2 while the previous kernel in
+// the stream finishes.  Anything read here may be stale, which costs at most
+// a useless prefetch: every index is range-checked, the block-table read
+// bypasses L1, and nothing is written.
+template <typename Warm>
+__device__ __forceinline__ void warm_first_pages(const DecodeParams& p, const SeqTable& t, int n, Warm warm) {
+  const int lane = threadIdx.x & 31;
+  const int f = t.span.begin + lane;
+  if (lane >= n || f >= t.span.end) return;
+  const int b = seq_of(t, p.batch, f);
+  const int lp = first_visible(t.len[b], p.window) / kPage + (f - t.prefix[b]);
+  if (lp < 0 || lp >= p.max_blocks) return;
+  const int phys = __ldcg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lp);
+  if (phys >= 0 && static_cast<int64_t>(phys) < p.num_pages) warm(phys * kPage);
 }
 
-__device__ __forceinline__ Span block_span(const DecodeParams& p, const SeqTable& t, int g) {
-  const int total = t.prefix[p.batch];
-  const int per = span_pages(total, p.grid_x, p.min_pages);
-  Span s;
-  const long long b0 = static_cast<long long>(g) * per;
-  s.begin = b0 < total ? static_cast<int>(b0) : total;
-  s.end = s.begin + per < total ? s.begin + per : total;
-  return s;
+// Before griddepcontrol.wait, by threads [0, n): pull into L2 the `bytes` of q
+// (from element `offset` of its sequence's [Hq, D] block) that the
+// consumers load first: the span's first sequence, as the hint table has it.
+__device__ __forceinline__ void warm_q(const DecodeParams& p, const SeqTable& t, int hq_d, int offset, int bytes,
+                                       int n) {
+  if (t.span.end <= t.span.begin) return;
+  const int b = seq_of(t, p.batch, t.span.begin);
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(p.q + static_cast<size_t>(b) * hq_d + offset);
+  const int i = threadIdx.x;  // one 128-byte line each
+  if (i < n && i * 128 < bytes) prefetch_l2(base + i * 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -154,23 +261,32 @@ __device__ __forceinline__ void store_out2(const DecodeParams& p, size_t idx, fl
 // returns, the warp waits (bounded) until every copy it issued has landed,
 // so no copy is in flight when the block retires.
 // ---------------------------------------------------------------------------
+// Block-table entry of page i of span sp (0 past its end).  A logical page
+// outside the table cannot come from a consistent schedule: it gives -1 and,
+// with report_it, ATTN_DEV_INTERNAL.  The producer also calls it while the
+// table may still be rebuilt (report_it false, result discarded then), so
+// every index is range-checked whatever the table holds.
+__device__ __forceinline__ int page_entry(const DecodeParams& p, const SeqTable& t, const Span& sp, int i,
+                                          bool report_it) {
+  if (i < 0 || i >= sp.end - sp.begin) return 0;
+  const int f = sp.begin + i;
+  const int b = seq_of(t, p.batch, f);
+  const int lp = first_visible(t.len[b], p.window) / kPage + (f - t.prefix[b]);
+  if (lp < 0 || lp >= p.max_blocks) {
+    if (report_it) report(p.status, ATTN_DEV_INTERNAL);
+    return -1;
+  }
+  return p.block_table[static_cast<int64_t>(b) * p.max_blocks + lp];
+}
+
+// first: this lane's page_entry(sp, lane), read ahead by the caller.
 template <int kStages, int kTxBytes, typename Issue>
 __device__ __forceinline__ void produce_pages(const DecodeParams& p, const SeqTable& t, const Span& sp,
-                                              uint64_t* full, uint64_t* empty, Issue issue) {
+                                              uint64_t* full, uint64_t* empty, int first, Issue issue) {
   const int lane = threadIdx.x & 31;
   const int n_pages = sp.end - sp.begin;
-  auto entry = [&](int i) -> int {
-    if (i >= n_pages) return 0;
-    const int f = sp.begin + i;
-    const int b = seq_of(t, p.batch, f);
-    const int lp = first_visible(t.len[b], p.window) / kPage + (f - t.prefix[b]);
-    if (lp < 0 || lp >= p.max_blocks) {  // cannot happen for a consistent schedule
-      report(p.status, ATTN_DEV_INTERNAL);
-      return -1;
-    }
-    return p.block_table[static_cast<int64_t>(b) * p.max_blocks + lp];
-  };
-  int nxt = entry(lane);
+  auto entry = [&](int i) -> int { return page_entry(p, t, sp, i, true); };
+  int nxt = first;
   int cur = 0;
   int issued = 0;
   bool ok = true;

@@ -41,7 +41,9 @@ constexpr int kPageBytes = kPage * kD * 2;          // 16 KB
 constexpr int kStages = 3;
 constexpr int kBlocksPerSm = 2;
 constexpr int kMinPages = 4;
-constexpr int kShortSpanPages = 32;  // below this many pages per block the plan uses one block per SM
+constexpr int kWarmPages = 2;  // pages per block pulled into L2 before the wait (32 KB each)
+constexpr float kRescaleSlack = 8.f;  // log2 units: exponentials stay below 256
+constexpr int kAhead = 2;  // ldmatrix fragments read ahead of their MMAs
 
 static_assert(kHq == 16, "the m16n8k16 tiling uses the 16 query heads as the M dimension");
 
@@ -71,7 +73,6 @@ __global__ void __launch_bounds__(kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  allow_dependent_launch();
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
@@ -79,20 +80,41 @@ __global__ void __launch_bounds__(kThreads)
     }
     fence_mbar_init();
   }
-  build_seq_table(p, s.table);  // ends with __syncthreads
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+  }
+  // With a programmatic launch this prologue overlaps the previous kernel in
+  // the stream, whose writes (q, the cache, the tables, the workspace it
+  // reads) are complete and visible only once griddepcontrol.wait returns.
+  // Until then the block writes nothing outside its shared memory: it builds
+  // the schedule from hint reads and pulls its first pages into L2.
+  build_seq_table_hint(p, s.table, gb);  // ends with __syncthreads
+  if (warp == kConsumerWarps) {
+    warm_first_pages(p, s.table, kWarmPages, [&](int32_t y) {
+      // a page is 16 contiguous rows of D elements in each pool
+      bulk_prefetch_l2(p.k_pool + static_cast<size_t>(y) * kD, kPageBytes);
+      bulk_prefetch_l2(p.v_pool + static_cast<size_t>(y) * kD, kPageBytes);
+    });
+  } else {
+    warm_q(p, s.table, kHq * kD, 0, kHq * kD * 2, kConsumerWarps * 32);
+  }
+  wait_for_primary_grid();
+  allow_dependent_launch();
+  // The producer reads its first block-table entries while warp 0 confirms
+  // the table; it reads them again if the table had to be rebuilt.
+  int first = warp == kConsumerWarps ? page_entry(p, s.table, s.table.span, lane, false) : 0;
+  confirm_seq_table(p, s.table, gb);  // ends with __syncthreads
   const SeqTable& t = s.table;
-  const Span sp = block_span(p, t, gb);
+  const Span sp = t.span;
   const int n_pages = sp.end - sp.begin;
   if (n_pages <= 0) return;
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
-    if (lane == 0) {
-      prefetch_tensor_map(&tm_k);
-      prefetch_tensor_map(&tm_v);
-    }
     const uint64_t policy = l2_policy_evict_first();
-    produce_pages<kStages, 2 * kPageBytes>(p, t, sp, s.full, s.empty, [&](int stage, int32_t y) {
+    if (t.rebuilt) first = page_entry(p, t, sp, lane, true);
+    produce_pages<kStages, 2 * kPageBytes>(p, t, sp, s.full, s.empty, first, [&](int stage, int32_t y) {
 #pragma unroll
       for (int ch = 0; ch < kChunks; ++ch)
         tma_load_2d_hint(s.k[stage] + ch * kChunkBytes, &tm_k, ch * kChunk, y, &s.full[stage], policy);
@@ -169,19 +191,28 @@ __global__ void __launch_bounds__(kThreads)
 
     // ---- partial S over this warp's dims: two n-tiles of 8 positions; even
     //      and odd k-steps accumulate separately (two chains of 4 MMAs) ----
+    //      The K fragments are read kAhead k-steps before their MMAs.
     float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      auto k_frag = [&](int ks, uint32_t (&b)[4]) {
+        const int ch = 2 * warp + (ks >> 2);
+        const int row = ((mi >> 1) << 3) + lr;
+        const int unit = 2 * (ks & 3) + (mi & 1);
+        ldmatrix_x4(kst + ch * kChunkBytes + swz(row, unit), b[0], b[1], b[2], b[3]);
+      };
+      uint32_t kb[kAhead + 1][4];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int ch = 2 * warp + (ks >> 2);
-      const int row = ((mi >> 1) << 3) + lr;
-      const int unit = 2 * (ks & 3) + (mi & 1);
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4(kst + ch * kChunkBytes + swz(row, unit), b0, b1, b2, b3);
-      float (&s0)[4] = (ks & 1) ? so[0] : se[0];
-      float (&s1)[4] = (ks & 1) ? so[1] : se[1];
-      mma_bf16_16816(s0, qa[ks], b0, b1);
-      mma_bf16_16816(s1, qa[ks], b2, b3);
+      for (int ks = 0; ks < kAhead; ++ks) k_frag(ks, kb[ks]);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        if (ks + kAhead < 8) k_frag(ks + kAhead, kb[(ks + kAhead) % (kAhead + 1)]);
+        const uint32_t (&b)[4] = kb[ks % (kAhead + 1)];
+        float (&s0)[4] = (ks & 1) ? so[0] : se[0];
+        float (&s1)[4] = (ks & 1) ? so[1] : se[1];
+        mma_bf16_16816(s0, qa[ks], b[0], b[1]);
+        mma_bf16_16816(s1, qa[ks], b[2], b[3]);
+      }
     }
 
     // ---- sum the four partials in a fixed order ----
@@ -205,32 +236,48 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---- masked online softmax (log2 units) ----
-    // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*tq + (e&1)
+    // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*tq + (e&1).
+    // Positions outside [lo, L) get -inf (pages inside the range skip the
+    // test); the factor log2(e) is applied inside the exponent.
+    if (pos0 < cur.lo || pos0 + kPage > cur.L) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int pos = pos0 + 8 * nt + 2 * tq + (e & 1);
-        sc[nt][e] = (pos >= cur.lo && pos < cur.L) ? sc[nt][e] * kLog2e : -INFINITY;
-      }
+        for (int e = 0; e < 4; ++e) {
+          const int pos = pos0 + 8 * nt + 2 * tq + (e & 1);
+          if (pos < cur.lo || pos >= cur.L) sc[nt][e] = -INFINITY;
+        }
+    }
     float mx[2];
     mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
     mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-    float m_use[2], scale[2];
+    // The reference max m of a row moves only when the page's max exceeds it
+    // by more than kRescaleSlack: the exponentials then stay below
+    // 2^kRescaleSlack, and the accumulators are rescaled rarely.  Every term
+    // and the sum share one reference, so the softmax is unchanged.
+    // A row's maximum over the four lanes that share it is needed only when
+    // some score passes the threshold, which after a sequence's first page
+    // is rare: one vote decides.
+    float scale[2] = {1.f, 1.f};
+    if (__any_sync(0xffffffffu, mx[0] * kLog2e > m[0] + kRescaleSlack || mx[1] * kLog2e > m[1] + kRescaleSlack)) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-      const float m_new = fmaxf(m[rr], mx[rr]);
-      m_use[rr] = m_new == -INFINITY ? 0.f : m_new;
-      scale[rr] = exp2f(m[rr] - m_use[rr]);
-      m[rr] = m_new;
+      for (int rr = 0; rr < 2; ++rr) {
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+        const float cand = mx[rr] * kLog2e;
+        const float m_new = cand > m[rr] + kRescaleSlack ? cand : m[rr];
+        scale[rr] = m_new == m[rr] ? 1.f : ex2_approx(m[rr] - m_new);  // 0 on the first visible page
+        m[rr] = m_new;
+      }
     }
+    float m_use[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) m_use[rr] = m[rr] == -INFINITY ? 0.f : m[rr];
     float pr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(sc[nt][e] - m_use[e >> 1]);
+      for (int e = 0; e < 4; ++e) pr[nt][e] = ex2_approx(fmaf(sc[nt][e], kLog2e, -m_use[e >> 1]));
     l[0] = l[0] * scale[0] + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
     l[1] = l[1] * scale[1] + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
     // rescale only when some row's running max moved (multiplying by 1 is exact)
@@ -262,15 +309,23 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---- O += P V over this warp's 128 dims ----
+    {
+      auto v_frag = [&](int np, uint32_t (&b)[4]) {
+        const int ch = 2 * warp + (np >> 2);
+        const int row = ((mi & 1) << 3) + lr;
+        const int unit = 2 * (np & 3) + (mi >> 1);
+        ldmatrix_x4_trans(vst + ch * kChunkBytes + swz(row, unit), b[0], b[1], b[2], b[3]);
+      };
+      uint32_t vb[kAhead + 1][4];
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      const int ch = 2 * warp + (np >> 2);
-      const int row = ((mi & 1) << 3) + lr;
-      const int unit = 2 * (np & 3) + (mi >> 1);
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(vst + ch * kChunkBytes + swz(row, unit), b0, b1, b2, b3);
-      mma_bf16_16816(acc[2 * np], pa, b0, b1);
-      mma_bf16_16816(acc[2 * np + 1], pa, b2, b3);
+      for (int np = 0; np < kAhead; ++np) v_frag(np, vb[np]);
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        if (np + kAhead < 8) v_frag(np + kAhead, vb[(np + kAhead) % (kAhead + 1)]);
+        const uint32_t (&b)[4] = vb[np % (kAhead + 1)];
+        mma_bf16_16816(acc[2 * np], pa, b[0], b[1]);
+        mma_bf16_16816(acc[2 * np + 1], pa, b[2], b[3]);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[stage]);

@@ -36,6 +36,7 @@ constexpr int kTileBytes = kPage * kRowBytes;          // 8 KB per K (or V) page
 constexpr int kStages = 4;
 constexpr int kBlocksPerSm = 3;
 constexpr int kMinPages = 4;
+constexpr int kWarmPages = 4;  // pages per block pulled into L2 before the wait
 
 static_assert(kG == 2, "the lane mapping below assumes two query heads per KV head");
 
@@ -63,7 +64,6 @@ __global__ void __launch_bounds__(kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  allow_dependent_launch();
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
@@ -71,21 +71,41 @@ __global__ void __launch_bounds__(kThreads)
     }
     fence_mbar_init();
   }
-  build_seq_table(p, s.table);  // ends with __syncthreads
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+  }
+  // With a programmatic launch this prologue overlaps the previous kernel in
+  // the stream, whose writes (q, the cache, the tables, the workspace it
+  // reads) are complete and visible only once griddepcontrol.wait returns.
+  // Until then the block writes nothing outside its shared memory: it builds
+  // the schedule from hint reads and pulls its first pages into L2.
+  build_seq_table_hint(p, s.table, g);  // ends with __syncthreads
+  if (warp == kConsumerWarps) {
+    warm_first_pages(p, s.table, kWarmPages, [&](int32_t y) {
+      tma_prefetch_2d(&tm_k, c * kD, y);
+      tma_prefetch_2d(&tm_v, c * kD, y);
+    });
+  } else {
+    warm_q(p, s.table, kHq * kD, c * kG * kD, kG * kD * 2, kConsumerWarps * 32);
+  }
+  wait_for_primary_grid();
+  allow_dependent_launch();
+  // The producer reads its first block-table entries while warp 0 confirms
+  // the table; it reads them again if the table had to be rebuilt.
+  int first = warp == kConsumerWarps ? page_entry(p, s.table, s.table.span, lane, false) : 0;
+  confirm_seq_table(p, s.table, g);  // ends with __syncthreads
   const SeqTable& t = s.table;
-  const Span sp = block_span(p, t, g);
+  const Span sp = t.span;
   const int n_pages = sp.end - sp.begin;
   if (n_pages <= 0) return;
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
-    if (lane == 0) {
-      prefetch_tensor_map(&tm_k);
-      prefetch_tensor_map(&tm_v);
-    }
     const uint64_t policy = l2_policy_evict_first();
     const int x = c * kD;
-    produce_pages<kStages, 2 * kTileBytes>(p, t, sp, s.full, s.empty, [&](int stage, int32_t y) {
+    if (t.rebuilt) first = page_entry(p, t, sp, lane, true);
+    produce_pages<kStages, 2 * kTileBytes>(p, t, sp, s.full, s.empty, first, [&](int stage, int32_t y) {
       tma_load_2d_hint(s.k[stage], &tm_k, x, y, &s.full[stage], policy);
       tma_load_2d_hint(s.v[stage], &tm_v, x, y, &s.full[stage], policy);
     });
