@@ -142,6 +142,27 @@ int32_t encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, i
   return ATTN_OK;
 }
 
+// The global pool [num_pages*16 rows][512] seen as a 3-D tensor (x: 64 dims
+// of a chunk, y: row, z: chunk of 64 dims, stride 128 bytes), so that one
+// box {64, 16, 8} copies a whole page as 8 swizzled tiles of [16 rows][64],
+// the layout the consumers read with ldmatrix.
+int32_t encode_global_page_map(CUtensorMap* map, const void* pool, int64_t num_pages) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  constexpr int kChunk = pda::global::kChunk;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kChunk), static_cast<cuuint64_t>(num_pages) * ATTN_PAGE_SIZE,
+                              static_cast<cuuint64_t>(ATTN_GLOBAL_D / kChunk)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ATTN_GLOBAL_D) * 2, static_cast<cuuint64_t>(kChunk) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), ATTN_PAGE_SIZE,
+                             static_cast<cuuint32_t>(ATTN_GLOBAL_D / kChunk)};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
+                   elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (page map) failed (%d)", static_cast<int>(r));
+  return ATTN_OK;
+}
+
 template <typename Kernel>
 int32_t ensure_smem(Kernel kernel, size_t bytes, int dev, bool* done) {
   if (done[dev]) return ATTN_OK;
@@ -269,9 +290,8 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
                      dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, 0,
                      s, p);
   } else {
-    const int row = ATTN_GLOBAL_HKV * ATTN_GLOBAL_D;
-    if ((st = encode_pool_map(&tm_k, k_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
-    if ((st = encode_pool_map(&tm_v, v_pool, num_pages, row, pda::global::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
+    if ((st = encode_global_page_map(&tm_k, k_pool, num_pages))) return st;
+    if ((st = encode_global_page_map(&tm_v, v_pool, num_pages))) return st;
     static bool smem_set[kMaxDevices] = {false};
     if ((st = ensure_smem(pda::global::decode_kernel, pda::global::kSmemBytes, dev, smem_set))) return st;
     static bool comb_set[kMaxDevices] = {false};

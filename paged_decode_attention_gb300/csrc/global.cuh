@@ -115,12 +115,9 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t policy = l2_policy_evict_first();
     if (t.rebuilt) first = page_entry(p, t, sp, lane, true);
     produce_pages<kStages, 2 * kPageBytes>(p, t, sp, s.full, s.empty, first, [&](int stage, int32_t y) {
-#pragma unroll
-      for (int ch = 0; ch < kChunks; ++ch)
-        tma_load_2d_hint(s.k[stage] + ch * kChunkBytes, &tm_k, ch * kChunk, y, &s.full[stage], policy);
-#pragma unroll
-      for (int ch = 0; ch < kChunks; ++ch)
-        tma_load_2d_hint(s.v[stage] + ch * kChunkBytes, &tm_v, ch * kChunk, y, &s.full[stage], policy);
+      // one copy per pool: the page's 16 rows as kChunks tiles of [16][64]
+      tma_load_3d_hint(s.k[stage], &tm_k, 0, y, 0, &s.full[stage], policy);
+      tma_load_3d_hint(s.v[stage], &tm_v, 0, y, 0, &s.full[stage], policy);
     });
     return;
   }
