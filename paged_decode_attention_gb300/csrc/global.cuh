@@ -42,7 +42,6 @@ constexpr int kStages = 3;
 constexpr int kBlocksPerSm = 2;
 constexpr int kMinPages = 4;
 constexpr int kWarmPages = 2;  // pages per block pulled into L2 before the wait (32 KB each)
-constexpr float kRescaleSlack = 8.f;  // log2 units: exponentials stay below 256
 constexpr int kAhead = 2;  // ldmatrix fragments read ahead of their MMAs
 
 static_assert(kHq == 16, "the m16n8k16 tiling uses the 16 query heads as the M dimension");
@@ -248,21 +247,18 @@ __global__ void __launch_bounds__(kThreads)
     float mx[2];
     mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
     mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-    // The reference max m of a row moves only when the page's max exceeds it
-    // by more than kRescaleSlack: the exponentials then stay below
-    // 2^kRescaleSlack, and the accumulators are rescaled rarely.  Every term
-    // and the sum share one reference, so the softmax is unchanged.
-    // A row's maximum over the four lanes that share it is needed only when
-    // some score passes the threshold, which after a sequence's first page
-    // is rare: one vote decides.
+    // The running max of a row changes only when some score exceeds it, which
+    // after a sequence's first pages is rare: one vote decides whether the
+    // row maxima over the four lanes that share a row are needed at all.
+    // Tracking the exact max keeps the largest weight at exactly 1, so the
+    // dominant term of P carries no bf16 rounding.
     float scale[2] = {1.f, 1.f};
-    if (__any_sync(0xffffffffu, mx[0] * kLog2e > m[0] + kRescaleSlack || mx[1] * kLog2e > m[1] + kRescaleSlack)) {
+    if (__any_sync(0xffffffffu, mx[0] * kLog2e > m[0] || mx[1] * kLog2e > m[1])) {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-        const float cand = mx[rr] * kLog2e;
-        const float m_new = cand > m[rr] + kRescaleSlack ? cand : m[rr];
+        const float m_new = fmaxf(m[rr], mx[rr] * kLog2e);
         scale[rr] = m_new == m[rr] ? 1.f : ex2_approx(m[rr] - m_new);  // 0 on the first visible page
         m[rr] = m_new;
       }
