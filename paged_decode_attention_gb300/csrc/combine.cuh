@@ -26,7 +26,8 @@ namespace pda {
 
 constexpr int kCombineCols = 128;  // dims per combine block
 constexpr int kCombineWarps = 4;
-constexpr int kPerWarp = 12;       // partials a warp keeps in flight per round
+constexpr int kPerWarp = 8;        // partials a warp keeps in flight per round (74 registers: one
+                                   // block fits beside the decode blocks of an SM)
 
 template <int kD>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ DecodeParams p) {
