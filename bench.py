@@ -396,48 +396,94 @@ def _packed_inputs(c, dev):
 
 
 def run_e2e(args, plans, n_sets, stream, status, dev):
-    """Per step and call: one H2D copy of the packed q, block_table and seq_lens
-    from pinned memory, the API call (a prepared call of the public binding),
-    and a D2H copy of o into pinned memory.  The KV cache stays resident."""
+    """End to end through the public binding.  Every step, for every call: an
+    H2D copy of its packed q, block_table and seq_lens from pinned memory, the
+    call (a PreparedDecode of the binding), and a D2H copy of o into pinned
+    memory; the KV cache stays resident.  Steps are pipelined as a serving
+    loop runs them: step i's input copy and step i-1's output copy run on
+    their own streams while the compute stream works, input and output
+    buffers alternate between two sets, and events order every reuse.  The K
+    steps are captured as one CUDA graph (eager with --no-graph)."""
     import torch
     import paged_decode_attention_gb300 as pda
-    staged = []
+    staged = []  # staged[set][parity] = [(host, device, prepared call, o, pinned o), ...]
     for pl in plans:
-        calls = []
-        for c, ws, o in pl:
-            hbuf, dbuf, (qv, btv, slv) = _packed_inputs(c, dev)
-            prep = pda.PreparedDecode(pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL,
-                                      qv, c.k_pool, c.v_pool, btv, slv, o, window=c.window,
-                                      max_seq_len=c.max_seq_len, num_splits=NUM_SPLITS, workspace=ws,
-                                      status=status)
-            calls.append((hbuf, dbuf, prep, torch.empty(o.shape, dtype=o.dtype).pin_memory()))
-        staged.append(calls)
-    h2d = sum(hbuf.numel() for hbuf, _, _, _ in staged[0])
-    d2h = sum(oh.numel() * oh.element_size() for _, _, _, oh in staged[0])
+        per_parity = []
+        for par in range(2):
+            calls = []
+            for c, ws, o in pl:
+                hbuf, dbuf, (qv, btv, slv) = _packed_inputs(c, dev)
+                o_dev = o if par == 0 else torch.empty_like(o)
+                prep = pda.PreparedDecode(pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL,
+                                          qv, c.k_pool, c.v_pool, btv, slv, o_dev, window=c.window,
+                                          max_seq_len=c.max_seq_len, num_splits=NUM_SPLITS, workspace=ws,
+                                          status=status)
+                calls.append((hbuf, dbuf, prep, o_dev, torch.empty(o.shape, dtype=o.dtype).pin_memory()))
+            per_parity.append(calls)
+        staged.append(per_parity)
+    h2d = sum(hbuf.numel() for hbuf, _, _, _, _ in staged[0][0])
+    d2h = sum(oh.numel() * oh.element_size() for _, _, _, _, oh in staged[0][0])
     steps = max(3, min(args.steps, 200))
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of a parity copied
+    ev_comp = [torch.cuda.Event() for _ in range(2)]  # its calls done
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # its outputs read back
 
-    def one(i):
-        for hbuf, dbuf, prep, oh in staged[i % n_sets]:
-            dbuf.copy_(hbuf, non_blocking=True)
-            oh.copy_(prep.run(stream), non_blocking=True)
+    def run_steps(n):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        for i in range(n):
+            par = i % 2
+            calls = staged[i % n_sets][par]
+            if i >= 2:
+                s_in.wait_event(ev_comp[par])  # step i-2 no longer reads these inputs
+            with torch.cuda.stream(s_in):
+                for hbuf, dbuf, _, _, _ in calls:
+                    dbuf.copy_(hbuf, non_blocking=True)
+            ev_in[par].record(s_in)
+            stream.wait_event(ev_in[par])
+            if i >= 2:
+                stream.wait_event(ev_out[par])  # step i-2's outputs have been read back
+            for _, _, prep, _, _ in calls:
+                prep.run(stream)
+            ev_comp[par].record(stream)
+            s_out.wait_event(ev_comp[par])
+            with torch.cuda.stream(s_out):
+                for _, _, _, o_dev, oh in calls:
+                    oh.copy_(o_dev, non_blocking=True)
+            ev_out[par].record(s_out)
+        for par in range(min(n, 2)):  # join
+            stream.wait_event(ev_out[par])
 
     with torch.cuda.stream(stream):
-        for i in range(3):
-            one(i)
-    stream.synchronize()
+        run_steps(3)
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            run_steps(steps)
+        graph.replay()  # warm
+        torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(steps):
-            one(i)
+        if graph is not None:
+            graph.replay()
+        else:
+            run_steps(steps)
         e1.record(stream)
     e1.synchronize()
     ms = e0.elapsed_time(e1)
     step_bytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c, _, _ in plans[0])
     return {"value": round(step_bytes * steps / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(ms / steps, 6)}
+            "ms_per_step": round(ms / steps, 6),
+            "pipelined": "input copy, calls and output copy of consecutive steps overlap on 3 streams"}
 
 
 # ---------------------------------------------------------------------------
