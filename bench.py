@@ -364,9 +364,47 @@ def run_ours(args, rank, world, local_rank):
     hc = calls0[heavy]
     heavy_bytes = algorithmic_bytes(hc.kind, hc.seq_lens_host, hc.window)
 
+    # --- mixed workloads: each layer type's calls of one step, timed apart ---
+    per_type = {}
+    kinds = sorted(set(c.kind for c in calls0))
+    if len(kinds) > 1:
+        for kind in kinds:
+            idx = [j for j, c in enumerate(calls0) if c.kind == kind]
+
+            def launch_kind(i, idx=idx):
+                for j in idx:
+                    c, ws, o = plans[i % n_sets][j]
+                    fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
+                    fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
+                       max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
+                       num_splits=NUM_SPLITS)
+            kg = None
+            if not args.no_graph:
+                kg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(kg, stream=stream):
+                    launch_kind(0)
+            kind_step = (lambda i: kg.replay()) if kg is not None else launch_kind  # noqa: E731
+            with torch.cuda.stream(stream):
+                kind_step(0)
+            stream.synchronize()
+            k0 = torch.cuda.Event(enable_timing=True)
+            k1 = torch.cuda.Event(enable_timing=True)
+            krounds = 5
+            with torch.cuda.stream(stream):
+                k0.record(stream)
+                for i in range(krounds):
+                    kind_step(i)
+                k1.record(stream)
+            k1.synchronize()
+            kms = k0.elapsed_time(k1) / krounds
+            kbytes = sum(algorithmic_bytes(calls0[j].kind, calls0[j].seq_lens_host, calls0[j].window) for j in idx)
+            per_type[kind] = {"calls_per_step": len(idx), "ms_per_step": round(kms, 6),
+                              "value": round(kbytes / (kms * 1e-3) / 1e9, 2), "unit": UNIT}
+
     # --- end to end through the public API with host buffers ---
     e2e = run_e2e(args, plans, n_sets, stream, status, dev)
 
+    res.update(per_type=per_type)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
                heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
                launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
@@ -490,7 +528,7 @@ def run_e2e(args, plans, n_sets, stream, status, dev):
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(cfg, budget_s=2.0):
+def oracle_sample(cfg, budget_s=2.0, threads=None):
     """A bounded sample of workload `cfg` for the fp64 oracle: (callable, bytes, description)."""
     import numpy as np
     import oracle
@@ -514,7 +552,8 @@ def oracle_sample(cfg, budget_s=2.0):
         acc += n * per_pos_s
     case = make_case(kind, take, seed=5150, device="cpu", window=window,
                      window_only=(kind == "sliding"), poison=False)
-    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    if threads is None:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     args = (bits(case.q), bits(case.k_pool), bits(case.v_pool), case.block_table.numpy(),
             case.seq_lens.numpy(), case.window)
 
@@ -528,16 +567,23 @@ def oracle_sample(cfg, budget_s=2.0):
 
 
 def cpu_baseline(cfg, budget_s=2.0, reps=3):
-    run, nbytes, desc, threads = oracle_sample(cfg, budget_s)
-    run()
-    t = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
+    """The oracle on all the host cores the process may use, and on one core
+    (over a sample scaled down by the core count)."""
+    def timed(run):
         run()
-        t.append(time.perf_counter() - t0)
-    sec = min(t)
+        t = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            run()
+            t.append(time.perf_counter() - t0)
+        return min(t)
+    run, nbytes, desc, threads = oracle_sample(cfg, budget_s)
+    sec = timed(run)
+    run1, nbytes1, desc1, _ = oracle_sample(cfg, budget_s / max(threads, 1), threads=1)
+    sec1 = timed(run1)
     return {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": desc, "seconds_per_sample": round(sec, 4)}
+            "sample": desc, "seconds_per_sample": round(sec, 4),
+            "one_core": {"value": round(nbytes1 / sec1 / 1e9, 4), "unit": UNIT, "sample": desc1}}
 
 
 def run_reference(args, rank, world):
@@ -646,6 +692,9 @@ def main(argv=None):
                         "kernel": "%s decode (%d launch%s per call, timed together)"
                         % (r0["heavy_kind"], r0["heavy_kernels"], "es" if r0["heavy_kernels"] > 1 else "")}
     line["hbm_frac_of_peak"] = round(line["value"] / peak, 4)
+    if r0.get("per_type"):
+        line["per_layer_type"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4))
+                                  for k, v in r0["per_type"].items()}
     line["gpu_launches"] = r0["launches_per_step"] * args.steps
     line["e2e"] = r0["e2e"]
     line["clocks"] = r0["clocks"]
