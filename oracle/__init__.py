@@ -7,6 +7,8 @@ never imports the CUDA library.
 
 * ``decode_paged`` -- the paged decode oracle in ``oracle.c`` (plain C,
   double precision, pthreads over output rows), called through ctypes.
+* ``qkv_append``   -- the per-head norms, RoPE and paged KV-cache append of
+  one new token per sequence (``oracle.c``, double precision).
 * ``dense``        -- the literal Lean definitions over unpaged arrays, for
   tiny cases (see ``dense.py``).
 
@@ -67,6 +69,16 @@ def _load(lib_path=None):
             ctypes.c_void_p, ctypes.c_int32,                     # rows, n_rows
             ctypes.c_void_p, ctypes.c_int32,                     # out, n_threads
         ]
+        fa = lib.oracle_qkv_append
+        fa.restype = ctypes.c_int
+        fa.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # qkv, w_q, w_k
+            ctypes.c_void_p, ctypes.c_void_p,                    # block_table, positions
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,  # B Hq Hkv D shared
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,      # page_size max_blocks num_pages
+            ctypes.c_double, ctypes.c_int32, ctypes.c_double,    # theta, rope_pairs, eps
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q_out, k_pool, v_pool
+        ]
         _libs[key] = lib
     return _libs[key]
 
@@ -120,3 +132,41 @@ def decode_paged(q_bits, k_bits, v_bits, block_table, seq_lens, window, page_siz
     if st != 0:
         raise OracleError(ERRORS.get(st, "error %d" % st))
     return out
+
+
+def qkv_append(qkv_bits, wq_bits, wk_bits, block_table, positions, q_out, k_pool, v_pool, *, Hq, Hkv, D,
+               shared_kv, theta, rope_pairs, eps=1e-6, page_size=16, lib_path=None):
+    """Norms, RoPE and cache append of one token per sequence, fp64, rounded once to bf16.
+
+    qkv_bits    uint16 [B, Hq*D + (D if shared_kv else 2*Hkv*D)]   (bf16 bit patterns)
+    wq_bits, wk_bits  uint16 [D]   qk_norm weights of q and k
+    block_table int32 [B, max_blocks];  positions int32 [B] (each token's position)
+    q_out       uint16 [B, Hq, D], written
+    k_pool, v_pool  uint16 [num_pages, page_size, Hkv, D]; each token's slot is written
+    Raises OracleError on a position beyond the table or an unmapped page.
+    """
+    qkv_bits = _as(qkv_bits, np.uint16)
+    wq_bits = _as(wq_bits, np.uint16)
+    wk_bits = _as(wk_bits, np.uint16)
+    block_table = _as(block_table, np.int32)
+    positions = _as(positions, np.int32)
+    for name, arr in (("q_out", q_out), ("k_pool", k_pool), ("v_pool", v_pool)):
+        if arr.dtype != np.uint16 or not arr.flags["C_CONTIGUOUS"] or not arr.flags["WRITEABLE"]:
+            raise TypeError("%s must be a writeable C-contiguous uint16 array" % name)
+    B = qkv_bits.shape[0]
+    row_len = Hq * D + (D if shared_kv else 2 * Hkv * D)
+    if qkv_bits.shape != (B, row_len) or wq_bits.shape != (D,) or wk_bits.shape != (D,):
+        raise ValueError("qkv / weight shape")
+    if q_out.shape != (B, Hq, D) or positions.shape != (B,) or block_table.shape[0] != B:
+        raise ValueError("q_out / positions / block_table shape")
+    num_pages = k_pool.shape[0]
+    if k_pool.shape != (num_pages, page_size, Hkv, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("pool shape")
+    st = _load(lib_path).oracle_qkv_append(
+        qkv_bits.ctypes.data, wq_bits.ctypes.data, wk_bits.ctypes.data, block_table.ctypes.data,
+        positions.ctypes.data, B, Hq, Hkv, D, int(bool(shared_kv)), page_size, block_table.shape[1],
+        num_pages, float(theta), int(rope_pairs), float(eps), q_out.ctypes.data, k_pool.ctypes.data,
+        v_pool.ctypes.data)
+    if st != 0:
+        raise OracleError("oracle_qkv_append: %s" % ERRORS.get(st, st))
+    return q_out, k_pool, v_pool

@@ -223,3 +223,121 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_
   free(tids);
   return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/*
+ * The steps that feed attn.core for one new token per sequence: per-head
+ * norms, RoPE, and the append of the token's key and value to the paged
+ * cache.  Gemma-4-12B model page, "Compute-graph nodes":
+ *
+ *   attn.qk_norm  rmsnorm, per head:  y[i] = x[i] / sqrt(sum_j x[j]^2 / D + eps) * w[i]
+ *   attn.v_norm   rmsnormUnit, per head:  y[i] = x[i] / sqrt(sum_j x[j]^2 / D + eps)
+ *   attn.rope     rotate pairs (i, i + D/2) by pos * theta^(-2i/D), i < active;
+ *                 the other coordinates are unchanged
+ *   ("What to watch for": sliding layers theta 10,000 with all 128 pairs of
+ *   D = 256 active; global layers theta 1,000,000 with the first 64 of the
+ *   256 pairs of D = 512 active, and values = keys.)
+ *
+ * The qkv row of token b (the attn.qkv_proj output) is [q: Hq*D | k: Hkv*D |
+ * v: Hkv*D], or with shared_kv [q: Hq*D | x: D], whose one head x gives both
+ * the key (qk_norm, RoPE) and the value (v_norm).  Rotating (a, b) by phi is
+ * (a cos phi - b sin phi, b cos phi + a sin phi).  The token sits at position
+ * pos = positions[b]: its key and value go to page block_table[b, pos/16],
+ * slot pos % 16; q leaves normed and rotated.  Everything is computed in
+ * double from the exact bf16 inputs and rounded once to bf16 (nearest, ties
+ * to even).
+ */
+
+/* double -> bf16 bits, round to nearest, ties to even (finite, normal range). */
+static uint16_t double_to_bf16_rne(double x) {
+  if (x == 0.0) return signbit(x) ? 0x8000u : 0;
+  int e;
+  const double m = frexp(x, &e);          /* x = m * 2^e, 0.5 <= |m| < 1 */
+  const double r = nearbyint(ldexp(m, 8)); /* 8 significant bits, ties to even */
+  const float f = (float)ldexp(r, e - 8);  /* exact in binary32 */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+/* y = x / rms(x) (* w when w != NULL), x and w bf16 bits, D values. */
+static void rms_norm(const uint16_t* x, const uint16_t* w, int D, double eps, double* y) {
+  double ss = 0.0;
+  for (int i = 0; i < D; ++i) {
+    const double v = bf16_bits_to_double(x[i]);
+    ss += v * v;
+  }
+  const double inv = 1.0 / sqrt(ss / D + eps);
+  for (int i = 0; i < D; ++i) y[i] = bf16_bits_to_double(x[i]) * inv * (w ? bf16_bits_to_double(w[i]) : 1.0);
+}
+
+/* Rotate pairs (i, i + D/2), i < pairs, by pos * theta^(-2i/D). */
+static void rope(double* y, int D, int pairs, double theta, int pos) {
+  const int half = D / 2;
+  for (int i = 0; i < pairs; ++i) {
+    const double phi = (double)pos * pow(theta, -2.0 * i / D);
+    const double c = cos(phi), s = sin(phi);
+    const double a = y[i], b = y[i + half];
+    y[i] = a * c - b * s;
+    y[i + half] = b * c + a * s;
+  }
+}
+
+/*
+ * qkv         bf16 bits [B, Hq*D + (shared_kv ? D : 2*Hkv*D)]
+ * w_q, w_k    bf16 bits [D]: the qk_norm weights of q and k
+ * block_table int32 [B, max_blocks]; positions int32 [B]
+ * q_out       bf16 bits [B, Hq, D] (written)
+ * k_pool      bf16 bits [num_pages, page_size, Hkv, D] (the token's slot written)
+ * v_pool      likewise
+ * returns     ORACLE_OK, ORACLE_ERR_ARG, ORACLE_ERR_SEQ_LEN (a position
+ *             beyond the block table) or ORACLE_ERR_UNMAPPED (its page id
+ *             outside [0, num_pages)); nothing is written for that sequence
+ */
+int oracle_qkv_append(const uint16_t* qkv, const uint16_t* w_q, const uint16_t* w_k,
+                      const int32_t* block_table, const int32_t* positions, int32_t B, int32_t Hq,
+                      int32_t Hkv, int32_t D, int32_t shared_kv, int32_t page_size, int32_t max_blocks,
+                      int64_t num_pages, double theta, int32_t rope_pairs, double eps, uint16_t* q_out,
+                      uint16_t* k_pool, uint16_t* v_pool) {
+  if (!qkv || !w_q || !w_k || !block_table || !positions || !q_out || !k_pool || !v_pool) return ORACLE_ERR_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 2 || (D & 1) || page_size < 1 || max_blocks < 1 || num_pages < 1)
+    return ORACLE_ERR_ARG;
+  if (rope_pairs < 0 || rope_pairs > D / 2 || (shared_kv && Hkv != 1)) return ORACLE_ERR_ARG;
+  const int64_t row_len = (int64_t)Hq * D + (shared_kv ? D : 2 * (int64_t)Hkv * D);
+  double* y = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!y) return ORACLE_ERR_NOMEM;
+  int status = ORACLE_OK;
+  for (int b = 0; b < B; ++b) {
+    const uint16_t* row = qkv + (int64_t)b * row_len;
+    const int pos = positions[b];
+    const int page = pos >= 0 ? pos / page_size : -1;
+    if (pos < 0 || page >= max_blocks) {
+      if (status == ORACLE_OK) status = ORACLE_ERR_SEQ_LEN;
+      continue;
+    }
+    const int64_t phys = block_table[(int64_t)b * max_blocks + page];
+    if (phys < 0 || phys >= num_pages) {
+      if (status == ORACLE_OK) status = ORACLE_ERR_UNMAPPED;
+      continue;
+    }
+    const int64_t slot = phys * page_size + pos % page_size;
+    for (int h = 0; h < Hq; ++h) {
+      rms_norm(row + (int64_t)h * D, w_q, D, eps, y);
+      rope(y, D, rope_pairs, theta, pos);
+      for (int i = 0; i < D; ++i) q_out[((int64_t)b * Hq + h) * D + i] = double_to_bf16_rne(y[i]);
+    }
+    for (int c = 0; c < Hkv; ++c) {
+      const uint16_t* xk = row + (int64_t)Hq * D + (shared_kv ? 0 : (int64_t)c * D);
+      const uint16_t* xv = row + (int64_t)Hq * D + (shared_kv ? 0 : ((int64_t)Hkv + c) * D);
+      uint16_t* kd = k_pool + (slot * Hkv + c) * D;
+      uint16_t* vd = v_pool + (slot * Hkv + c) * D;
+      rms_norm(xk, w_k, D, eps, y);
+      rope(y, D, rope_pairs, theta, pos);
+      for (int i = 0; i < D; ++i) kd[i] = double_to_bf16_rne(y[i]);
+      rms_norm(xv, NULL, D, eps, y);
+      for (int i = 0; i < D; ++i) vd[i] = double_to_bf16_rne(y[i]);
+    }
+  }
+  free(y);
+  return status;
+}

@@ -43,6 +43,10 @@ GLOBAL = dict(Hq=16, Hkv=1, D=512, window=0)
 
 N_LAYERS = 48  # layer i is global iff i % 6 == 5
 
+# attn.rope per layer type (model page, "What to watch for" and the attn.rope
+# rows): theta, and the number of active pairs (i, i + D/2)
+ROPE = {"sliding": dict(theta=1.0e4, pairs=128), "global": dict(theta=1.0e6, pairs=64)}
+
 
 def is_global_layer(i):
     return i % 6 == 5
@@ -282,3 +286,50 @@ WORKLOADS = {
     4: "long-context global decode: B=16 x 131072 (variant b: B=4 x 262144), 16/1 heads, D=512",
     5: "Gemma-4-12B decode-step mix: B=64, seq_lens log-uniform [16,262144], 40 sliding + 8 global layers",
 }
+
+
+# ---------------------------------------------------------------------------
+# One new token per sequence for the norm + RoPE + cache-append step
+# ---------------------------------------------------------------------------
+
+@dataclass
+class AppendCase:
+    """The attn.qkv_proj output of one new token per sequence, the qk_norm
+    weights, the token positions, and a cache whose pages cover them."""
+    kind: str
+    qkv: torch.Tensor        # bf16 [B, Hq*D + 2*Hkv*D] (sliding) or [B, Hq*D + D] (global)
+    w_q: torch.Tensor        # bf16 [D]
+    w_k: torch.Tensor        # bf16 [D]
+    positions: torch.Tensor  # int32 [B]
+    cache: DecodeCase        # block table and pools; seq_lens = positions + 1
+
+    @property
+    def shared_kv(self):
+        return self.kind == "global"
+
+    def to(self, device):
+        return AppendCase(self.kind, self.qkv.to(device), self.w_q.to(device), self.w_k.to(device),
+                          self.positions.to(device), self.cache.to(device))
+
+
+def append_row_len(kind):
+    shape = SLIDING if kind == "sliding" else GLOBAL
+    return shape["Hq"] * shape["D"] + (shape["D"] if kind == "global" else 2 * shape["Hkv"] * shape["D"])
+
+
+def make_append_case(kind, positions, seed, device="cpu", scale=1.0, full_cache=False):
+    """Tokens at `positions` (one per sequence), and a cache filled like
+    make_case (no poison, so every other slot keeps a known value) whose pages
+    cover each token's position: with full_cache every position 0..pos (for a
+    decode after the append), else only the token's own page.
+    qkv ~ N(0, scale^2) in bf16."""
+    positions = [int(p) for p in positions]
+    cache = make_case(kind, [p + 1 for p in positions], seed, device=device, poison=False,
+                      **({} if full_cache else dict(window=1, window_only=True)))
+    shape = SLIDING if kind == "sliding" else GLOBAL
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(int(seed) + 11)
+    qkv = (scale * torch.randn((len(positions), append_row_len(kind)), generator=gen, device=device)).to(torch.bfloat16)
+    w_q = _norm_weight(shape["D"], gen, device)
+    w_k = _norm_weight(shape["D"], gen, device)
+    return AppendCase(kind, qkv, w_q, w_k, torch.tensor(positions, dtype=torch.int32, device=device), cache)
