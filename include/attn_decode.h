@@ -92,6 +92,13 @@ extern "C" {
 #define ATTN_GLOBAL_D 512
 #define ATTN_PAGE_SIZE 16
 
+/* attn.rope of each layer type (model page, "What to watch for" and the
+ * attn.rope rows): pairs (i, i + D/2), i < PAIRS, turn by pos * THETA^(-2i/D). */
+#define ATTN_SLIDING_ROPE_THETA 10000.0
+#define ATTN_SLIDING_ROPE_PAIRS 128
+#define ATTN_GLOBAL_ROPE_THETA 1000000.0
+#define ATTN_GLOBAL_ROPE_PAIRS 64
+
 /* Shape domain (Gemma-4-12B model page, "At a glance"): B in [1,256],
  * up to 262144 cached positions. */
 #define ATTN_MAX_BATCH 256
@@ -210,6 +217,46 @@ int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool, const voi
                                     int32_t batch, int32_t max_blocks, int64_t num_pages,
                                     int32_t max_seq_len, int32_t window, int32_t out_dtype,
                                     int32_t num_splits, int32_t* status, void* stream);
+
+/*
+ * attn_kv_append_sliding / attn_kv_append_global -- the steps that feed the
+ * decode for one new token per sequence (Gemma-4-12B model page, "Compute-
+ * graph nodes": attn.qk_norm, attn.v_norm, attn.rope; "What to watch for":
+ * the RoPE constants above and "values = keys" on global layers):
+ *
+ *   q heads  q_out[b,h] = rope(rmsnorm(x_q[b,h]) * w_q, pos)
+ *   key      rope(rmsnorm(x_k) * w_k, pos)  -> k_pool at the token's slot
+ *   value    rmsnormUnit(x_v)                -> v_pool at the token's slot
+ *
+ * with rmsnorm(x)[i] = x[i] / sqrt(sum_j x[j]^2 / D + 1e-6), pos =
+ * positions[b], and the token's slot = page block_table[b, pos/16], row
+ * pos % 16 (so the caller's next decode call has seq_lens[b] = pos + 1).
+ *
+ * qkv          bf16 [batch, row]: the attn.qkv_proj output of the token.
+ *              Sliding: row = [q 16x256 | k 8x256 | v 8x256] (8192).
+ *              Global: row = [q 16x512 | x 512] (8704); x gives both the key
+ *              (qk_norm with w_k, then RoPE) and the value (v_norm).
+ * w_q, w_k     bf16 [D]: the qk_norm weights, shared by all heads.
+ * block_table  int32 [batch, max_blocks]; positions int32 [batch].
+ * q_out        bf16 [batch, 16, D] (written): the decode's q.
+ * k_pool, v_pool  the decode's pools (one row per sequence written).
+ * status       optional device int32: a position outside [0, max_blocks*16)
+ *              raises ATTN_DEV_BAD_SEQ_LEN, a page id outside [0, num_pages)
+ *              ATTN_DEV_BAD_PAGE; that token's cache row is then not written
+ *              (its q is).
+ *
+ * Computed in fp32 (RoPE angles without the fp32 rounding of pos * freq,
+ * see kv_append.cuh), rounded once to bf16 (nearest even).  Asynchronous on
+ * `stream`, launched like the decode kernels (programmatic dependent of the
+ * previous kernel).  Alignment: qkv and q_out 4 bytes, the pools 16 bytes.
+ * Returns ATTN_OK or ATTN_ERR_* with nothing launched.
+ */
+int32_t attn_kv_append_sliding(const void* qkv, const void* w_q, const void* w_k, const int32_t* block_table,
+                               const int32_t* positions, void* q_out, void* k_pool, void* v_pool, int32_t batch,
+                               int32_t max_blocks, int64_t num_pages, int32_t* status, void* stream);
+int32_t attn_kv_append_global(const void* qkv, const void* w_q, const void* w_k, const int32_t* block_table,
+                              const int32_t* positions, void* q_out, void* k_pool, void* v_pool, int32_t batch,
+                              int32_t max_blocks, int64_t num_pages, int32_t* status, void* stream);
 
 /*
  * attn_selftest_wait_timeout -- exercises the device-side failure path of the

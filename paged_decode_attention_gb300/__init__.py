@@ -35,7 +35,9 @@ PAGE_SIZE = 16
 SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
 
 EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_plan",
-           "attn_decode_workspace_size", "attn_last_error", "attn_abi_version")
+           "attn_decode_workspace_size", "attn_kv_append_sliding", "attn_kv_append_global",
+           "attn_last_error", "attn_abi_version")
+APPEND_ROW = {KIND_SLIDING: 16 * 256 + 2 * 8 * 256, KIND_GLOBAL: 16 * 512 + 512}  # qkv row length
 
 
 class AttnDecodeError(RuntimeError):
@@ -74,6 +76,12 @@ def load(path=None):
                                      ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]
     lib.attn_decode_workspace_size.restype = c_sz
     lib.attn_decode_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32]
+    app = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,  # qkv w_q w_k block_table positions q_out k_pool v_pool
+           c_i32, c_i32, c_i64, c_vp, c_vp]                 # batch max_blocks num_pages status stream
+    for name in ("attn_kv_append_sliding", "attn_kv_append_global"):
+        fn = getattr(lib, name)
+        fn.restype = c_i32
+        fn.argtypes = app
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_abi_version.restype = c_i32
@@ -244,3 +252,49 @@ def attn_decode_global(q, k_pool, v_pool, block_table, seq_lens, o=None, *, wind
     """decodeGQA: q [B,16,512], pools [P,16,1,512] bf16 -> o [B,16,512] (window <= 0: none)."""
     return _call(KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len,
                  out_dtype, num_splits, workspace, status, stream)
+
+
+def _append(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream):
+    Hq, Hkv, D = SHAPES[kind]
+    batch, max_blocks, num_pages = qkv.shape[0], block_table.shape[1], k_pool.shape[0]
+    args = [_ptr(qkv, "qkv", torch.bfloat16, (batch, APPEND_ROW[kind])),
+            _ptr(w_q, "w_q", torch.bfloat16, (D,)),
+            _ptr(w_k, "w_k", torch.bfloat16, (D,)),
+            _ptr(block_table, "block_table", torch.int32, (batch, max_blocks)),
+            _ptr(positions, "positions", torch.int32, (batch,))]
+    if q_out is None:
+        q_out = torch.empty((batch, Hq, D), dtype=torch.bfloat16, device=qkv.device)
+    args += [_ptr(q_out, "q_out", torch.bfloat16, (batch, Hq, D)),
+             _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
+             _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))]
+    st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device)
+    s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    lib = load()
+    fn = lib.attn_kv_append_sliding if kind == KIND_SLIDING else lib.attn_kv_append_global
+    rc = fn(*args, batch, max_blocks, num_pages, st_ptr, s_ptr)
+    if rc != ATTN_OK:
+        raise AttnDecodeError(rc, attn_last_error())
+    return q_out
+
+
+def attn_kv_append_sliding(qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out=None, *, status=None,
+                           stream=None):
+    """Norms, RoPE and cache append of one token per sequence (sliding layers).
+
+    qkv [B, 8192] bf16 = [q 16x256 | k 8x256 | v 8x256]; w_q, w_k [256] bf16;
+    positions [B] int32.  Writes each token's key and value into k_pool /
+    v_pool at page block_table[b, pos/16], row pos % 16; returns q_out [B,16,256].
+    """
+    return _append(KIND_SLIDING, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream)
+
+
+def attn_kv_append_global(qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out=None, *, status=None,
+                          stream=None):
+    """Norms, RoPE and cache append of one token per sequence (global layers).
+
+    qkv [B, 8704] bf16 = [q 16x512 | x 512], x giving both key and value
+    (values = keys); w_q, w_k [512] bf16.  Returns q_out [B,16,512].
+    """
+    return _append(KIND_GLOBAL, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream)

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -12,6 +13,7 @@
 #include "attn_decode.h"
 #include "combine.cuh"
 #include "global.cuh"
+#include "kv_append.cuh"
 #include "sliding.cuh"
 
 namespace {
@@ -361,6 +363,105 @@ const char* attn_last_error(void) { return g_err; }
 int32_t attn_abi_version(void) { return ATTN_DECODE_ABI_VERSION; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Norms, RoPE and cache append of one token per sequence
+// ---------------------------------------------------------------------------
+namespace {
+
+// 2*pi as three floats for the additive range reduction (Cody and Waite):
+// the first two keep 8 significant bits, so n * part is exact for n < 2^16
+// turns; the third is the float nearest to what remains.
+void split_two_pi(float out[3]) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double rest = two_pi;
+  for (int k = 0; k < 2; ++k) {
+    int e;
+    const double m = std::frexp(rest, &e);  // rest = m * 2^e, 0.5 <= m < 1
+    const double part = std::ldexp(std::trunc(std::ldexp(m, 8)), e - 8);
+    out[k] = static_cast<float>(part);
+    rest -= part;
+  }
+  out[2] = static_cast<float>(rest);
+}
+
+int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w_k, const int32_t* block_table,
+                   const int32_t* positions, void* q_out, void* k_pool, void* v_pool, int32_t batch,
+                   int32_t max_blocks, int64_t num_pages, int32_t* status, void* stream) {
+  g_err[0] = '\0';
+  const bool sliding = kind == ATTN_KIND_SLIDING;
+  const char* name = sliding ? "attn_kv_append_sliding" : "attn_kv_append_global";
+  if (!qkv || !w_q || !w_k || !block_table || !positions || !q_out || !k_pool || !v_pool)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  auto aligned = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; };
+  if (!aligned(qkv, 4) || !aligned(w_q, 2) || !aligned(w_k, 2) || !aligned(q_out, 4) || !aligned(k_pool, 16) ||
+      !aligned(v_pool, 16) || !aligned(block_table, 4) || !aligned(positions, 4))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer (qkv and q_out 4 bytes, pools 16 bytes)", name);
+  if (status && !aligned(status, 4)) return fail(ATTN_ERR_INVALID_ARG, "%s: status must be 4-byte aligned", name);
+  if (batch < 1 || batch > ATTN_MAX_BATCH)
+    return fail(ATTN_ERR_UNSUPPORTED, "%s: batch %d outside [1, %d]", name, batch, ATTN_MAX_BATCH);
+  if (max_blocks < 1) return fail(ATTN_ERR_INVALID_ARG, "%s: max_blocks must be >= 1", name);
+  if (num_pages < 1 || num_pages > (int64_t{1} << 31) / ATTN_PAGE_SIZE - 1)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: num_pages %lld out of range", name, static_cast<long long>(num_pages));
+
+  const int D = sliding ? ATTN_SLIDING_D : ATTN_GLOBAL_D;
+  const int pairs = sliding ? ATTN_SLIDING_ROPE_PAIRS : ATTN_GLOBAL_ROPE_PAIRS;
+  const double theta = sliding ? ATTN_SLIDING_ROPE_THETA : ATTN_GLOBAL_ROPE_THETA;
+  pda::append::AppendParams p{};
+  p.qkv = static_cast<const __nv_bfloat16*>(qkv);
+  p.w_q = static_cast<const __nv_bfloat16*>(w_q);
+  p.w_k = static_cast<const __nv_bfloat16*>(w_k);
+  p.block_table = block_table;
+  p.positions = positions;
+  p.q_out = static_cast<__nv_bfloat16*>(q_out);
+  p.k_pool = static_cast<__nv_bfloat16*>(k_pool);
+  p.v_pool = static_cast<__nv_bfloat16*>(v_pool);
+  p.status = status;
+  p.num_pages = num_pages;
+  p.batch = batch;
+  p.max_blocks = max_blocks;
+  p.eps = 1e-6f;
+  split_two_pi(p.two_pi);
+  p.inv_two_pi = static_cast<float>(1.0 / 6.283185307179586476925286766559);
+  for (int i = 0; i < pairs; ++i) {
+    const double f = std::pow(theta, -2.0 * i / D);
+    p.freq_hi[i] = static_cast<float>(f);
+    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
+  }
+  const int rows = sliding ? ATTN_SLIDING_HQ + 2 * ATTN_SLIDING_HKV : ATTN_GLOBAL_HQ + 1;
+  const dim3 grid((batch * rows + 3) / 4);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (sliding)
+    e = launch_pdl(pda::append::append_kernel<ATTN_SLIDING_D, ATTN_SLIDING_HQ, ATTN_SLIDING_HKV,
+                                              ATTN_SLIDING_ROPE_PAIRS, false>,
+                   grid, 128, 0, s, p);
+  else
+    e = launch_pdl(pda::append::append_kernel<ATTN_GLOBAL_D, ATTN_GLOBAL_HQ, ATTN_GLOBAL_HKV,
+                                              ATTN_GLOBAL_ROPE_PAIRS, true>,
+                   grid, 128, 0, s, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t attn_kv_append_sliding(const void* qkv, const void* w_q, const void* w_k,
+                                          const int32_t* block_table, const int32_t* positions, void* q_out,
+                                          void* k_pool, void* v_pool, int32_t batch, int32_t max_blocks,
+                                          int64_t num_pages, int32_t* status, void* stream) {
+  return run_append(ATTN_KIND_SLIDING, qkv, w_q, w_k, block_table, positions, q_out, k_pool, v_pool, batch,
+                    max_blocks, num_pages, status, stream);
+}
+
+extern "C" int32_t attn_kv_append_global(const void* qkv, const void* w_q, const void* w_k,
+                                         const int32_t* block_table, const int32_t* positions, void* q_out,
+                                         void* k_pool, void* v_pool, int32_t batch, int32_t max_blocks,
+                                         int64_t num_pages, int32_t* status, void* stream) {
+  return run_append(ATTN_KIND_GLOBAL, qkv, w_q, w_k, block_table, positions, q_out, k_pool, v_pool, batch,
+                    max_blocks, num_pages, status, stream);
+}
 
 // One warp waits, with the decode kernels' bounded wait and time limit, on a
 // barrier that nothing arrives at; the wait gives up, the timeout bit is
