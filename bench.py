@@ -404,11 +404,76 @@ def run_ours(args, rank, world, local_rank):
     # --- end to end through the public API with host buffers ---
     e2e = run_e2e(args, plans, n_sets, stream, status, dev)
 
-    res.update(per_type=per_type)
+    # --- the step before the decode: norms, RoPE and the cache append ---
+    append = time_append(calls0, stream, status, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d after the cache append" % int(status.item()))
+
+    res.update(per_type=per_type, append=append)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
                heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
                launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
     return res
+
+
+def append_bytes(kind, B):
+    """qkv row read, q write and the key and value rows written, per call of B tokens."""
+    from workloads import append_row_len
+    Hq, Hkv, D = (16, 8, 256) if kind == "sliding" else (16, 1, 512)
+    return B * (append_row_len(kind) * 2 + Hq * D * 2 + 2 * Hkv * D * 2) + 2 * D * 2
+
+
+def time_append(calls0, stream, status, dev, rounds=20):
+    """The norm + RoPE + cache-append step for one new token per sequence,
+    at position seq_len - 1 of each decode call of the step, per layer type.
+    Each call reads its own qkv and writes its own q, rotating over enough
+    sets that a set is reused only after more than L2's worth of others."""
+    import torch
+    import paged_decode_attention_gb300 as pda
+    from workloads import append_row_len
+    out = {}
+    for kind in sorted(set(c.kind for c in calls0)):
+        c = next(c for c in calls0 if c.kind == kind)
+        D = c.D
+        per_call = append_bytes(kind, c.B)
+        n = rotation_count(per_call, floor=2, cap=256)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(77)
+        qkv = [torch.randn((c.B, append_row_len(kind)), generator=gen, device=dev).to(torch.bfloat16)
+               for _ in range(n)]
+        q_out = [torch.empty((c.B, c.Hq, D), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        w_q = (1.0 + 0.1 * torch.randn(D, generator=gen, device=dev)).to(torch.bfloat16)
+        w_k = (1.0 + 0.1 * torch.randn(D, generator=gen, device=dev)).to(torch.bfloat16)
+        positions = (c.seq_lens - 1).to(torch.int32)
+        fn = pda.attn_kv_append_sliding if kind == "sliding" else pda.attn_kv_append_global
+
+        def launch_all():
+            for i in range(n):
+                fn(qkv[i], w_q, w_k, c.block_table, positions, c.k_pool, c.v_pool, q_out[i],
+                   status=status, stream=stream)
+        with torch.cuda.stream(stream):
+            launch_all()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch_all()
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(rounds):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / (rounds * n)
+        out[kind] = {"tokens_per_call": c.B, "us_per_call": round(ms * 1e3, 3),
+                     "bytes_per_call": per_call, "value": round(per_call / (ms * 1e-3) / 1e9, 2),
+                     "unit": "GB/s", "sets": n,
+                     "launch": "%d calls back to back in one CUDA graph, %d replays" % (n, rounds)}
+    return out
 
 
 def _packed_inputs(c, dev):
@@ -696,6 +761,8 @@ def main(argv=None):
         line["per_layer_type"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4))
                                   for k, v in r0["per_type"].items()}
     line["gpu_launches"] = r0["launches_per_step"] * args.steps
+    if r0.get("append"):
+        line["append"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4)) for k, v in r0["append"].items()}
     line["e2e"] = r0["e2e"]
     line["clocks"] = r0["clocks"]
     if not args.no_cpu_baseline:

@@ -248,7 +248,7 @@ int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool, const voi
  * Computed in fp32 (RoPE angles without the fp32 rounding of pos * freq,
  * see kv_append.cuh), rounded once to bf16 (nearest even).  Asynchronous on
  * `stream`, launched like the decode kernels (programmatic dependent of the
- * previous kernel).  Alignment: qkv and q_out 4 bytes, the pools 16 bytes.
+ * previous kernel).  Alignment: qkv, w_q, w_k, q_out and the pools 16 bytes.
  * Returns ATTN_OK or ATTN_ERR_* with nothing launched.
  */
 int32_t attn_kv_append_sliding(const void* qkv, const void* w_q, const void* w_k, const int32_t* block_table,

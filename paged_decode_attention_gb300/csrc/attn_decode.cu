@@ -394,9 +394,9 @@ int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w
   if (!qkv || !w_q || !w_k || !block_table || !positions || !q_out || !k_pool || !v_pool)
     return fail(ATTN_ERR_INVALID_ARG, "%s: null pointer argument", name);
   auto aligned = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; };
-  if (!aligned(qkv, 4) || !aligned(w_q, 2) || !aligned(w_k, 2) || !aligned(q_out, 4) || !aligned(k_pool, 16) ||
+  if (!aligned(qkv, 16) || !aligned(w_q, 16) || !aligned(w_k, 16) || !aligned(q_out, 16) || !aligned(k_pool, 16) ||
       !aligned(v_pool, 16) || !aligned(block_table, 4) || !aligned(positions, 4))
-    return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer (qkv and q_out 4 bytes, pools 16 bytes)", name);
+    return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer (qkv, w_q, w_k, q_out and the pools 16 bytes)", name);
   if (status && !aligned(status, 4)) return fail(ATTN_ERR_INVALID_ARG, "%s: status must be 4-byte aligned", name);
   if (batch < 1 || batch > ATTN_MAX_BATCH)
     return fail(ATTN_ERR_UNSUPPORTED, "%s: batch %d outside [1, %d]", name, batch, ATTN_MAX_BATCH);
@@ -405,7 +405,6 @@ int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w
     return fail(ATTN_ERR_INVALID_ARG, "%s: num_pages %lld out of range", name, static_cast<long long>(num_pages));
 
   const int D = sliding ? ATTN_SLIDING_D : ATTN_GLOBAL_D;
-  const int pairs = sliding ? ATTN_SLIDING_ROPE_PAIRS : ATTN_GLOBAL_ROPE_PAIRS;
   const double theta = sliding ? ATTN_SLIDING_ROPE_THETA : ATTN_GLOBAL_ROPE_THETA;
   pda::append::AppendParams p{};
   p.qkv = static_cast<const __nv_bfloat16*>(qkv);
@@ -423,11 +422,17 @@ int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w
   p.eps = 1e-6f;
   split_two_pi(p.two_pi);
   p.inv_two_pi = static_cast<float>(1.0 / 6.283185307179586476925286766559);
-  for (int i = 0; i < pairs; ++i) {
-    const double f = std::pow(theta, -2.0 * i / D);
-    p.freq_hi[i] = static_cast<float>(f);
-    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
-  }
+  // frequencies theta^(-2i/D), i = V*lane + j, as products of these factors
+  const int V = D / 64;
+  auto split = [](double f) {
+    pda::append::FloatPair fp;
+    fp.hi = static_cast<float>(f);
+    fp.lo = static_cast<float>(f - static_cast<double>(fp.hi));
+    return fp;
+  };
+  for (int k = 0; k < pda::append::kLaneBits; ++k) p.lane_factor[k] = split(std::pow(theta, -2.0 * V * (1 << k) / D));
+  for (int j = 0; j < V; ++j) p.dim_factor[j] = split(std::pow(theta, -2.0 * j / D));
+  static_assert(ATTN_SLIDING_D / 64 <= pda::append::kMaxV && ATTN_GLOBAL_D / 64 <= pda::append::kMaxV, "dims per lane");
   const int rows = sliding ? ATTN_SLIDING_HQ + 2 * ATTN_SLIDING_HKV : ATTN_GLOBAL_HQ + 1;
   const dim3 grid((batch * rows + 3) / 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -13,13 +13,23 @@
 //
 // One warp per head row of one token.  Lane l holds dims [V l, V l + V) and
 // their rotation partners [D/2 + V l, D/2 + V l + V), V = D / 64, so a pair
-// never leaves its lane.  Sums of squares are reduced with shuffles in fp32.
-// The rotation angle pos * f_i is formed without the rounding of pos * f_i
-// in fp32 (which reaches 0.016 rad at pos = 262143): f_i is split on the
-// host into f_hi + f_lo, the product pos * f_hi is carried as a float plus
-// its exact fma remainder, and the turns are removed with a three-part
-// 2*pi (Cody and Waite's additive range reduction) before __sincosf of an
-// argument in [-pi, pi].  Outputs are rounded once to bf16 (nearest even).
+// never leaves its lane; each half is one 8- or 16-byte access.  Sums of
+// squares are reduced with shuffles in fp32.
+//
+// RoPE angles.  pos * f_i rounded to fp32 is off by up to 0.016 rad at
+// pos = 262143, so f_i is carried as a pair of floats hi + lo (about 46
+// significant bits), pos * f_i as a float plus its exact fma remainder, and
+// the turns are removed with a three-part 2*pi (Cody and Waite's additive
+// range reduction) before __sincosf of an argument in [-pi, pi].  f_i is not
+// looked up per lane (a kernel-parameter table read at 32 different offsets
+// is served one offset at a time): lane l forms it as
+//   theta^(-2 V l / D) * theta^(-2 j / D),  j = i - V l,
+// the first factor the product of theta^(-2 V 2^k / D) over the set bits k
+// of l, every factor a host-computed float pair read at the same offset by
+// all lanes, and every product a double-float product (Dekker's, with the
+// fma giving the exact error of the leading product).
+//
+// Outputs are rounded once to bf16 (nearest even).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -30,7 +40,12 @@
 namespace pda {
 namespace append {
 
-constexpr int kMaxPairs = 128;
+constexpr int kLaneBits = 5;  // lanes 0..31
+constexpr int kMaxV = 8;      // D / 64 for D = 512
+
+struct FloatPair {  // hi + lo, |lo| <= ulp(hi) / 2
+  float hi, lo;
+};
 
 struct AppendParams {
   const __nv_bfloat16* qkv;    // [B, row_len]
@@ -46,18 +61,38 @@ struct AppendParams {
   int32_t batch;
   int32_t max_blocks;
   float eps;
-  float two_pi[3];             // 2*pi = two_pi[0] + two_pi[1] + two_pi[2]; [0], [1] with 8 significant bits
+  float two_pi[3];                  // 2*pi = two_pi[0] + two_pi[1] + two_pi[2]; [0], [1] with 8 significant bits
   float inv_two_pi;
-  float freq_hi[kMaxPairs];    // theta^(-2i/D) = freq_hi[i] + freq_lo[i]
-  float freq_lo[kMaxPairs];
+  FloatPair lane_factor[kLaneBits];  // theta^(-2 V 2^k / D)
+  FloatPair dim_factor[kMaxV];       // theta^(-2 j / D), j < V
 };
 
-// cos and sin of pos * (freq_hi + freq_lo) for an integer 0 <= pos < 2^24.
-__device__ __forceinline__ void rope_angle(const AppendParams& p, int i, int pos, float& c, float& s) {
+// a * b in double-float arithmetic: relative error about 2^-46.
+__device__ __forceinline__ FloatPair df_mul(FloatPair a, FloatPair b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);  // exact error of p
+  e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
+  const float hi = p + e;
+  return {hi, e - (hi - p)};
+}
+
+// theta^(-2 V lane / D): the lane's share of its frequencies.
+__device__ __forceinline__ FloatPair lane_frequency(const AppendParams& p, int lane) {
+  FloatPair f{1.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kLaneBits; ++k) {
+    const FloatPair m = (lane >> k) & 1 ? p.lane_factor[k] : FloatPair{1.f, 0.f};
+    f = df_mul(f, m);
+  }
+  return f;
+}
+
+// cos and sin of pos * (f.hi + f.lo) for an integer 0 <= pos < 2^24.
+__device__ __forceinline__ void rope_angle(const AppendParams& p, FloatPair f, int pos, float& c, float& s) {
   const float fp = static_cast<float>(pos);  // exact
-  const float hi = fp * p.freq_hi[i];
-  const float err = fmaf(fp, p.freq_hi[i], -hi);  // pos * freq_hi - hi, exactly
-  const float small = fmaf(fp, p.freq_lo[i], err);
+  const float hi = fp * f.hi;
+  const float err = fmaf(fp, f.hi, -hi);  // pos * f.hi - hi, exactly
+  const float small = fmaf(fp, f.lo, err);
   const float n = rintf(hi * p.inv_two_pi);
   float r = fmaf(-n, p.two_pi[0], hi);  // n * two_pi[0] and n * two_pi[1] are exact for n < 2^16
   r = fmaf(-n, p.two_pi[1], r);
@@ -72,23 +107,57 @@ struct Row {
   float lo[kV], hi[kV];               // dims [kV*lane, +kV) and [D/2 + kV*lane, +kV)
 };
 
-template <int kD>
-__device__ __forceinline__ void load_row(const __nv_bfloat16* src, Row<kD>& r) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kV = Row<kD>::kV;
+// kV consecutive bf16 (8 or 16 bytes) <-> fp32
+template <int kV>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float* out) {
+  static_assert(kV == 4 || kV == 8, "one 8- or 16-byte access");
+  uint32_t w[kV / 2];
+  if constexpr (kV == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    w[0] = u.x; w[1] = u.y;
+  }
 #pragma unroll
-  for (int j = 0; j < kV; j += 2) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + kV * lane + j));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + kD / 2 + kV * lane + j));
-    r.lo[j] = a.x; r.lo[j + 1] = a.y;
-    r.hi[j] = b.x; r.hi[j + 1] = b.y;
+  for (int j = 0; j < kV / 2; ++j) {
+    const float2 f = bf16x2_to_float2(w[j]);
+    out[2 * j] = f.x;
+    out[2 * j + 1] = f.y;
   }
 }
 
-// x / sqrt(mean(x^2) + eps), times w when given.
+template <int kV>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16* dst, const float* in) {
+  uint32_t w[kV / 2];
+#pragma unroll
+  for (int j = 0; j < kV / 2; ++j) w[j] = pack_bf16x2(in[2 * j], in[2 * j + 1]);
+  if constexpr (kV == 8) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  }
+}
+
 template <int kD>
-__device__ __forceinline__ void normalise(Row<kD>& r, const __nv_bfloat16* w, float eps) {
+__device__ __forceinline__ void load_row(const __nv_bfloat16* src, Row<kD>& r) {
+  constexpr int kV = Row<kD>::kV;
   const int lane = threadIdx.x & 31;
+  load_bf16<kV>(src + kV * lane, r.lo);
+  load_bf16<kV>(src + kD / 2 + kV * lane, r.hi);
+}
+
+template <int kD>
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const Row<kD>& r) {
+  constexpr int kV = Row<kD>::kV;
+  const int lane = threadIdx.x & 31;
+  store_bf16<kV>(dst + kV * lane, r.lo);
+  store_bf16<kV>(dst + kD / 2 + kV * lane, r.hi);
+}
+
+// x / sqrt(mean(x^2) + eps)
+template <int kD>
+__device__ __forceinline__ void normalise(Row<kD>& r, float eps) {
   constexpr int kV = Row<kD>::kV;
   float ss = 0.f;
 #pragma unroll
@@ -101,40 +170,30 @@ __device__ __forceinline__ void normalise(Row<kD>& r, const __nv_bfloat16* w, fl
     r.lo[j] *= inv;
     r.hi[j] *= inv;
   }
-  if (w) {
+}
+
+template <int kD>
+__device__ __forceinline__ void scale(Row<kD>& r, const Row<kD>& w) {
 #pragma unroll
-    for (int j = 0; j < kV; ++j) {
-      r.lo[j] *= __bfloat162float(w[kV * lane + j]);
-      r.hi[j] *= __bfloat162float(w[kD / 2 + kV * lane + j]);
-    }
+  for (int j = 0; j < Row<kD>::kV; ++j) {
+    r.lo[j] *= w.lo[j];
+    r.hi[j] *= w.hi[j];
   }
 }
 
 template <int kD, int kPairs>
 __device__ __forceinline__ void rotate(const AppendParams& p, Row<kD>& r, int pos) {
-  const int lane = threadIdx.x & 31;
   constexpr int kV = Row<kD>::kV;
+  const int lane = threadIdx.x & 31;
+  if (kV * lane >= kPairs) return;  // kPairs is a multiple of kV
+  const FloatPair fl = lane_frequency(p, lane);
 #pragma unroll
   for (int j = 0; j < kV; ++j) {
-    const int i = kV * lane + j;
-    if (i < kPairs) {
-      float c, s;
-      rope_angle(p, i, pos, c, s);
-      const float a = r.lo[j], b = r.hi[j];
-      r.lo[j] = a * c - b * s;
-      r.hi[j] = b * c + a * s;
-    }
-  }
-}
-
-template <int kD>
-__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const Row<kD>& r) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kV = Row<kD>::kV;
-#pragma unroll
-  for (int j = 0; j < kV; j += 2) {
-    *reinterpret_cast<uint32_t*>(dst + kV * lane + j) = pack_bf16x2(r.lo[j], r.lo[j + 1]);
-    *reinterpret_cast<uint32_t*>(dst + kD / 2 + kV * lane + j) = pack_bf16x2(r.hi[j], r.hi[j + 1]);
+    float c, s;
+    rope_angle(p, df_mul(fl, p.dim_factor[j]), pos, c, s);
+    const float a = r.lo[j], b = r.hi[j];
+    r.lo[j] = a * c - b * s;
+    r.hi[j] = b * c + a * s;
   }
 }
 
@@ -145,6 +204,7 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
   constexpr int kRowsPerToken = kHq + (kShared ? 1 : 2 * kHkv);
   constexpr int kRowLen = kHq * kD + (kShared ? kD : 2 * kHkv * kD);
   static_assert(!kShared || kHkv == 1, "a shared key/value source is one head");
+  static_assert(kPairs % Row<kD>::kV == 0 && kPairs <= kD / 2, "whole lanes of active pairs");
   // The previous kernel in the stream may still be writing qkv or the tables.
   wait_for_primary_grid();
   allow_dependent_launch();
@@ -152,13 +212,21 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
   if (gw >= p.batch * kRowsPerToken) return;
   const int b = gw / kRowsPerToken;
   const int r = gw % kRowsPerToken;
-  const int pos = p.positions[b];
+  const int is_q = r < kHq;
+  const int c = kShared ? 0 : (r - kHq) % kHkv;
+  const bool is_value = !kShared && r >= kHq + kHkv;
   const __nv_bfloat16* row = p.qkv + static_cast<size_t>(b) * kRowLen;
-  Row<kD> x;
+  const __nv_bfloat16* src = is_q ? row + r * kD : row + kHq * kD + (is_value ? (kHkv + c) * kD : c * kD);
 
-  if (r < kHq) {  // query head r
-    load_row<kD>(row + r * kD, x);
-    normalise<kD>(x, p.w_q, p.eps);
+  // independent loads first: position, the row, its norm weights
+  const int pos = p.positions[b];
+  Row<kD> x, w;
+  load_row<kD>(src, x);
+  if (!is_value) load_row<kD>(is_q ? p.w_q : p.w_k, w);
+
+  if (is_q) {
+    normalise<kD>(x, p.eps);
+    scale<kD>(x, w);
     rotate<kD, kPairs>(p, x, pos < 0 ? 0 : pos);
     store_row<kD>(p.q_out + (static_cast<size_t>(b) * kHq + r) * kD, x);
     return;
@@ -177,20 +245,10 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
   }
   const size_t slot = static_cast<size_t>(phys) * ATTN_PAGE_SIZE + pos % ATTN_PAGE_SIZE;
 
-  const int c = kShared ? 0 : (r - kHq) % kHkv;
-  const bool is_value = !kShared && r >= kHq + kHkv;
-  load_row<kD>(row + kHq * kD + (is_value ? (kHkv + c) * kD : c * kD), x);
-  if (is_value) {
-    normalise<kD>(x, nullptr, p.eps);
-    store_row<kD>(p.v_pool + (slot * kHkv + c) * kD, x);
-    return;
-  }
-  if (kShared) {  // the value is the same head, normalised without weights
-    Row<kD> v = x;
-    normalise<kD>(v, nullptr, p.eps);
-    store_row<kD>(p.v_pool + (slot * kHkv + c) * kD, v);
-  }
-  normalise<kD>(x, p.w_k, p.eps);
+  normalise<kD>(x, p.eps);
+  if (is_value || kShared) store_row<kD>(p.v_pool + (slot * kHkv + c) * kD, x);  // v_norm: no weights
+  if (is_value) return;
+  scale<kD>(x, w);
   rotate<kD, kPairs>(p, x, pos);
   store_row<kD>(p.k_pool + (slot * kHkv + c) * kD, x);
 }

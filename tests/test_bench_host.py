@@ -27,6 +27,15 @@ def test_algorithmic_bytes_per_position():
     assert bench.algorithmic_bytes("global", [0, 0], 0) == 2 * 16 * 512 * 2 * 2
 
 
+def test_append_bytes_per_token():
+    # sliding: qkv row 8192 x 2 read, q 16 x 256 x 2 written, k and v 8 x 256 x 2 each written
+    assert bench.append_bytes("sliding", 2) - bench.append_bytes("sliding", 1) == 16384 + 8192 + 8192
+    # global: qkv row 8704 x 2 read, q 16 x 512 x 2 written, one key and one value row of 512 x 2
+    assert bench.append_bytes("global", 2) - bench.append_bytes("global", 1) == 17408 + 16384 + 2048
+    # the two weight vectors are read once per call
+    assert bench.append_bytes("global", 0) == 2 * 512 * 2
+
+
 def test_rotation_exceeds_l2():
     n = bench.rotation_count(67 * 10**6)
     assert n * 67 * 10**6 > 3 * bench.L2_BYTES
