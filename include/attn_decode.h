@@ -269,6 +269,21 @@ int32_t attn_kv_append_global(const void* qkv, const void* w_q, const void* w_k,
  */
 int32_t attn_selftest_wait_timeout(int32_t* status, void* stream);
 
+/*
+ * attn_selftest_delayed_copy -- a stand-in for a kernel that rewrites the
+ * decode's inputs while the decode is already being scheduled.  It launches
+ * one block as a programmatic dependent of the previous kernel in `stream`:
+ * the block waits for that kernel, lets its own dependents launch at once,
+ * sleeps `delay_ns` (0 to 1,000,000), then copies `bytes` (a multiple of 4,
+ * at most 16 MiB) from `src` to `dst` (device pointers, 4-byte aligned, not
+ * overlapping).  A decode launched next builds its schedule hints and starts
+ * its first copies from the old contents of dst, and must still read the new
+ * ones after its wait.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG /
+ * ATTN_ERR_CUDA with nothing launched.  For tests of the launch order; the
+ * pages have no counterpart for it.
+ */
+int32_t attn_selftest_delayed_copy(void* dst, const void* src, int64_t bytes, int32_t delay_ns, void* stream);
+
 /* Message of the last error on this host thread ("" if none). */
 const char* attn_last_error(void);
 

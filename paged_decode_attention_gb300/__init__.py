@@ -82,6 +82,8 @@ def load(path=None):
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = app
+    lib.attn_selftest_delayed_copy.restype = c_i32
+    lib.attn_selftest_delayed_copy.argtypes = [c_vp, c_vp, c_i64, c_i32, c_vp]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_abi_version.restype = c_i32
@@ -298,3 +300,19 @@ def attn_kv_append_global(qkv, w_q, w_k, block_table, positions, k_pool, v_pool,
     (values = keys); w_q, w_k [512] bf16.  Returns q_out [B,16,512].
     """
     return _append(KIND_GLOBAL, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream)
+
+
+def selftest_delayed_copy(dst, src, delay_ns=5000, stream=None):
+    """attn_selftest_delayed_copy: copy src into dst (same-size int32 CUDA tensors)
+    from a kernel that lets the next kernel launch first and copies after
+    delay_ns.  For tests of the launch order."""
+    if dst.dtype != torch.int32 or src.dtype != torch.int32 or dst.shape != src.shape:
+        raise ValueError("dst and src must be int32 tensors of one shape")
+    if not (dst.is_cuda and src.is_cuda and dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("dst and src must be contiguous CUDA tensors")
+    if stream is None:
+        stream = torch.cuda.current_stream(dst.device)
+    s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = load().attn_selftest_delayed_copy(dst.data_ptr(), src.data_ptr(), dst.numel() * 4, int(delay_ns), s_ptr)
+    if rc != ATTN_OK:
+        raise AttnDecodeError(rc, attn_last_error())

@@ -492,6 +492,41 @@ extern "C" int32_t attn_selftest_wait_timeout(int32_t* status, void* stream) {
   return ATTN_OK;
 }
 
+// Waits for the previous kernel in the stream, lets its own dependents launch
+// at once, sleeps `delay_ns` (bounded by the host to 1 ms, and by an
+// iteration cap), then copies `words` 32-bit words.  A programmatic dependent
+// launched after it therefore runs its pre-wait prologue while dst still
+// holds the old values.
+__global__ void __launch_bounds__(256) selftest_delayed_copy_kernel(uint32_t* dst, const uint32_t* src, int64_t words,
+                                                                    int32_t delay_ns) {
+  pda::wait_for_primary_grid();
+  pda::allow_dependent_launch();
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int it = 0; it < (1 << 20); ++it) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 >= static_cast<uint64_t>(delay_ns)) break;
+    __nanosleep(256);
+  }
+  for (int64_t i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+}
+
+extern "C" int32_t attn_selftest_delayed_copy(void* dst, const void* src, int64_t bytes, int32_t delay_ns,
+                                              void* stream) {
+  g_err[0] = '\0';
+  if (!dst || !src || (reinterpret_cast<uintptr_t>(dst) & 3u) || (reinterpret_cast<uintptr_t>(src) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_selftest_delayed_copy: dst and src must be 4-byte aligned device pointers");
+  if (bytes < 0 || (bytes & 3) || bytes > (int64_t{1} << 24))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_selftest_delayed_copy: bytes must be a multiple of 4 in [0, 16 MiB]");
+  if (delay_ns < 0 || delay_ns > 1000000)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_selftest_delayed_copy: delay_ns must be in [0, 1000000]");
+  const cudaError_t e = launch_pdl(selftest_delayed_copy_kernel, dim3(1), 256, 0, static_cast<cudaStream_t>(stream),
+                                   static_cast<uint32_t*>(dst), static_cast<const uint32_t*>(src), bytes / 4, delay_ns);
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, "attn_selftest_delayed_copy: launch failed: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Sliding-window decode with built-in scratch, for callers that cannot
 // allocate device memory themselves.

@@ -3,10 +3,18 @@
 * Every decode grid is launched as a programmatic dependent of the previous
   kernel in the stream: it builds its schedule from hint reads and warms L2
   before griddepcontrol.wait, then re-reads seq_lens and rebuilds the schedule
-  if it changed.  Here each call's inputs are rewritten by a torch kernel
-  launched immediately before it on the same stream, so the hint pass may see
-  the previous values; every output must still match the oracle for the new
-  ones.
+  if it changed.  Here each call's q is rewritten by a torch kernel right
+  before it, and its seq_lens by attn_selftest_delayed_copy, which lets the
+  decode launch first and writes a few microseconds later, so the hint pass
+  sees the previous lengths; every output must still match the oracle for
+  the new ones.
+* Right after the wait the producer copies the first pages of its span with
+  the page ids the hint pass read, and hands them to the consumers only if
+  the fresh block-table entries agree.  Here the block table is switched
+  between two physical layouts of the same cache right before each call by
+  attn_selftest_delayed_copy, a kernel that lets the decode launch first and
+  writes a few microseconds later, so the hints and the speculative copies
+  see the old table.
 * The global kernel reduces a row's maximum across lanes, and rescales its
   accumulators, only on pages where some score exceeds the running max.
   Scores that rise along the sequence move it on almost every page; scores
@@ -14,6 +22,8 @@
   Both must match the exact softmax (Attention.lean `softmax`) within the
   parity tolerance.
 """
+
+import dataclasses
 
 import pytest
 import torch
@@ -84,9 +94,12 @@ def test_inputs_written_by_the_previous_kernel(cuda_lib, kind):
     outs = [torch.empty((g.B, g.Hq, g.D), dtype=torch.float32, device=DEV) for _ in rounds]
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     stream = torch.cuda.current_stream()
-    for (lens, scale), delta, o in zip(rounds, deltas, outs):
-        torch.add(lens0, delta, out=g.seq_lens)   # a kernel writes seq_lens ...
-        torch.mul(q0, scale, out=g.q)             # ... and q, just before the decode
+    new_lens = [torch.empty_like(lens0) for _ in rounds]
+    for (lens, scale), delta, nl, o in zip(rounds, deltas, new_lens, outs):
+        torch.mul(q0, scale, out=g.q)             # a kernel writes q ...
+        torch.add(lens0, delta, out=nl)
+        # ... and seq_lens, from a kernel that lets the decode launch first
+        pda.selftest_delayed_copy(g.seq_lens, nl, delay_ns=4000, stream=stream)
         _call(g, o, status=status, stream=stream)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -95,3 +108,34 @@ def test_inputs_written_by_the_previous_kernel(cuda_lib, kind):
         case.seq_lens = torch.tensor(lens, dtype=torch.int32)
         case.q = (case.q.float() * scale).to(torch.bfloat16)
         assert_within_tolerance(o.double().cpu().numpy(), oracle_full(case), "%s lens=%s" % (kind, lens))
+
+
+@pytest.mark.parametrize("kind", ["global", "sliding"])
+def test_block_table_rewritten_by_the_previous_kernel(cuda_lib, kind):
+    lens = [1500, 40, 3300, 700, 2100, 1, 64, 17]
+    base = make_case(kind, lens, seed=122)
+    want = oracle_full(base)
+    P = base.k_pool.shape[0]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    # pages P + j hold page perm[j]: page x of the first layout is page P + inv[x] of the second
+    k2 = torch.cat([base.k_pool, base.k_pool[perm]])
+    v2 = torch.cat([base.v_pool, base.v_pool[perm]])
+    bt_a = base.block_table
+    bt_b = torch.where(bt_a >= 0, P + inv[bt_a.clamp(min=0).long()].to(torch.int32), bt_a)
+    g = dataclasses.replace(base, k_pool=k2, v_pool=v2).to(DEV)
+    tables = {"a": bt_a.to(DEV), "b": bt_b.to(DEV)}
+    order = "abbaabab"
+    outs = [torch.empty((g.B, g.Hq, g.D), dtype=torch.float32, device=DEV) for _ in order]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream()
+    for which, o in zip(order, outs):
+        pda.selftest_delayed_copy(g.block_table, tables[which], delay_ns=4000, stream=stream)
+        _call(g, o, status=status, stream=stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for which, o in zip(order, outs):
+        assert_within_tolerance(o.double().cpu().numpy(), want, "%s table %s" % (kind, which))
+        # the same logical cache in the same order: the same bits
+        assert torch.equal(o, outs[0])
