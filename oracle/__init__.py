@@ -7,6 +7,9 @@ never imports the CUDA library.
 
 * ``decode_paged`` -- the paged decode oracle in ``oracle.c`` (plain C,
   double precision, pthreads over output rows), called through ctypes.
+* ``prefill_paged`` -- multi-query (prefill) attention over the paged cache:
+  each query row is the decode of its sequence cut at the query's position
+  (``oracle.c``).
 * ``qkv_append``   -- the per-head norms, RoPE and paged KV-cache append of
   one new token per sequence (``oracle.c``, double precision).
 * ``dense``        -- the literal Lean definitions over unpaged arrays, for
@@ -63,6 +66,17 @@ def _load(lib_path=None):
         fn.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q, k_pool, v_pool
             ctypes.c_void_p, ctypes.c_void_p,                    # block_table, seq_lens
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,  # B Hq Hkv D
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,      # page_size max_blocks num_pages
+            ctypes.c_int32,                                      # window
+            ctypes.c_void_p, ctypes.c_int32,                     # rows, n_rows
+            ctypes.c_void_p, ctypes.c_int32,                     # out, n_threads
+        ]
+        fp = lib.oracle_prefill_paged
+        fp.restype = ctypes.c_int
+        fp.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q, k_pool, v_pool
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # block_table, seq_lens, cu_q
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,  # B Hq Hkv D
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,      # page_size max_blocks num_pages
             ctypes.c_int32,                                      # window
@@ -126,6 +140,49 @@ def decode_paged(q_bits, k_bits, v_bits, block_table, seq_lens, window, page_siz
         q_bits.ctypes.data, k_bits.ctypes.data, v_bits.ctypes.data,
         block_table.ctypes.data, seq_lens.ctypes.data,
         B, Hq, Hkv, D, page_size, max_blocks, num_pages, int(window),
+        None if rows_arr is None else rows_arr.ctypes.data, n_rows,
+        out.ctypes.data, int(threads),
+    )
+    if st != 0:
+        raise OracleError(ERRORS.get(st, "error %d" % st))
+    return out
+
+
+def prefill_paged(q_bits, k_bits, v_bits, block_table, seq_lens, cu_q, window, page_size=16,
+                  rows=None, threads=1, lib_path=None):
+    """Multi-query attention over the paged cache, fp64.
+
+    q_bits      uint16 [T, Hq, D], the queries of every sequence packed in order
+    cu_q        int32 [B+1]: sequence b owns rows cu_q[b] .. cu_q[b+1]-1, the
+                last n = cu_q[b+1] - cu_q[b] of its L = seq_lens[b] tokens, so its
+                query i sits at position L - n + i
+    rows        None (all T*Hq rows) or flat t*Hq + h indices
+    returns     float64 [T, Hq, D], or [len(rows), D]
+    The other arguments are as for decode_paged.
+    """
+    q_bits = _as(q_bits, np.uint16)
+    k_bits = _as(k_bits, np.uint16)
+    v_bits = _as(v_bits, np.uint16)
+    block_table = _as(block_table, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    cu_q = _as(cu_q, np.int32)
+    T, Hq, D = q_bits.shape
+    num_pages, ps, Hkv, Dk = k_bits.shape
+    B = seq_lens.shape[0]
+    if ps != page_size or Dk != D or v_bits.shape != k_bits.shape:
+        raise ValueError("pool shape does not match q / page_size")
+    if block_table.ndim != 2 or block_table.shape[0] != B or cu_q.shape != (B + 1,) or cu_q[-1] != T:
+        raise ValueError("block_table / cu_q shape")
+    if rows is None:
+        rows_arr, n_rows, out = None, 0, np.zeros((T, Hq, D), dtype=np.float64)
+    else:
+        rows_arr = _as(np.asarray(rows, dtype=np.int32), np.int32)
+        n_rows = len(rows_arr)
+        out = np.zeros((n_rows, D), dtype=np.float64)
+    st = _load(lib_path).oracle_prefill_paged(
+        q_bits.ctypes.data, k_bits.ctypes.data, v_bits.ctypes.data,
+        block_table.ctypes.data, seq_lens.ctypes.data, cu_q.ctypes.data,
+        B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, int(window),
         None if rows_arr is None else rows_arr.ctypes.data, n_rows,
         out.ctypes.data, int(threads),
     )

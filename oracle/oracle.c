@@ -70,8 +70,10 @@ typedef struct {
   int32_t B, Hq, Hkv, D, page_size, max_blocks;
   int64_t num_pages;
   int32_t window;
-  const int32_t* rows; /* flat b*Hq+h indices, or NULL for all rows */
+  const int32_t* rows; /* flat b*Hq+h indices (t*Hq+h for prefill), or NULL for all rows */
   int32_t n_rows;
+  const int32_t* cu_q; /* prefill: [B+1] query-row offsets; NULL for decode */
+  int32_t T;           /* prefill: cu_q[B], the number of query rows */
   double* out;         /* [n_rows, D] */
   int32_t n_threads;
   int32_t thread_id;
@@ -87,13 +89,13 @@ static int64_t pool_row(const job_t* j, int b, int l) {
   return phys * j->page_size + (l % j->page_size);
 }
 
-/* One output row o[b,h,:] (decodeGQA / slidingGQA at position L-1). */
-static int decode_one_row(const job_t* j, int b, int h, double* o, double* logit) {
+/* The output row of query vector qv (head h) of sequence b sitting at
+ * position L-1, over the cached positions l <= L-1 (decodeGQA, or
+ * slidingGQA at p = L-1).  L <= seq_lens[b] has been checked by the caller. */
+static int attend_one_row(const job_t* j, int b, int h, const uint16_t* qv, int L, double* o, double* logit) {
   const int G = j->Hq / j->Hkv;
   const int c = h / G;               /* query head c*G+g reads KV head c */
   const int D = j->D;
-  const int L = j->seq_lens[b];
-  if (L < 0 || (int64_t)L > (int64_t)j->max_blocks * j->page_size) return ORACLE_ERR_SEQ_LEN;
 
   /* visible positions: p - window < l <= p with p = L-1 (no lower bound when window <= 0) */
   int lo = 0;
@@ -102,8 +104,6 @@ static int decode_one_row(const job_t* j, int b, int h, double* o, double* logit
 
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (n <= 0) return ORACLE_OK;
-
-  const uint16_t* qv = j->q + ((int64_t)b * j->Hq + h) * D;
 
   /* logits s_l = 1 * sum_e q[e] * k[l,c,e]  (scale 1) */
   double m = -INFINITY;
@@ -135,6 +135,32 @@ static int decode_one_row(const job_t* j, int b, int h, double* o, double* logit
   return ORACLE_OK;
 }
 
+/* One output row o[b,h,:] (decodeGQA / slidingGQA at position L-1). */
+static int decode_one_row(const job_t* j, int b, int h, double* o, double* logit) {
+  const int L = j->seq_lens[b];
+  if (L < 0 || (int64_t)L > (int64_t)j->max_blocks * j->page_size) return ORACLE_ERR_SEQ_LEN;
+  return attend_one_row(j, b, h, j->q + ((int64_t)b * j->Hq + h) * j->D, L, o, logit);
+}
+
+/* One prefill output row o[t,h,:]: query row t belongs to the sequence b with
+ * cu_q[b] <= t < cu_q[b+1]; its n = cu_q[b+1] - cu_q[b] queries are the last
+ * n tokens of the L = seq_lens[b] cached ones, so query i = t - cu_q[b] sits
+ * at position p = L - n + i (causalGQA / slidingGQA with that pos), which is
+ * the decode of the sequence cut to its first p + 1 tokens. */
+static int prefill_one_row(const job_t* j, int t, int h, double* o, double* logit) {
+  int lo = 0, hi = j->B; /* largest b with cu_q[b] <= t */
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (j->cu_q[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int n = j->cu_q[b + 1] - j->cu_q[b];
+  const int L = j->seq_lens[b];
+  if (L < n || (int64_t)L > (int64_t)j->max_blocks * j->page_size) return ORACLE_ERR_SEQ_LEN;
+  const int p = L - n + (t - j->cu_q[b]);
+  return attend_one_row(j, b, h, j->q + ((int64_t)t * j->Hq + h) * j->D, p + 1, o, logit);
+}
+
 static void* worker(void* arg) {
   job_t* j = (job_t*)arg;
   int max_L = 0;
@@ -145,11 +171,12 @@ static void* worker(void* arg) {
     j->status = ORACLE_ERR_NOMEM;
     return NULL;
   }
-  const int total = j->rows ? j->n_rows : j->B * j->Hq;
+  const int total = j->rows ? j->n_rows : (j->cu_q ? j->T : j->B) * j->Hq;
   for (int i = j->thread_id; i < total; i += j->n_threads) {
     const int flat = j->rows ? j->rows[i] : i;
-    const int b = flat / j->Hq, h = flat % j->Hq;
-    int st = decode_one_row(j, b, h, j->out + (int64_t)i * j->D, logit);
+    const int b = flat / j->Hq, h = flat % j->Hq; /* b is the query row t for prefill */
+    int st = j->cu_q ? prefill_one_row(j, b, h, j->out + (int64_t)i * j->D, logit)
+                     : decode_one_row(j, b, h, j->out + (int64_t)i * j->D, logit);
     if (st != ORACLE_OK && j->status == ORACLE_OK) j->status = st;
   }
   free(logit);
@@ -172,19 +199,20 @@ static void* worker(void* arg) {
  * n_threads   worker threads (>= 1); rows are striped over them
  * returns     ORACLE_OK or an ORACLE_ERR_* code
  */
-int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
-                        const int32_t* block_table, const int32_t* seq_lens, int32_t B,
-                        int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
-                        int32_t max_blocks, int64_t num_pages, int32_t window,
-                        const int32_t* rows, int32_t n_rows, double* out, int32_t n_threads) {
+static int run_jobs(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                    const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q, int32_t T,
+                    int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size, int32_t max_blocks,
+                    int64_t num_pages, int32_t window, const int32_t* rows, int32_t n_rows, double* out,
+                    int32_t n_threads) {
   if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return ORACLE_ERR_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || page_size < 1 || max_blocks < 1 || num_pages < 1)
     return ORACLE_ERR_ARG;
   if (Hq % Hkv != 0) return ORACLE_ERR_ARG;
+  const int n_out = cu_q ? T : B; /* output rows per head */
   if (rows) {
     if (n_rows < 0) return ORACLE_ERR_ARG;
     for (int i = 0; i < n_rows; ++i)
-      if (rows[i] < 0 || rows[i] >= B * Hq) return ORACLE_ERR_ARG;
+      if (rows[i] < 0 || rows[i] >= n_out * Hq) return ORACLE_ERR_ARG;
   }
   if (n_threads < 1) n_threads = 1;
 
@@ -202,6 +230,7 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_
     j->B = B; j->Hq = Hq; j->Hkv = Hkv; j->D = D; j->page_size = page_size;
     j->max_blocks = max_blocks; j->num_pages = num_pages; j->window = window;
     j->rows = rows; j->n_rows = n_rows; j->out = out;
+    j->cu_q = cu_q; j->T = T;
     j->n_threads = n_threads; j->thread_id = t; j->status = ORACLE_OK;
   }
   int status = ORACLE_OK;
@@ -222,6 +251,46 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_
   free(jobs);
   free(tids);
   return status;
+}
+
+int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                        const int32_t* block_table, const int32_t* seq_lens, int32_t B,
+                        int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                        int32_t max_blocks, int64_t num_pages, int32_t window,
+                        const int32_t* rows, int32_t n_rows, double* out, int32_t n_threads) {
+  return run_jobs(q, k_pool, v_pool, block_table, seq_lens, NULL, 0, B, Hq, Hkv, D, page_size, max_blocks,
+                  num_pages, window, rows, n_rows, out, n_threads);
+}
+
+/*
+ * Multi-query attention over the paged cache (prefill of a chunk of new
+ * tokens whose keys and values are already in the cache), fp64.
+ *
+ * Attention.lean, `causalGQA` and `slidingGQA` with S > 1: query s at
+ * position pos s sees key l iff l <= pos s (and pos s < l + window).  Here
+ * sequence b holds L = seq_lens[b] cached tokens and n = cu_q[b+1] - cu_q[b]
+ * queries, the last n tokens: query i (packed row cu_q[b] + i) sits at
+ * position L - n + i.  Query row s of causalGQA depends on pos s alone, so it
+ * equals decodeGQA over the first pos s + 1 tokens; that is how each row is
+ * computed.
+ *
+ * q           bf16 bits [T, Hq, D], T = cu_q[B], rows packed sequence by sequence
+ * cu_q        int32 [B+1], cu_q[0] = 0, non-decreasing; n <= L for every sequence
+ * rows        NULL for every (t, h) row in t-major order, else n_rows flat
+ *             indices t*Hq + h
+ * out         double [n_rows (or T*Hq), D]
+ * the rest as for oracle_decode_paged
+ */
+int oracle_prefill_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                         int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size, int32_t max_blocks,
+                         int64_t num_pages, int32_t window, const int32_t* rows, int32_t n_rows, double* out,
+                         int32_t n_threads) {
+  if (!cu_q || B < 1 || cu_q[0] != 0) return ORACLE_ERR_ARG;
+  for (int b = 0; b < B; ++b)
+    if (cu_q[b + 1] < cu_q[b]) return ORACLE_ERR_ARG;
+  return run_jobs(q, k_pool, v_pool, block_table, seq_lens, cu_q, cu_q[B], B, Hq, Hkv, D, page_size, max_blocks,
+                  num_pages, window, rows, n_rows, out, n_threads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -32,8 +32,8 @@ MUTANTS = {
                              "return phys * j->page_size + (page % j->page_size);"),
     "logits_read_v_pool": ("const uint16_t* kv = j->k_pool + (r * j->Hkv + c) * D;",
                            "const uint16_t* kv = j->v_pool + (r * j->Hkv + c) * D;"),
-    "query_of_wrong_head": ("const uint16_t* qv = j->q + ((int64_t)b * j->Hq + h) * D;",
-                            "const uint16_t* qv = j->q + ((int64_t)b * j->Hq + c) * D;"),
+    "query_of_wrong_head": ("attend_one_row(j, b, h, j->q + ((int64_t)b * j->Hq + h) * j->D, L, o, logit)",
+                            "attend_one_row(j, b, h, j->q + ((int64_t)b * j->Hq + h / (j->Hq / j->Hkv)) * j->D, L, o, logit)"),
     "denominator_drops_last_term": ("    Z += logit[i];", "    Z += (i + 1 < n) ? logit[i] : 0.0;"),
 }
 

@@ -333,3 +333,75 @@ def make_append_case(kind, positions, seed, device="cpu", scale=1.0, full_cache=
     w_q = _norm_weight(shape["D"], gen, device)
     w_k = _norm_weight(shape["D"], gen, device)
     return AppendCase(kind, qkv, w_q, w_k, torch.tensor(positions, dtype=torch.int32, device=device), cache)
+
+
+# ---------------------------------------------------------------------------
+# Multi-query (prefill) cases: the last q_len[b] tokens of each sequence query
+# the paged cache, which already holds their keys and values
+# ---------------------------------------------------------------------------
+
+@dataclass
+class PrefillCase:
+    """Packed queries q [T, Hq, D] (sequence b owns rows cu_q[b] .. cu_q[b+1]-1,
+    its last q_lens[b] tokens) and the paged cache they attend to."""
+    kind: str
+    q: torch.Tensor       # bf16 [T, Hq, D]
+    cu_q: torch.Tensor    # int32 [B+1]
+    q_lens: list
+    cache: DecodeCase     # pools, block table, seq_lens (= every cached token), window
+
+    @property
+    def T(self):
+        return self.q.shape[0]
+
+    def to(self, device):
+        return PrefillCase(self.kind, self.q.to(device), self.cu_q.to(device), list(self.q_lens),
+                           self.cache.to(device))
+
+
+def _poison_outside(k_pool, v_pool, block_table, first, seq_lens):
+    """NaN-fill every pool slot outside positions [first[b], L_b) of every sequence."""
+    num_pages = k_pool.shape[0]
+    keep = torch.zeros(num_pages * PAGE_SIZE, dtype=torch.bool)
+    for b, L in enumerate(seq_lens):
+        if L <= first[b]:
+            continue
+        pos = torch.arange(first[b], L)
+        phys = block_table[b, pos // PAGE_SIZE].long()
+        keep[phys * PAGE_SIZE + pos % PAGE_SIZE] = True
+    dead = (~keep).nonzero().flatten().to(k_pool.device)
+    nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+    k_pool.view(num_pages * PAGE_SIZE, -1).index_fill_(0, dead, nan)
+    v_pool.view(num_pages * PAGE_SIZE, -1).index_fill_(0, dead, nan)
+
+
+def make_prefill_case(kind, seq_lens, q_lens, seed, device="cpu", window=None, window_only=False, poison=True,
+                      Hq=None, Hkv=None, D=None):
+    """Sequences of seq_lens[b] cached tokens whose last q_lens[b] (1 <= q_len <= L,
+    or 0 for none) are queries.  The cache is built as by make_case; with
+    window_only only the pages the queries can see are allocated.  With poison
+    every slot no query may read is NaN: positions before the first query's
+    window, and the unused tail of the last page.  q is rms-normalised times a
+    weight vector, like the decode's q."""
+    assert len(seq_lens) == len(q_lens) and all(0 <= n <= L for n, L in zip(q_lens, seq_lens))
+    shape = dict(SLIDING if kind == "sliding" else GLOBAL)
+    w = shape["window"] if window is None else window
+    n_max = max(q_lens) if q_lens else 0
+    # allocate as for one query whose window reaches back to the first query's
+    alloc_window = w + max(n_max, 1) - 1 if w > 0 else w
+    cache = make_case(kind, seq_lens, seed, device=device, window=alloc_window, window_only=window_only,
+                      poison=False, Hq=Hq, Hkv=Hkv, D=D)
+    cache.window = w
+    if poison:
+        first = [max(0, L - n - w + 1) if w > 0 else 0 for L, n in zip(seq_lens, q_lens)]
+        _poison_outside(cache.k_pool, cache.v_pool, cache.block_table.cpu(), first, seq_lens)
+    Hq_, D_ = cache.q.shape[1], cache.q.shape[2]
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(int(seed) + 23)
+    T = sum(q_lens)
+    w_q = _norm_weight(D_, gen, device)
+    q = _rms_normalise(_randn_bf16((T, Hq_, D_), gen, device), w_q).to(torch.bfloat16)
+    cu = [0]
+    for n in q_lens:
+        cu.append(cu[-1] + int(n))
+    return PrefillCase(kind, q, torch.tensor(cu, dtype=torch.int32, device=device), [int(n) for n in q_lens], cache)
