@@ -259,6 +259,50 @@ int32_t attn_kv_append_global(const void* qkv, const void* w_q, const void* w_k,
                               int32_t max_blocks, int64_t num_pages, int32_t* status, void* stream);
 
 /*
+ * attn_prefill_sliding / attn_prefill_global -- multi-query attention over the
+ * paged cache, for a chunk of new tokens per sequence whose keys and values
+ * are already in the cache (Attention.lean `causalGQA` / `slidingGQA` with
+ * S > 1 queries, Op Specs page, "Attention"; shapes and scale 1 as in the
+ * decode calls above):
+ *
+ *   sequence b caches L = seq_lens[b] tokens; its last n = cu_q[b+1] - cu_q[b]
+ *   tokens are the queries, packed as rows cu_q[b] .. cu_q[b+1]-1 of q, and
+ *   query i sits at position p = L - n + i.  It sees key l iff l <= p (and
+ *   p - window < l when window > 0):
+ *       o[t, h] = sum over visible l of softmax_l(<q[t, h], k[l, h/G]>) * v[l, h/G]
+ *
+ * q            bf16 [total_q, 16, D], D = 256 (sliding) or 512 (global)
+ * k_pool, v_pool, block_table, num_pages, max_blocks: as for the decode calls
+ * seq_lens     int32 [batch], n <= L <= max_blocks*16 for every sequence
+ * cu_q         int32 [batch + 1], cu_q[0] = 0, non-decreasing, cu_q[batch] = total_q
+ * o            [total_q, 16, D], bf16 (RNE) or fp32 per out_dtype
+ * max_q        host-side bound on the per-sequence query count n (sizes the grid)
+ * window       sliding: > 0 (1024 for Gemma-4-12B); global: <= 0 none, > 0 a window
+ * status       optional device int32: a sequence with n > L, L beyond the
+ *              table, n > max_q or rows past total_q raises
+ *              ATTN_DEV_BAD_SEQ_LEN and that sequence's rows (or those past
+ *              max_q) are not written; a visible page id outside
+ *              [0, num_pages) raises ATTN_DEV_BAD_PAGE and is read as zeros.
+ *
+ * All pointers are device pointers owned by the caller (q and o may be null
+ * when total_q is 0); nothing is allocated and nothing synchronises.
+ * Alignment: q, o and the pools 16 bytes, the int32
+ * arrays 4.  Asynchronous on `stream`, launched as a programmatic dependent of
+ * the previous kernel.  Computed with bf16 tensor-core products and fp32
+ * accumulation; P is rounded to bf16 for the P*V product.  Returns ATTN_OK
+ * (also when max_q is 0: nothing is launched) or ATTN_ERR_* with nothing
+ * launched.
+ */
+int32_t attn_prefill_sliding(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* cu_q, void* o, int32_t batch, int32_t total_q,
+                             int32_t max_q, int32_t max_blocks, int64_t num_pages, int32_t window, int32_t out_dtype,
+                             int32_t* status, void* stream);
+int32_t attn_prefill_global(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                            const int32_t* seq_lens, const int32_t* cu_q, void* o, int32_t batch, int32_t total_q,
+                            int32_t max_q, int32_t max_blocks, int64_t num_pages, int32_t window, int32_t out_dtype,
+                            int32_t* status, void* stream);
+
+/*
  * attn_selftest_wait_timeout -- exercises the device-side failure path of the
  * copy pipeline.  It launches one warp that waits, with the same bounded
  * wait and time limit as the decode kernels (1 s), on a shared-memory

@@ -36,6 +36,7 @@ SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
 
 EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_plan",
            "attn_decode_workspace_size", "attn_kv_append_sliding", "attn_kv_append_global",
+           "attn_prefill_sliding", "attn_prefill_global",
            "attn_last_error", "attn_abi_version")
 APPEND_ROW = {KIND_SLIDING: 16 * 256 + 2 * 8 * 256, KIND_GLOBAL: 16 * 512 + 512}  # qkv row length
 
@@ -82,6 +83,13 @@ def load(path=None):
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = app
+    pre = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,  # q k_pool v_pool block_table seq_lens cu_q o
+           c_i32, c_i32, c_i32, c_i32, c_i64,          # batch total_q max_q max_blocks num_pages
+           c_i32, c_i32, c_vp, c_vp]                   # window out_dtype status stream
+    for name in ("attn_prefill_sliding", "attn_prefill_global"):
+        fn = getattr(lib, name)
+        fn.restype = c_i32
+        fn.argtypes = pre
     lib.attn_selftest_delayed_copy.restype = c_i32
     lib.attn_selftest_delayed_copy.argtypes = [c_vp, c_vp, c_i64, c_i32, c_vp]
     lib.attn_last_error.restype = ctypes.c_char_p
@@ -301,6 +309,55 @@ def attn_kv_append_global(qkv, w_q, w_k, block_table, positions, k_pool, v_pool,
     """
     return _append(KIND_GLOBAL, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream)
 
+
+
+def _prefill(kind, q, k_pool, v_pool, block_table, seq_lens, cu_q, o, max_q, window, out_dtype, status, stream):
+    Hq, Hkv, D = SHAPES[kind]
+    if q.dim() != 3:
+        raise ValueError("q must be [total_q, %d, %d]" % (Hq, D))
+    total_q, batch = q.shape[0], seq_lens.shape[0]
+    num_pages, max_blocks = k_pool.shape[0], block_table.shape[1]
+    if max_q is None:
+        counts = (cu_q[1:] - cu_q[:-1]).cpu()   # host bound for the grid (synchronises)
+        max_q = int(counts.max().item()) if counts.numel() else 0
+    if o is None:
+        o = torch.empty((total_q, Hq, D), dtype=out_dtype, device=q.device)
+    code = {torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}.get(o.dtype)
+    if code is None:
+        raise ValueError("o must be bf16 or fp32")
+    args = [_ptr(q, "q", torch.bfloat16, (total_q, Hq, D)),
+            _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
+            _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
+            _ptr(block_table, "block_table", torch.int32, (batch, max_blocks)),
+            _ptr(seq_lens, "seq_lens", torch.int32, (batch,)),
+            _ptr(cu_q, "cu_q", torch.int32, (batch + 1,)),
+            _ptr(o, "o", o.dtype, (total_q, Hq, D))]
+    st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    lib = load()
+    fn = lib.attn_prefill_sliding if kind == KIND_SLIDING else lib.attn_prefill_global
+    rc = fn(*args, batch, total_q, int(max_q), max_blocks, num_pages, int(window), code, st_ptr, s_ptr)
+    if rc != ATTN_OK:
+        raise AttnDecodeError(rc, attn_last_error())
+    return o
+
+
+def attn_prefill_sliding(q, k_pool, v_pool, block_table, seq_lens, cu_q, o=None, *, max_q=None, window=1024,
+                         out_dtype=torch.bfloat16, status=None, stream=None):
+    """slidingGQA for the last n tokens of each sequence (n = cu_q[b+1] - cu_q[b]):
+    q [total_q,16,256] packed by sequence, pools as for the decode -> o [total_q,16,256].
+    max_q: host bound on n (read from cu_q, with a synchronisation, when None)."""
+    return _prefill(KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, cu_q, o, max_q, window, out_dtype,
+                    status, stream)
+
+
+def attn_prefill_global(q, k_pool, v_pool, block_table, seq_lens, cu_q, o=None, *, max_q=None, window=0,
+                        out_dtype=torch.bfloat16, status=None, stream=None):
+    """causalGQA for the last n tokens of each sequence: q [total_q,16,512] -> o [total_q,16,512]."""
+    return _prefill(KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, cu_q, o, max_q, window, out_dtype,
+                    status, stream)
 
 def selftest_delayed_copy(dst, src, delay_ns=5000, stream=None):
     """attn_selftest_delayed_copy: copy src into dst (same-size int32 CUDA tensors)

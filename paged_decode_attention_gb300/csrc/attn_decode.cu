@@ -14,6 +14,7 @@
 #include "combine.cuh"
 #include "global.cuh"
 #include "kv_append.cuh"
+#include "prefill.cuh"
 #include "sliding.cuh"
 
 namespace {
@@ -162,6 +163,25 @@ int32_t encode_global_page_map(CUtensorMap* map, const void* pool, int64_t num_p
                    elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (page map) failed (%d)", static_cast<int>(r));
+  return ATTN_OK;
+}
+
+// A pool [num_pages*16 rows][Hkv*D] seen as a 3-D tensor (x: 64 dims of a
+// chunk, y: row, z: chunk of 64 dims, stride 128 bytes); a box {64, 16,
+// chunks} copies `chunks` consecutive chunks of a page's 16 rows (one KV
+// head's D dims at z = c * D / 64) as swizzled [16 rows][64] tiles.
+int32_t encode_chunk_map(CUtensorMap* map, const void* pool, int64_t num_pages, int row_elems, int chunks) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_pages) * ATTN_PAGE_SIZE,
+                              static_cast<cuuint64_t>(row_elems / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_elems) * 2, 128};
+  const cuuint32_t box[3] = {64, ATTN_PAGE_SIZE, static_cast<cuuint32_t>(chunks)};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
+                   elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (chunk map) failed (%d)", static_cast<int>(r));
   return ATTN_OK;
 }
 
@@ -490,6 +510,90 @@ extern "C" int32_t attn_selftest_wait_timeout(int32_t* status, void* stream) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attn_selftest_wait_timeout: launch failed: %s", cudaGetErrorString(e));
   return ATTN_OK;
+}
+
+namespace {
+
+// Multi-query attention over the paged cache (attn_prefill_*).
+template <typename C>
+int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                    const int32_t* seq_lens, const int32_t* cu_q, void* o, int32_t batch, int32_t total_q,
+                    int32_t max_q, int32_t max_blocks, int64_t num_pages, int32_t window, int32_t out_dtype,
+                    int32_t* status, void* stream) {
+  g_err[0] = '\0';
+  const char* name = kind == ATTN_KIND_SLIDING ? "attn_prefill_sliding" : "attn_prefill_global";
+  if (!k_pool || !v_pool || !block_table || !seq_lens || !cu_q || (total_q > 0 && (!q || !o)))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  auto aligned = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; };
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(cu_q, 4) || (status && !aligned(status, 4)))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer (q, o and the pools 16 bytes, tables 4)", name);
+  if (batch < 1 || batch > ATTN_MAX_BATCH)
+    return fail(ATTN_ERR_UNSUPPORTED, "%s: batch %d outside [1, %d]", name, batch, ATTN_MAX_BATCH);
+  if (total_q < 0 || max_q < 0 || max_q > total_q || max_q > ATTN_MAX_SEQ_LEN)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: need 0 <= max_q <= total_q and max_q <= %d", name, ATTN_MAX_SEQ_LEN);
+  if (static_cast<int64_t>(total_q) * C::kHq * C::kD > (int64_t{1} << 40))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: total_q %d too large", name, total_q);
+  if (max_blocks < 1) return fail(ATTN_ERR_INVALID_ARG, "%s: max_blocks must be >= 1", name);
+  if (num_pages < 1 || num_pages > (int64_t{1} << 31) / ATTN_PAGE_SIZE - 1)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: num_pages %lld out of range", name, static_cast<long long>(num_pages));
+  if (kind == ATTN_KIND_SLIDING && window <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: window must be > 0", name);
+  if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: out_dtype must be ATTN_OUT_BF16 or ATTN_OUT_F32", name);
+  if (max_q == 0) return ATTN_OK;  // no queries
+
+  int dev = 0, num_sms = 0;
+  int32_t st = current_device(&dev, &num_sms);
+  if (st != ATTN_OK) return st;
+  static bool smem_set[2][kMaxDevices] = {{false}};
+  if ((st = ensure_smem(pda::prefill::prefill_kernel<C>, C::kSmemBytes, dev, smem_set[kind]))) return st;
+
+  CUtensorMap tm_k, tm_v;
+  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, C::kChunks))) return st;
+  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, C::kChunks))) return st;
+
+  pda::prefill::PrefillParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.cu_q = cu_q;
+  p.o = o;
+  p.status = status;
+  p.num_pages = num_pages;
+  p.batch = batch;
+  p.max_blocks = max_blocks;
+  p.window = window;
+  p.total_q = total_q;
+  p.out_f32 = out_dtype == ATTN_OUT_F32;
+  const dim3 grid((max_q + C::kQT - 1) / C::kQT, C::kHkv, batch);
+  cudaError_t e = launch_pdl(pda::prefill::prefill_kernel<C>, grid, C::kThreads, C::kSmemBytes,
+                             static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t attn_prefill_sliding(const void* q, const void* k_pool, const void* v_pool,
+                                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q,
+                                        void* o, int32_t batch, int32_t total_q, int32_t max_q, int32_t max_blocks,
+                                        int64_t num_pages, int32_t window, int32_t out_dtype, int32_t* status,
+                                        void* stream) {
+  return run_prefill<pda::prefill::SlidingConfig>(ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, cu_q,
+                                                  o, batch, total_q, max_q, max_blocks, num_pages, window, out_dtype,
+                                                  status, stream);
+}
+
+extern "C" int32_t attn_prefill_global(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q,
+                                       void* o, int32_t batch, int32_t total_q, int32_t max_q, int32_t max_blocks,
+                                       int64_t num_pages, int32_t window, int32_t out_dtype, int32_t* status,
+                                       void* stream) {
+  return run_prefill<pda::prefill::GlobalConfig>(ATTN_KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, cu_q, o,
+                                                 batch, total_q, max_q, max_blocks, num_pages, window, out_dtype,
+                                                 status, stream);
 }
 
 // Waits for the previous kernel in the stream, lets its own dependents launch
