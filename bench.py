@@ -41,6 +41,18 @@ METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and attention cal
 UNIT = "GB/s"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# Multi-query (prefill) workloads timed beside the decode: new tokens whose
+# keys and values are already in the cache attend to it (no such workload is
+# given with the decode configurations; these are chosen to span both layer
+# types at prompt-chunk sizes).
+PREFILL_WORKLOADS = {
+    "sliding": dict(seq_lens=[8192] * 4, q_lens=[2048] * 4,
+                    name="sliding prefill: B=4 x 2048 new tokens on 8192-token contexts, 16/8 heads, D=256, window 1024"),
+    "global": dict(seq_lens=[32768], q_lens=[4096],
+                   name="global prefill: B=1 x 4096 new tokens on a 32768-token context, 16/1 heads, D=512"),
+}
 NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 
 # DRAM bytes per launch of the dominant decode kernel (dram__bytes_read.sum +
@@ -117,6 +129,63 @@ def aggregate(per_rank, steps, warmup, n_gpus, config, dtype="bf16"):
         "data": "synthetic",
         "config": config,
     }
+
+
+def prefill_flops(seq_lens, q_lens, window, D, Hq=16):
+    """4 D flops (q.k and p.v) per query head per visible key: query i of a
+    sequence's last n tokens sits at position L - n + i and sees min(p + 1, window) keys."""
+    total = 0
+    for L, n in zip(seq_lens, q_lens):
+        for i in range(n):
+            p = L - n + i
+            total += min(p + 1, window) if window > 0 else p + 1
+    return 4 * D * Hq * total
+
+
+def load_bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def time_prefill(stream, dev, reps=5):
+    """attn_prefill_* on PREFILL_WORKLOADS: TFLOP/s of the algorithmic flops,
+    CUDA events on the launching stream around `reps` back-to-back calls."""
+    import torch
+    import paged_decode_attention_gb300 as pda
+    from workloads import make_prefill_case
+    out = {}
+    for kind, w in PREFILL_WORKLOADS.items():
+        case = make_prefill_case(kind, w["seq_lens"], w["q_lens"], seed=9, device=dev, poison=False, window_only=True)
+        c = case.cache
+        fn = pda.attn_prefill_sliding if kind == "sliding" else pda.attn_prefill_global
+        o = torch.empty_like(case.q)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        kw = dict(window=c.window, max_q=max(w["q_lens"]), status=status, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fn(case.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, case.cu_q, o, **kw)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn(case.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, case.cu_q, o, **kw)
+            e1.record(stream)
+        e1.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status %d in the prefill" % int(status.item()))
+        ms = e0.elapsed_time(e1) / reps
+        flops = prefill_flops(w["seq_lens"], w["q_lens"], c.window, c.D)
+        out[kind] = {"workload": w["name"], "ms_per_call": round(ms, 4), "flops_per_call": flops,
+                     "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                     "launch": "%d back-to-back calls, CUDA events" % reps}
+        del case, o
+    return out
 
 
 def load_peaks():
@@ -406,10 +475,12 @@ def run_ours(args, rank, world, local_rank):
 
     # --- the step before the decode: norms, RoPE and the cache append ---
     append = time_append(calls0, stream, status, dev)
+    # --- multi-query attention over the paged cache (prefill) ---
+    prefill = None if args.no_prefill else time_prefill(stream, dev)
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the cache append" % int(status.item()))
 
-    res.update(per_type=per_type, append=append)
+    res.update(per_type=per_type, append=append, prefill=prefill)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
                heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
                launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
@@ -718,6 +789,7 @@ def main(argv=None):
     ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4b", "5"])
     ap.add_argument("--no-graph", action="store_true", help="launch every call directly (no CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill timing")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="thread blocks per KV head (0 = the library's automatic plan)")
     args = ap.parse_args(argv)
@@ -761,6 +833,12 @@ def main(argv=None):
         line["per_layer_type"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4))
                                   for k, v in r0["per_type"].items()}
     line["gpu_launches"] = r0["launches_per_step"] * args.steps
+    if r0.get("prefill"):
+        tpeak, tsrc = load_bf16_peak()
+        line["prefill"] = {k: dict(v, roofline={"bound": "tensor", "achieved": v["value"], "peak": tpeak,
+                                                "unit": "TFLOP/s", "frac": round(v["value"] / tpeak, 4),
+                                                "peak_source": tsrc})
+                           for k, v in r0["prefill"].items()}
     if r0.get("append"):
         line["append"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4)) for k, v in r0["append"].items()}
     line["e2e"] = r0["e2e"]

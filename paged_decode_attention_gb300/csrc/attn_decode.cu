@@ -14,7 +14,7 @@
 #include "combine.cuh"
 #include "global.cuh"
 #include "kv_append.cuh"
-#include "prefill.cuh"
+#include "prefill_tc.cuh"
 #include "sliding.cuh"
 
 namespace {
@@ -547,13 +547,13 @@ int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void*
   int32_t st = current_device(&dev, &num_sms);
   if (st != ATTN_OK) return st;
   static bool smem_set[2][kMaxDevices] = {{false}};
-  if ((st = ensure_smem(pda::prefill::prefill_kernel<C>, C::kSmemBytes, dev, smem_set[kind]))) return st;
+  if ((st = ensure_smem(pda::prefill_tc::prefill_tc_kernel<C>, C::kSmemBytes, dev, smem_set[kind]))) return st;
 
-  CUtensorMap tm_k, tm_v;
-  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, C::kChunks))) return st;
-  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, C::kChunks))) return st;
+  CUtensorMap tm_k, tm_v;  // boxes of one page's 16 rows x 64 dims
+  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, 1))) return st;
+  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, 1))) return st;
 
-  pda::prefill::PrefillParams p{};
+  pda::prefill_tc::PrefillParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.block_table = block_table;
   p.seq_lens = seq_lens;
@@ -566,8 +566,8 @@ int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void*
   p.window = window;
   p.total_q = total_q;
   p.out_f32 = out_dtype == ATTN_OUT_F32;
-  const dim3 grid((max_q + C::kQT - 1) / C::kQT, C::kHkv, batch);
-  cudaError_t e = launch_pdl(pda::prefill::prefill_kernel<C>, grid, C::kThreads, C::kSmemBytes,
+  const dim3 grid((max_q + C::kQ - 1) / C::kQ, C::kHkv * C::kSlices, batch);
+  cudaError_t e = launch_pdl(pda::prefill_tc::prefill_tc_kernel<C>, grid, C::kThreads, C::kSmemBytes,
                              static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
@@ -581,7 +581,7 @@ extern "C" int32_t attn_prefill_sliding(const void* q, const void* k_pool, const
                                         void* o, int32_t batch, int32_t total_q, int32_t max_q, int32_t max_blocks,
                                         int64_t num_pages, int32_t window, int32_t out_dtype, int32_t* status,
                                         void* stream) {
-  return run_prefill<pda::prefill::SlidingConfig>(ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, cu_q,
+  return run_prefill<pda::prefill_tc::SlidingConfig>(ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, cu_q,
                                                   o, batch, total_q, max_q, max_blocks, num_pages, window, out_dtype,
                                                   status, stream);
 }
@@ -591,7 +591,7 @@ extern "C" int32_t attn_prefill_global(const void* q, const void* k_pool, const 
                                        void* o, int32_t batch, int32_t total_q, int32_t max_q, int32_t max_blocks,
                                        int64_t num_pages, int32_t window, int32_t out_dtype, int32_t* status,
                                        void* stream) {
-  return run_prefill<pda::prefill::GlobalConfig>(ATTN_KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, cu_q, o,
+  return run_prefill<pda::prefill_tc::GlobalConfig>(ATTN_KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, cu_q, o,
                                                  batch, total_q, max_q, max_blocks, num_pages, window, out_dtype,
                                                  status, stream);
 }

@@ -1,0 +1,458 @@
+// prefill_tc.cuh -- multi-query attention over the paged cache on the 5th-
+// generation tensor cores (tcgen05): the last n tokens of a sequence of L
+// cached tokens query the cache, which already holds their keys and values
+// (Attention.lean `causalGQA` / `slidingGQA` with S > 1): query i sits at
+// position p = L - n + i and sees key l iff l <= p (and p - window < l with
+// a window); scale 1; query head c*G + g reads KV head c.
+//
+// Block (tile, c * kSlices + slice, b): 128 rows = kQ = 128 / G queries of
+// sequence b times the G query heads of KV head c, row r being head r / kQ of
+// query r % kQ; `slice` selects which kDS of the D output dims it writes
+// (D = 512 is split in two so that O fits in tensor memory).  Per page of 16
+// keys:
+//   S   = Q K^T    tcgen05.mma M=128, N=16, K=D, A = Q (shared memory, K-major,
+//                  128-byte swizzle), B = the page's K tile as TMA wrote it;
+//                  accumulator in tensor memory, two buffers (a step is
+//                  kPPS pages: N = 16 kPPS keys);
+//   P   = softmax  warps 0-3, one thread per row (TMEM lane = row): masks,
+//                  running max, P rounded to bf16 into shared memory as
+//                  K-major core matrices;
+//   O  += P V      tcgen05.mma M=128, N=kDS, K=16, B = the V tile, MN-major
+//                  with the 128-byte swizzle; accumulator O in tensor memory.
+// Warp 4 streams the pages by TMA, warp 5 allocates tensor memory and one of
+// its threads issues the MMAs.  S of page j+1 is computed while the softmax
+// of page j runs, and P V of page j while the softmax of page j+1 runs.
+//
+// Running max.  A row's reference max m moves only when a score exceeds it by
+// more than 2^8 (kSlack log2 units): exp2(s - m) <= 256 stays well inside fp32
+// and bf16, numerator and denominator share m, so the result is the same
+// softmax; O is rescaled in tensor memory only then (rarely after a row's
+// first pages).  Key rows outside [k_lo, k_hi] of the first and last page are
+// zeroed in shared memory before P V (0 * NaN would be NaN); masked scores
+// become -inf.
+#pragma once
+
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+namespace pda {
+namespace prefill_tc {
+
+struct PrefillParams {
+  const __nv_bfloat16* q;      // [total_q, Hq, D]
+  const int32_t* block_table;  // [batch, max_blocks]
+  const int32_t* seq_lens;     // [batch]
+  const int32_t* cu_q;         // [batch + 1]
+  void* o;                     // [total_q, Hq, D], bf16 or fp32
+  int32_t* status;             // optional ATTN_DEV_* word
+  int64_t num_pages;
+  int32_t batch;
+  int32_t max_blocks;
+  int32_t window;  // > 0: sliding window; <= 0: none
+  int32_t total_q;
+  int32_t out_f32;
+};
+
+// 3-D tile copy without a cache hint: every query tile of a sequence reads the
+// same pages, so they should stay in L2 as long as possible.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_>
+struct Config {
+  static constexpr int kD = kD_;    // head dim (the contraction of S)
+  static constexpr int kDS = kDS_;  // output dims per block
+  static constexpr int kG = kG_;
+  static constexpr int kHkv = kHkv_;
+  static constexpr int kHq = kG * kHkv;
+  static constexpr int kStages = kStages_;
+  static constexpr int kPPS = kPPS_;                 // pages per step
+  static constexpr int kKeys = kPPS * kPage;         // keys per step: N of S, K of P V
+  static constexpr int kSlices = kD / kDS;
+  static constexpr int kRows = 128;
+  static constexpr int kQ = kRows / kG;  // queries per block
+  static constexpr int kKChunks = kD / 64;
+  static constexpr int kVChunks = kDS / 64;
+  static constexpr int kQChunkBytes = kRows * 128;  // [128 rows][64 dims]
+  static constexpr int kChunkRows = kKeys * 128;     // one chunk of a step: [kKeys rows][64 dims]
+  static constexpr int kKTile = kKChunks * kChunkRows;
+  static constexpr int kVTile = kVChunks * kChunkRows;
+  static constexpr int kPBytes = kRows * kKeys * 2;
+  static constexpr int kThreads = 6 * 32;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSCol = kDS;  // S buffers at columns kDS and kDS + kKeys
+  static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0, 0);
+  static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDS, 0, 1);
+  static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
+  static_assert(kSCol + 2 * kKeys <= kTmemCols, "O and two S buffers fit in tensor memory");
+  static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
+
+  struct Smem {
+    alignas(1024) uint8_t q[kKChunks][kQChunkBytes];
+    alignas(1024) uint8_t k[kStages][kKTile];
+    alignas(1024) uint8_t v[kStages][kVTile];
+    alignas(128) uint8_t p[2][kPBytes];
+    alignas(8) uint64_t full[kStages];   // K and V of the stage landed (TMA)
+    alignas(8) uint64_t empty[kStages];  // both products of the stage's page done (commit)
+    alignas(8) uint64_t s_full[2];       // S buffer written (commit)
+    alignas(8) uint64_t s_free[2];       // S buffer read (4 softmax warps)
+    alignas(8) uint64_t p_full[2];       // P buffer written, O rescaled, V edges zeroed (4 warps)
+    alignas(8) uint64_t p_empty[2];      // P V of the buffer's page done (commit)
+    alignas(8) uint64_t q_ready;         // Q tile written (4 warps)
+    alignas(8) uint64_t mma_done;        // every MMA done (commit)
+    uint32_t tmem_base;
+  };
+  static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+};
+
+constexpr float kSlack = 8.f;  // log2 units
+
+// 16 bytes global -> shared without a register round trip; src_bytes 0
+// writes zeros (src is then not read).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+template <typename C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ PrefillParams p) {
+  constexpr int kD = C::kD, kDS = C::kDS, kG = C::kG, kHq = C::kHq, kQ = C::kQ, kStages = C::kStages;
+  constexpr int kPPS = C::kPPS;
+  extern __shared__ uint8_t smem_raw[];
+  typename C::Smem& s =
+      *reinterpret_cast<typename C::Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tile = blockIdx.x;
+  const int c = blockIdx.y / C::kSlices;
+  const int slice = blockIdx.y % C::kSlices;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], 4);
+      mbar_init(&s.p_full[i], 4);
+      mbar_init(&s.p_empty[i], 1);
+    }
+    mbar_init(&s.q_ready, 4);
+    mbar_init(&s.mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+  }
+  if (warp == 5) tmem_alloc(&s.tmem_base, C::kTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+
+  // q, the cache and the tables may be written by the previous kernel in the stream.
+  wait_for_primary_grid();
+  allow_dependent_launch();
+
+  // ---- this block's queries and the keys they can see (uniform) ----
+  const int q0 = p.cu_q[b];
+  const int n = p.cu_q[b + 1] - q0;
+  const int i0 = tile * kQ;
+  const int L = p.seq_lens[b];
+  const int cap = p.max_blocks < ATTN_MAX_SEQ_LEN / kPage ? p.max_blocks * kPage : ATTN_MAX_SEQ_LEN;
+  bool run = true;
+  if (n < 0 || q0 < 0 || static_cast<int64_t>(q0) + n > p.total_q) {
+    if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
+    run = false;
+  } else {
+    if (tile + 1 == static_cast<int>(gridDim.x) && i0 + kQ < n && threadIdx.x == 0 && slice == 0)
+      report(p.status, ATTN_DEV_BAD_SEQ_LEN);  // more queries than the host's max_q: the rest are not computed
+    if (i0 >= n) {
+      run = false;
+    } else if (L < n || L > cap) {
+      if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
+      run = false;
+    }
+  }
+
+  if (run) {
+    const int P0 = L - n + i0;                   // position of the block's first query
+    const int nq = n - i0 < kQ ? n - i0 : kQ;    // valid queries in the block
+    const int k_hi = P0 + nq - 1;                // last visible key (inclusive)
+    const int k_lo = p.window > 0 ? (P0 - p.window + 1 > 0 ? P0 - p.window + 1 : 0) : 0;
+    const int page0 = k_lo / kPage;
+    const int n_pages = k_hi / kPage - page0 + 1;
+    const int n_steps = (n_pages + kPPS - 1) / kPPS;
+
+    if (warp == 4) {
+      // ---------------- producer: step i = pages page0 + i*kPPS ... ----------------
+      // Lane pg < kPPS copies page pg of the step chunk by chunk, so that the
+      // step's pages sit contiguously in each [kKeys rows][64 dims] chunk.
+      // Pages past the range (the last step) and bad page ids are copied from
+      // a fully out-of-range row: zeros.
+      static_assert(32 % kPPS == 0, "a step's pages in one batch of 32 table entries");
+      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+      bool ok = true;
+      int issued = 0;
+      // block-table entries of pages 32k + lane, one batch ahead
+      int cur = lane < n_pages ? bt[page0 + lane] : -1;
+      int nxt = 32 + lane < n_pages ? bt[page0 + 32 + lane] : -1;
+      for (int i = 0; i < n_steps; ++i) {
+        const int gp0 = i * kPPS;
+        if (gp0 > 0 && (gp0 & 31) == 0) {
+          cur = nxt;
+          nxt = gp0 + 32 + lane < n_pages ? bt[page0 + gp0 + 32 + lane] : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, cur, (gp0 + (lane < kPPS ? lane : 0)) & 31);
+        const int stage = i % kStages;
+        if (i >= kStages) {
+          const int w = lane == 0 ? static_cast<int>(mbar_wait(&s.empty[stage], ((i / kStages) - 1) & 1)) : 0;
+          ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        }
+        if (!ok) {
+          if (lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], C::kKTile + C::kVTile);
+        __syncwarp();
+        if (lane < kPPS) {
+          const int gp = gp0 + lane;
+          int32_t y = -kPage;
+          if (gp < n_pages) {
+            if (phys < 0 || static_cast<int64_t>(phys) >= p.num_pages)
+              report(p.status, ATTN_DEV_BAD_PAGE);
+            else
+              y = phys * kPage;
+          }
+#pragma unroll
+          for (int ch = 0; ch < C::kKChunks; ++ch)
+            tma_load_3d(s.k[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_k, 0, y,
+                                 c * C::kKChunks + ch, &s.full[stage]);
+#pragma unroll
+          for (int ch = 0; ch < C::kVChunks; ++ch)
+            tma_load_3d(s.v[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_v, 0, y,
+                                 c * C::kKChunks + slice * C::kVChunks + ch, &s.full[stage]);
+        }
+        ++issued;
+        __syncwarp();
+      }
+      if (lane == 0) {  // no copy may still be landing when the block retires
+        for (int st = 0; st < kStages && st < issued; ++st) {
+          const int uses = (issued - 1 - st) / kStages + 1;
+          if (!mbar_wait(&s.full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        }
+      }
+    } else if (warp == 5) {
+      // ---------------- MMA issuer (one thread) ----------------
+      if (lane == 0) {
+        bool ok = mbar_wait(&s.q_ready, 0);
+        const uint32_t q_base = smem_addr(s.q[0]);
+        auto pv = [&](int j) {  // O += P_j V_j, kKeys / 16 products of K = 16
+          const int bp = j & 1;
+          const int st = j % kStages;
+          if (ok) ok = mbar_wait(&s.p_full[bp], (j >> 1) & 1);
+          tc_fence_after_sync();
+          const uint32_t p_base = smem_addr(s.p[bp]);
+          const uint32_t v_base = smem_addr(s.v[st]);
+#pragma unroll
+          for (int kk = 0; kk < C::kKeys / 16; ++kk) {
+            const uint64_t a_desc = umma_desc(p_base + kk * 256, 128, C::kKeys * 16, 0);
+            const uint64_t b_desc = umma_desc(v_base + kk * (16 * 128), C::kChunkRows, 1024, 2);
+            umma_bf16(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&s.empty[st]);
+          umma_commit(&s.p_empty[bp]);
+        };
+        for (int j = 0; j < n_steps; ++j) {
+          const int st = j % kStages;
+          const int bs = j & 1;
+          if (ok) ok = mbar_wait(&s.full[st], (j / kStages) & 1);
+          if (ok && j >= 2) ok = mbar_wait(&s.s_free[bs], ((j - 2) >> 1) & 1);
+          tc_fence_after_sync();
+          const uint32_t k_base = smem_addr(s.k[st]);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
+            const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
+            umma_bf16(tmem + C::kSCol + C::kKeys * bs, a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s.s_full[bs]);
+          if (j >= 1) pv(j - 1);
+        }
+        pv(n_steps - 1);
+        umma_commit(&s.mma_done);
+        if (!mbar_wait(&s.mma_done, 0)) ok = false;  // every product done before the memory is freed
+        if (!ok) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      }
+      __syncwarp();
+    } else {
+      // ---------------- softmax and epilogue: one thread per row ----------------
+      const int r = threadIdx.x;  // 0..127: TMEM lane r
+      const int g = r / kQ;
+      const int qi = r % kQ;
+      const bool valid = qi < nq;
+      const int head = c * kG + g;
+      const int pos = P0 + qi;
+      const int lo_r = p.window > 0 ? pos - p.window + 1 : 0;
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+
+      // Q row into shared memory: K-major, 128-byte swizzle, chunks of 64 dims
+      {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            p.q + (static_cast<size_t>(valid ? q0 + i0 + qi : 0) * kHq + head) * kD);
+        const uint32_t q_base = smem_addr(s.q[0]);
+#pragma unroll 8
+        for (int u = 0; u < kD / 8; ++u)
+          cp_async_16(q_base + (u >> 3) * C::kQChunkBytes + r * 128 + (((u & 7) ^ (r & 7)) << 4), src + 16 * u,
+                      valid ? 16u : 0u);
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.q_ready);
+      }
+
+      float m = -INFINITY, l = 0.f;  // reference max (log2 units) and row sum
+      bool ok = true;
+      for (int j = 0; j < n_steps; ++j) {
+        const int bs = j & 1;
+        const int pos0 = (page0 + j * kPPS) * kPage;  // key of column 0
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[bs], (j >> 1) & 1));
+        tc_fence_after_sync();
+        float sv[C::kKeys];
+#pragma unroll
+        for (int blk = 0; blk < C::kKeys / 16; ++blk)
+          tmem_ld16(t_row + C::kSCol + C::kKeys * bs + 16 * blk, *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+        tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.s_free[bs]);
+
+        if (!valid || pos0 < lo_r || pos0 + C::kKeys - 1 > pos) {
+#pragma unroll
+          for (int k = 0; k < C::kKeys; ++k) {
+            const int key = pos0 + k;
+            if (!valid || key < lo_r || key > pos) sv[k] = -INFINITY;
+          }
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int k = 1; k < C::kKeys; ++k) mx = fmaxf(mx, sv[k]);
+        const float m_new = mx * kLog2e;
+        const bool move = m_new > m + kSlack;  // false while the row has no visible key
+        const bool rescale = move && m != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O's row holds P V up to step j-1: wait for that product, then scale in place
+          if (ok && j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          tc_fence_after_sync();
+          const float f = rescale ? ex2_approx(m - m_new) : 1.f;
+#pragma unroll 1
+          for (int col = 0; col < kDS; col += 16) {
+            float ov[16];
+            tmem_ld16(t_row + col, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) ov[k] *= f;
+            tmem_st16(t_row + col, ov);
+          }
+          tmem_wait_st();
+          l *= f;
+        }
+        if (move) m = m_new;
+        const float m_use = m == -INFINITY ? 0.f : m;
+        float ls = 0.f;
+#pragma unroll
+        for (int k = 0; k < C::kKeys; ++k) {
+          sv[k] = ex2_approx(fmaf(sv[k], kLog2e, -m_use));
+          ls += sv[k];
+        }
+        l += ls;
+
+        // P row into buffer bs (K-major core matrices of 8 rows x 8 keys) once
+        // P V of step j-2 has read it
+        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[bs], ((j - 2) >> 1) & 1));
+        const uint32_t p_row = smem_addr(s.p[bs]) + (r >> 3) * (C::kKeys * 16) + (r & 7) * 16;
+#pragma unroll
+        for (int kc = 0; kc < C::kKeys / 8; ++kc)
+          st_shared_v4(p_row + kc * 128,
+                       make_uint4(pack_bf16x2(sv[8 * kc], sv[8 * kc + 1]), pack_bf16x2(sv[8 * kc + 2], sv[8 * kc + 3]),
+                                  pack_bf16x2(sv[8 * kc + 4], sv[8 * kc + 5]),
+                                  pack_bf16x2(sv[8 * kc + 6], sv[8 * kc + 7])));
+        // zero this step's V rows outside [k_lo, k_hi] (the first and last steps)
+        if (pos0 < k_lo || pos0 + C::kKeys - 1 > k_hi) {
+          const uint32_t v_base = smem_addr(s.v[j % kStages]);
+#pragma unroll 1
+          for (int it = r; it < C::kKeys * 8; it += 128) {
+            const int kr = it >> 3;  // key row of the step
+            const int key = pos0 + kr;
+            if (key < k_lo || key > k_hi) {
+#pragma unroll
+              for (int ch = 0; ch < C::kVChunks; ++ch)
+                st_shared_v4(v_base + ch * C::kChunkRows + kr * 128 + (it & 7) * 16, make_uint4(0, 0, 0, 0));
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.p_full[bs]);
+      }
+
+      // ---- epilogue: wait for the last P V, normalise, write this row's kDS dims ----
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1));
+      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      tc_fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t o_off = (static_cast<size_t>(q0 + i0 + qi) * kHq + head) * kD + slice * kDS;
+#pragma unroll 1
+      for (int col = 0; col < kDS; col += 16) {
+        float ov[16];
+        tmem_ld16(t_row + col, ov);
+        tmem_wait_ld();
+        if (!valid) continue;
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_off + col);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_float4(ov[4 * k] * inv, ov[4 * k + 1] * inv, ov[4 * k + 2] * inv, ov[4 * k + 3] * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_off + col);
+          dst[0] = make_uint4(pack_bf16x2(ov[0] * inv, ov[1] * inv), pack_bf16x2(ov[2] * inv, ov[3] * inv),
+                              pack_bf16x2(ov[4] * inv, ov[5] * inv), pack_bf16x2(ov[6] * inv, ov[7] * inv));
+          dst[1] = make_uint4(pack_bf16x2(ov[8] * inv, ov[9] * inv), pack_bf16x2(ov[10] * inv, ov[11] * inv),
+                              pack_bf16x2(ov[12] * inv, ov[13] * inv), pack_bf16x2(ov[14] * inv, ov[15] * inv));
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown: free the tensor memory ----------------
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per block, D = 256,
+// 6 stages of 16 KB.  Global: 8 queries x 16 heads per block, D = 512 split
+// into two blocks of 256 output dims (both compute S), 3 stages of 24 KB.
+using SlidingConfig = Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 2, 4>;
+using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 3, 1>;
+
+}  // namespace prefill_tc
+}  // namespace pda

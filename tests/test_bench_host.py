@@ -36,6 +36,15 @@ def test_append_bytes_per_token():
     assert bench.append_bytes("global", 0) == 2 * 512 * 2
 
 
+def test_prefill_flops_count_visible_keys():
+    # a 3-token prompt from scratch: queries at 0, 1, 2 see 1 + 2 + 3 keys; 4 D flops per key per head
+    assert bench.prefill_flops([3], [3], 0, 8, Hq=1) == 4 * 8 * 6
+    # a window of 2 caps them: 1 + 2 + 2
+    assert bench.prefill_flops([3], [3], 2, 8, Hq=1) == 4 * 8 * 5
+    # the last 2 tokens of 10 sit at positions 8 and 9
+    assert bench.prefill_flops([10], [2], 0, 8, Hq=2) == 4 * 8 * 2 * (9 + 10)
+
+
 def test_rotation_exceeds_l2():
     n = bench.rotation_count(67 * 10**6)
     assert n * 67 * 10**6 > 3 * bench.L2_BYTES
