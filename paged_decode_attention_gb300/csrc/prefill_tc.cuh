@@ -64,7 +64,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_>
+template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
@@ -73,6 +73,7 @@ struct Config {
   static constexpr int kHq = kG * kHkv;
   static constexpr int kStages = kStages_;
   static constexpr int kPPS = kPPS_;                 // pages per step
+  static constexpr bool kPInTmem = kPInTmem_;        // P in tensor memory (else shared memory)
   static constexpr int kKeys = kPPS * kPage;         // keys per step: N of S, K of P V
   static constexpr int kSlices = kD / kDS;
   static constexpr int kRows = 128;
@@ -87,17 +88,18 @@ struct Config {
   static constexpr int kThreads = 6 * 32;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = kDS;  // S buffers at columns kDS and kDS + kKeys
+  static constexpr uint32_t kPCol = kSCol + 2 * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
-  static_assert(kSCol + 2 * kKeys <= kTmemCols, "O and two S buffers fit in tensor memory");
+  static_assert(kPCol + (kPInTmem ? kKeys : 0) <= kTmemCols, "O, two S buffers and P fit in tensor memory");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
 
   struct Smem {
     alignas(1024) uint8_t q[kKChunks][kQChunkBytes];
     alignas(1024) uint8_t k[kStages][kKTile];
     alignas(1024) uint8_t v[kStages][kVTile];
-    alignas(128) uint8_t p[2][kPBytes];
+    alignas(128) uint8_t p[kPInTmem ? 1 : 2][kPInTmem ? 16 : kPBytes];
     alignas(8) uint64_t full[kStages];   // K and V of the stage landed (TMA)
     alignas(8) uint64_t empty[kStages];  // both products of the stage's page done (commit)
     alignas(8) uint64_t s_full[2];       // S buffer written (commit)
@@ -266,13 +268,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           const int st = j % kStages;
           if (ok) ok = mbar_wait(&s.p_full[bp], (j >> 1) & 1);
           tc_fence_after_sync();
-          const uint32_t p_base = smem_addr(s.p[bp]);
           const uint32_t v_base = smem_addr(s.v[st]);
 #pragma unroll
           for (int kk = 0; kk < C::kKeys / 16; ++kk) {
-            const uint64_t a_desc = umma_desc(p_base + kk * 256, 128, C::kKeys * 16, 0);
             const uint64_t b_desc = umma_desc(v_base + kk * (16 * 128), C::kChunkRows, 1024, 2);
-            umma_bf16(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (C::kPInTmem) {
+              umma_bf16_ts(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              const uint64_t a_desc = umma_desc(smem_addr(s.p[bp]) + kk * 256, 128, C::kKeys * 16, 0);
+              umma_bf16(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           umma_commit(&s.empty[st]);
           umma_commit(&s.p_empty[bp]);
@@ -384,13 +390,25 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // P row into buffer bs (K-major core matrices of 8 rows x 8 keys) once
         // P V of step j-2 has read it
         if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[bs], ((j - 2) >> 1) & 1));
-        const uint32_t p_row = smem_addr(s.p[bs]) + (r >> 3) * (C::kKeys * 16) + (r & 7) * 16;
+        if constexpr (C::kPInTmem) {
+          // this row of P into its lane: columns kPCol + (kKeys / 2) bs + j hold keys 2j, 2j + 1
 #pragma unroll
-        for (int kc = 0; kc < C::kKeys / 8; ++kc)
-          st_shared_v4(p_row + kc * 128,
-                       make_uint4(pack_bf16x2(sv[8 * kc], sv[8 * kc + 1]), pack_bf16x2(sv[8 * kc + 2], sv[8 * kc + 3]),
-                                  pack_bf16x2(sv[8 * kc + 4], sv[8 * kc + 5]),
-                                  pack_bf16x2(sv[8 * kc + 6], sv[8 * kc + 7])));
+          for (int kc = 0; kc < C::kKeys / 16; ++kc) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
+            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * bs + 8 * kc, w);
+          }
+          tmem_wait_st();
+        } else {
+          const uint32_t p_row = smem_addr(s.p[bs]) + (r >> 3) * (C::kKeys * 16) + (r & 7) * 16;
+#pragma unroll
+          for (int kc = 0; kc < C::kKeys / 8; ++kc)
+            st_shared_v4(p_row + kc * 128,
+                         make_uint4(pack_bf16x2(sv[8 * kc], sv[8 * kc + 1]), pack_bf16x2(sv[8 * kc + 2], sv[8 * kc + 3]),
+                                    pack_bf16x2(sv[8 * kc + 4], sv[8 * kc + 5]),
+                                    pack_bf16x2(sv[8 * kc + 6], sv[8 * kc + 7])));
+        }
         // zero this step's V rows outside [k_lo, k_hi] (the first and last steps)
         if (pos0 < k_lo || pos0 + C::kKeys - 1 > k_hi) {
           const uint32_t v_base = smem_addr(s.v[j % kStages]);
@@ -451,8 +469,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per block, D = 256,
 // 6 stages of 16 KB.  Global: 8 queries x 16 heads per block, D = 512 split
 // into two blocks of 256 output dims (both compute S), 3 stages of 24 KB.
-using SlidingConfig = Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 2, 4>;
-using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 3, 1>;
+using SlidingConfig = Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 5, 2, true>;
+using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true>;
 
 }  // namespace prefill_tc
 }  // namespace pda
