@@ -549,9 +549,9 @@ int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void*
   static bool smem_set[2][kMaxDevices] = {{false}};
   if ((st = ensure_smem(pda::prefill_tc::prefill_tc_kernel<C>, C::kSmemBytes, dev, smem_set[kind]))) return st;
 
-  CUtensorMap tm_k, tm_v;  // boxes of one page's 16 rows x 64 dims
+  CUtensorMap tm_k, tm_v;  // K: one page's 16 rows x 64 dims; V: a page's kDS dims of one KV head
   if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, 1))) return st;
-  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, 1))) return st;
+  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, C::kVChunks))) return st;
 
   pda::prefill_tc::PrefillParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);

@@ -81,9 +81,11 @@ struct Config {
   static constexpr int kKChunks = kD / 64;
   static constexpr int kVChunks = kDS / 64;
   static constexpr int kQChunkBytes = kRows * 128;  // [128 rows][64 dims]
-  static constexpr int kChunkRows = kKeys * 128;     // one chunk of a step: [kKeys rows][64 dims]
+  static constexpr int kChunkRows = kKeys * 128;     // one K chunk of a step: [kKeys rows][64 dims]
+  static constexpr int kChunkBytes = kPage * 128;    // one chunk of one page: [16 rows][64 dims]
+  static constexpr int kVPage = kVChunks * kChunkBytes;  // one page of V: one TMA box
   static constexpr int kKTile = kKChunks * kChunkRows;
-  static constexpr int kVTile = kVChunks * kChunkRows;
+  static constexpr int kVTile = kPPS * kVPage;
   static constexpr int kPBytes = kRows * kKeys * 2;
   static constexpr int kThreads = 6 * 32;
   static constexpr uint32_t kTmemCols = 512;
@@ -244,10 +246,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int ch = 0; ch < C::kKChunks; ++ch)
             tma_load_3d(s.k[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_k, 0, y,
                                  c * C::kKChunks + ch, &s.full[stage]);
-#pragma unroll
-          for (int ch = 0; ch < C::kVChunks; ++ch)
-            tma_load_3d(s.v[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_v, 0, y,
-                                 c * C::kKChunks + slice * C::kVChunks + ch, &s.full[stage]);
+          tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, c * C::kKChunks + slice * C::kVChunks,
+                      &s.full[stage]);
         }
         ++issued;
         __syncwarp();
@@ -263,15 +263,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (lane == 0) {
         bool ok = mbar_wait(&s.q_ready, 0);
         const uint32_t q_base = smem_addr(s.q[0]);
-        auto pv = [&](int j) {  // O += P_j V_j, kKeys / 16 products of K = 16
+        auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
           const int bp = j & 1;
           const int st = j % kStages;
           if (ok) ok = mbar_wait(&s.p_full[bp], (j >> 1) & 1);
           tc_fence_after_sync();
           const uint32_t v_base = smem_addr(s.v[st]);
 #pragma unroll
-          for (int kk = 0; kk < C::kKeys / 16; ++kk) {
-            const uint64_t b_desc = umma_desc(v_base + kk * (16 * 128), C::kChunkRows, 1024, 2);
+          for (int kk = 0; kk < kPPS; ++kk) {
+            const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
             if constexpr (C::kPInTmem) {
               umma_bf16_ts(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
                            (j > 0 || kk > 0) ? 1u : 0u);
@@ -419,7 +419,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (key < k_lo || key > k_hi) {
 #pragma unroll
               for (int ch = 0; ch < C::kVChunks; ++ch)
-                st_shared_v4(v_base + ch * C::kChunkRows + kr * 128 + (it & 7) * 16, make_uint4(0, 0, 0, 0));
+                st_shared_v4(v_base + (kr >> 4) * C::kVPage + ch * C::kChunkBytes + (kr & 15) * 128 + (it & 7) * 16,
+                             make_uint4(0, 0, 0, 0));
             }
           }
         }
