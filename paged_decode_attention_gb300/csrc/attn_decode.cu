@@ -565,6 +565,7 @@ int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void*
   p.max_blocks = max_blocks;
   p.window = window;
   p.total_q = total_q;
+  p.max_q = max_q;
   p.out_f32 = out_dtype == ATTN_OUT_F32;
   const dim3 grid((max_q + C::kQ - 1) / C::kQ, C::kHkv * C::kSlices, batch);
   cudaError_t e = launch_pdl(pda::prefill_tc::prefill_tc_kernel<C>, grid, C::kThreads, C::kSmemBytes,

@@ -50,6 +50,7 @@ struct PrefillParams {
   int32_t max_blocks;
   int32_t window;  // > 0: sliding window; <= 0: none
   int32_t total_q;
+  int32_t max_q;  // queries past max_q of a sequence are not computed (and flagged)
   int32_t out_f32;
 };
 
@@ -183,9 +184,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
     run = false;
   } else {
-    if (tile + 1 == static_cast<int>(gridDim.x) && i0 + kQ < n && threadIdx.x == 0 && slice == 0)
+    if (n > p.max_q && tile == 0 && blockIdx.y == 0 && threadIdx.x == 0)
       report(p.status, ATTN_DEV_BAD_SEQ_LEN);  // more queries than the host's max_q: the rest are not computed
-    if (i0 >= n) {
+    if (i0 >= (n < p.max_q ? n : p.max_q)) {
       run = false;
     } else if (L < n || L > cap) {
       if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   if (run) {
     const int P0 = L - n + i0;                   // position of the block's first query
-    const int nq = n - i0 < kQ ? n - i0 : kQ;    // valid queries in the block
+    const int n_run = n < p.max_q ? n : p.max_q;   // queries computed
+    const int nq = n_run - i0 < kQ ? n_run - i0 : kQ;  // valid queries in the block
     const int k_hi = P0 + nq - 1;                // last visible key (inclusive)
     const int k_lo = p.window > 0 ? (P0 - p.window + 1 > 0 ? P0 - p.window + 1 : 0) : 0;
     const int page0 = k_lo / kPage;
