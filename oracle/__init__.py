@@ -10,6 +10,9 @@ never imports the CUDA library.
 * ``prefill_paged`` -- multi-query (prefill) attention over the paged cache:
   each query row is the decode of its sequence cut at the query's position
   (``oracle.c``).
+* ``decode_paged_shared`` -- the global-layer decode over a cache that stores
+  values only: keys rebuilt as rope(V * w_k), rounded once to bf16
+  (``oracle.c``), then ``decode_paged``.
 * ``qkv_append``   -- the per-head norms, RoPE and paged KV-cache append of
   one new token per sequence (``oracle.c``, double precision).
 * ``dense``        -- the literal Lean definitions over unpaged arrays, for
@@ -82,6 +85,14 @@ def _load(lib_path=None):
             ctypes.c_int32,                                      # window
             ctypes.c_void_p, ctypes.c_int32,                     # rows, n_rows
             ctypes.c_void_p, ctypes.c_int32,                     # out, n_threads
+        ]
+        fr = lib.oracle_rebuild_keys
+        fr.restype = ctypes.c_int
+        fr.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # v_pool w_k block_table seq_lens
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,      # B Hkv D page_size
+            ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,                      # max_blocks num_pages window
+            ctypes.c_double, ctypes.c_int32, ctypes.c_void_p,                    # theta rope_pairs k_out
         ]
         fa = lib.oracle_qkv_append
         fa.restype = ctypes.c_int
@@ -189,6 +200,37 @@ def prefill_paged(q_bits, k_bits, v_bits, block_table, seq_lens, cu_q, window, p
     if st != 0:
         raise OracleError(ERRORS.get(st, "error %d" % st))
     return out
+
+
+def rebuild_keys(v_bits, wk_bits, block_table, seq_lens, window, theta, rope_pairs, k_init=None, page_size=16,
+                 lib_path=None):
+    """Keys of a values-only cache: K = bf16(rope(V * w_k)) at every visible
+    position (fp64, one rounding).  Returns uint16 [num_pages, page_size, Hkv, D]:
+    k_init (default: all NaN) with the visible slots written."""
+    v_bits = _as(v_bits, np.uint16)
+    wk_bits = _as(wk_bits, np.uint16)
+    block_table = _as(block_table, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    num_pages, ps, Hkv, D = v_bits.shape
+    if ps != page_size or wk_bits.shape != (D,) or block_table.shape[0] != seq_lens.shape[0]:
+        raise ValueError("shapes")
+    k = np.full(v_bits.shape, 0x7FC0, dtype=np.uint16) if k_init is None else _as(k_init, np.uint16).copy()
+    st = _load(lib_path).oracle_rebuild_keys(
+        v_bits.ctypes.data, wk_bits.ctypes.data, block_table.ctypes.data, seq_lens.ctypes.data,
+        seq_lens.shape[0], Hkv, D, page_size, block_table.shape[1], num_pages, int(window), float(theta),
+        int(rope_pairs), k.ctypes.data)
+    if st != 0:
+        raise OracleError("oracle_rebuild_keys: %s" % ERRORS.get(st, st))
+    return k
+
+
+def decode_paged_shared(q_bits, v_bits, wk_bits, block_table, seq_lens, window, theta, rope_pairs, page_size=16,
+                        rows=None, threads=1, lib_path=None):
+    """decode_paged over a values-only cache: the keys are rebuild_keys(...)."""
+    k = rebuild_keys(v_bits, wk_bits, block_table, seq_lens, window, theta, rope_pairs, page_size=page_size,
+                     lib_path=lib_path)
+    return decode_paged(q_bits, k, v_bits, block_table, seq_lens, window, page_size=page_size, rows=rows,
+                        threads=threads, lib_path=lib_path)
 
 
 def qkv_append(qkv_bits, wq_bits, wk_bits, block_table, positions, q_out, k_pool, v_pool, *, Hq, Hkv, D,

@@ -410,3 +410,57 @@ int oracle_qkv_append(const uint16_t* qkv, const uint16_t* w_q, const uint16_t* 
   free(y);
   return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/*
+ * The keys of a global-layer cache that stores values only.  With "values =
+ * keys" (Gemma-4-12B model page, "What to watch for": attention_k_eq_v) one
+ * head x gives both, V = rmsnormUnit(x) and K = rope(rmsnorm(x) * w_k), so
+ * K = rope(V * w_k): a cache holding V can rebuild K.  Reading: the rebuilt
+ * key is V * w_k rotated as attn.rope rotates it at the key's position,
+ * computed in double from the stored bf16 V and w_k and rounded once to bf16
+ * (the precision keys have in a cache that stores them).
+ *
+ * v_pool      bf16 bits [num_pages, page_size, Hkv, D]
+ * w_k         bf16 bits [D]
+ * block_table int32 [B, max_blocks]; seq_lens int32 [B]; window as for
+ *             oracle_decode_paged: only the visible positions are rebuilt
+ * k_out       bf16 bits, same shape as v_pool: the slot of every visible
+ *             position is written, every other slot is left as it is
+ */
+int oracle_rebuild_keys(const uint16_t* v_pool, const uint16_t* w_k, const int32_t* block_table,
+                        const int32_t* seq_lens, int32_t B, int32_t Hkv, int32_t D, int32_t page_size,
+                        int32_t max_blocks, int64_t num_pages, int32_t window, double theta, int32_t rope_pairs,
+                        uint16_t* k_out) {
+  if (!v_pool || !w_k || !block_table || !seq_lens || !k_out) return ORACLE_ERR_ARG;
+  if (B < 1 || Hkv < 1 || D < 2 || (D & 1) || page_size < 1 || max_blocks < 1 || num_pages < 1)
+    return ORACLE_ERR_ARG;
+  if (rope_pairs < 0 || rope_pairs > D / 2) return ORACLE_ERR_ARG;
+  double* y = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!y) return ORACLE_ERR_NOMEM;
+  int status = ORACLE_OK;
+  for (int b = 0; b < B && status == ORACLE_OK; ++b) {
+    const int L = seq_lens[b];
+    if (L < 0 || (int64_t)L > (int64_t)max_blocks * page_size) {
+      status = ORACLE_ERR_SEQ_LEN;
+      break;
+    }
+    const int lo = (window > 0 && L > window) ? L - window : 0;
+    for (int l = lo; l < L; ++l) {
+      const int64_t phys = block_table[(int64_t)b * max_blocks + l / page_size];
+      if (phys < 0 || phys >= num_pages) {
+        status = ORACLE_ERR_UNMAPPED;
+        break;
+      }
+      const int64_t slot = phys * page_size + l % page_size;
+      for (int c = 0; c < Hkv; ++c) {
+        const uint16_t* v = v_pool + (slot * Hkv + c) * D;
+        for (int i = 0; i < D; ++i) y[i] = bf16_bits_to_double(v[i]) * bf16_bits_to_double(w_k[i]);
+        rope(y, D, rope_pairs, theta, l);
+        for (int i = 0; i < D; ++i) k_out[(slot * Hkv + c) * D + i] = double_to_bf16_rne(y[i]);
+      }
+    }
+  }
+  free(y);
+  return status;
+}
