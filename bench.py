@@ -100,6 +100,13 @@ def algorithmic_bytes(kind, seq_lens, window, Hq=16, out_bytes=2):
     return vis * Hkv * D * 2 * 2 + B * Hq * D * 2 + B * Hq * D * out_bytes
 
 
+def shared_bytes(seq_lens, window, Hq=16, D=512, out_bytes=2):
+    """Values-only global cache: visible V rows + q + o + w_k of one call."""
+    vis = sum(min(L, window) if window > 0 else L for L in seq_lens)
+    B = len(seq_lens)
+    return vis * D * 2 + B * Hq * D * 2 + B * Hq * D * out_bytes + D * 2
+
+
 def rotation_count(bytes_per_set, floor=1, cap=16):
     """Distinct input sets so that consecutive reuse of a set is separated by > 3x L2."""
     if bytes_per_set <= 0:
@@ -478,14 +485,77 @@ def run_ours(args, rank, world, local_rank):
     append = time_append(calls0, stream, status, dev)
     # --- multi-query attention over the paged cache (prefill) ---
     prefill = None if args.no_prefill else time_prefill(stream, dev)
+    # --- the global calls again over a values-only cache ---
+    shared = time_global_shared(plans, n_sets, stream, status, dev)
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the cache append" % int(status.item()))
 
-    res.update(per_type=per_type, append=append, prefill=prefill)
+    res.update(per_type=per_type, append=append, prefill=prefill, shared=shared)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
                heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
                launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
     return res
+
+
+def time_global_shared(plans, n_sets, stream, status, dev, rounds=5):
+    """The step's global calls with a values-only cache (attn_decode_global_shared:
+    each call's v_pool as the cache, keys rebuilt in the kernel) and, timed the
+    same way, with the separate key and value pools.  Each timing is a CUDA
+    graph of the calls over every rotating input set, replayed `rounds` times."""
+    import torch
+    import paged_decode_attention_gb300 as pda
+    from workloads import key_weight
+    idx = [j for j, c in enumerate(plans[0]) if c[0].kind == "global"]
+    if not idx:
+        return None
+    w_k = key_weight(512, 5, device=dev)
+    reps = max(2, n_sets)
+
+    def launch(shared):
+        for i in range(reps):
+            for j in idx:
+                c, ws, o = plans[i % n_sets][j]
+                if shared:
+                    pda.attn_decode_global_shared(c.q, c.v_pool, w_k, c.block_table, c.seq_lens, o,
+                                                  max_seq_len=c.max_seq_len, workspace=ws, status=status,
+                                                  stream=stream, num_splits=NUM_SPLITS)
+                else:
+                    pda.attn_decode_global(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o,
+                                           max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
+                                           num_splits=NUM_SPLITS)
+    ms = {}
+    for shared in (True, False):
+        with torch.cuda.stream(stream):
+            launch(shared)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch(shared)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(rounds):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        ms[shared] = e0.elapsed_time(e1) / (rounds * reps)
+        del g
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the values-only decode" % int(status.item()))
+    calls = [plans[0][j][0] for j in idx]
+    nbytes = sum(shared_bytes(c.seq_lens_host, c.window) for c in calls)
+    sep_bytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c in calls)
+    return {"calls_per_step": len(idx), "us_per_step": round(ms[True] * 1e3, 3),
+            "bytes_per_step": nbytes, "value": round(nbytes / (ms[True] * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "separate_cache_us_per_step": round(ms[False] * 1e3, 3),
+            "separate_cache_value": round(sep_bytes / (ms[False] * 1e-3) / 1e9, 2),
+            "cache_bytes_per_position": {"values_only": 1024, "separate": 2048},
+            "launch": "%d steps of the global calls (input sets rotating) in one CUDA graph, %d replays"
+                      % (reps, rounds)}
 
 
 def append_bytes(kind, B):
@@ -854,6 +924,8 @@ def main(argv=None):
                            for k, v in r0["prefill"].items()}
     if r0.get("append"):
         line["append"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4)) for k, v in r0["append"].items()}
+    if r0.get("shared"):
+        line["global_values_only_cache"] = dict(r0["shared"], frac_of_peak=round(r0["shared"]["value"] / peak, 4))
     line["e2e"] = r0["e2e"]
     line["clocks"] = r0["clocks"]
     if not args.no_cpu_baseline:

@@ -160,6 +160,37 @@ int32_t attn_decode_global(const void* q, const void* k_pool, const void* v_pool
                            int32_t* status, void* stream);
 
 /*
+ * attn_decode_global_shared -- decodeGQA over a values-only global cache.
+ *
+ * On global layers keys and values come from one head x (Gemma-4-12B model
+ * page, "What to watch for": values = keys; "Compute-graph nodes":
+ * attn.qk_norm, attn.v_norm, attn.rope): V = rmsnormUnit(x) and
+ * K = rope(rmsnorm(x) * w_k), so K = rope(V * w_k) and the cache need hold
+ * V only.  This call reads V pages only (half the bytes of
+ * attn_decode_global) and rebuilds each visible key as
+ *
+ *   k[l] = bf16( rope(v[l] * w_k, l) )     (rounded once, nearest even)
+ *
+ * with RoPE over pairs (i, i + 256), i < ATTN_GLOBAL_ROPE_PAIRS, angle
+ * l * ATTN_GLOBAL_ROPE_THETA^(-2i/512), l the key's own position; then it
+ * computes exactly what attn_decode_global computes with that k_pool.
+ *
+ * kv_pool   bf16 [num_pages, 16, 1, 512]: V, as attn_kv_append_global
+ *           writes it with k_pool = NULL
+ * w_k       bf16 [512]: the qk_norm weight of the keys (device pointer)
+ * Every other argument, the plan and the workspace are attn_decode_global's.
+ * The product v * w_k is exact in fp32; the rotation is fp32 with angles
+ * accurate to about 1e-7 rad, so a rebuilt key may differ from the fp64
+ * definition by one bf16 rounding step.
+ */
+int32_t attn_decode_global_shared(const void* q, const void* kv_pool, const void* w_k,
+                                  const int32_t* block_table, const int32_t* seq_lens, void* o,
+                                  int32_t batch, int32_t max_blocks, int64_t num_pages,
+                                  int32_t max_seq_len, int32_t window, int32_t out_dtype,
+                                  int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* status, void* stream);
+
+/*
  * attn_decode_plan -- the launch plan, as pure host arithmetic (no CUDA call).
  *
  * kind         ATTN_KIND_SLIDING or ATTN_KIND_GLOBAL
@@ -240,6 +271,9 @@ int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool, const voi
  * block_table  int32 [batch, max_blocks]; positions int32 [batch].
  * q_out        bf16 [batch, 16, D] (written): the decode's q.
  * k_pool, v_pool  the decode's pools (one row per sequence written).
+ *              attn_kv_append_global only: k_pool may be NULL for a
+ *              values-only cache (attn_decode_global_shared), and then
+ *              only the value row is written.
  * status       optional device int32: a position outside [0, max_blocks*16)
  *              raises ATTN_DEV_BAD_SEQ_LEN, a page id outside [0, num_pages)
  *              ATTN_DEV_BAD_PAGE; that token's cache row is then not written

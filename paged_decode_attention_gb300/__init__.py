@@ -19,8 +19,9 @@ import torch
 from . import _build
 
 __all__ = [
-    "attn_decode_sliding", "attn_decode_global", "attn_decode_plan", "attn_decode_workspace_size",
-    "PreparedDecode", "prepare_decode_sliding", "prepare_decode_global",
+    "attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared", "attn_decode_plan",
+    "attn_decode_workspace_size",
+    "PreparedDecode", "prepare_decode_sliding", "prepare_decode_global", "prepare_decode_global_shared",
     "attn_last_error", "load", "library_path", "AttnDecodeError",
     "KIND_SLIDING", "KIND_GLOBAL", "DEV_WAIT_TIMEOUT", "DEV_BAD_PAGE", "DEV_BAD_SEQ_LEN",
 ]
@@ -34,7 +35,7 @@ DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN, DEV_INTERNAL = 1, 2, 4, 8
 PAGE_SIZE = 16
 SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
 
-EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_plan",
+EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared", "attn_decode_plan",
            "attn_decode_workspace_size", "attn_kv_append_sliding", "attn_kv_append_global",
            "attn_prefill_sliding", "attn_prefill_global",
            "attn_last_error", "attn_abi_version")
@@ -72,6 +73,8 @@ def load(path=None):
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = call
+    lib.attn_decode_global_shared.restype = c_i32
+    lib.attn_decode_global_shared.argtypes = call[:2] + [c_vp] + call[3:]  # q kv_pool w_k block_table ...
     lib.attn_decode_plan.restype = c_i32
     lib.attn_decode_plan.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                                      ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]
@@ -142,7 +145,7 @@ def _ptr(t, name, dtype, shape=None):
 
 
 def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len, out_dtype,
-          num_splits, workspace, status, stream):
+          num_splits, workspace, status, stream, w_k=None):
     Hq, Hkv, D = SHAPES[kind]
     if q.dim() != 3:
         raise ValueError("q must be [batch, %d, %d]" % (Hq, D))
@@ -156,6 +159,8 @@ def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len
     args_q = _ptr(q, "q", torch.bfloat16, (batch, Hq, D))
     args_k = _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))
     args_v = _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))
+    if w_k is not None:
+        args_v = _ptr(w_k, "w_k", torch.bfloat16, (D,))
     args_bt = _ptr(block_table, "block_table", torch.int32, (batch, max_blocks))
     args_sl = _ptr(seq_lens, "seq_lens", torch.int32, (batch,))
     if out_dtype not in (torch.bfloat16, torch.float32):
@@ -175,7 +180,8 @@ def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    fn = lib.attn_decode_sliding if kind == KIND_SLIDING else lib.attn_decode_global
+    fn = (lib.attn_decode_sliding if kind == KIND_SLIDING else
+          lib.attn_decode_global if w_k is None else lib.attn_decode_global_shared)
     with torch.cuda.device(q.device):
         st = fn(args_q, args_k, args_v, args_bt, args_sl, args_o, batch, max_blocks, num_pages,
                 int(max_seq_len), int(window), OUT_F32 if o.dtype == torch.float32 else OUT_BF16,
@@ -196,12 +202,13 @@ class PreparedDecode:
     """
 
     def __init__(self, kind, q, k_pool, v_pool, block_table, seq_lens, o=None, *, window, max_seq_len=None,
-                 out_dtype=torch.bfloat16, num_splits=0, workspace=None, status=None):
+                 out_dtype=torch.bfloat16, num_splits=0, workspace=None, status=None, w_k=None):
         Hq, Hkv, D = SHAPES[kind]
         batch, num_pages, max_blocks = q.shape[0], k_pool.shape[0], block_table.shape[1]
         ptrs = [_ptr(q, "q", torch.bfloat16, (batch, Hq, D)),
                 _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
-                _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
+                _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))
+                if w_k is None else _ptr(w_k, "w_k", torch.bfloat16, (D,)),
                 _ptr(block_table, "block_table", torch.int32, (batch, max_blocks)),
                 _ptr(seq_lens, "seq_lens", torch.int32, (batch,))]
         if o is None:
@@ -216,9 +223,10 @@ class PreparedDecode:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         ws_ptr = _ptr(workspace, "workspace", torch.uint8)
         st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
-        self._keep = (q, k_pool, v_pool, block_table, seq_lens, o, workspace, status)
+        self._keep = (q, k_pool, v_pool, block_table, seq_lens, o, workspace, status, w_k)
         self.o = o
-        self._fn = lib.attn_decode_sliding if kind == KIND_SLIDING else lib.attn_decode_global
+        self._fn = (lib.attn_decode_sliding if kind == KIND_SLIDING else
+                    lib.attn_decode_global if w_k is None else lib.attn_decode_global_shared)
         self._args = tuple(ptrs) + (batch, max_blocks, num_pages, int(max_seq_len), int(window),
                                     OUT_F32 if o.dtype == torch.float32 else OUT_BF16, int(num_splits),
                                     ws_ptr, workspace.numel(), st_ptr)
@@ -240,6 +248,11 @@ def prepare_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, 
 def prepare_decode_global(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=0, **kw):
     """PreparedDecode for attn_decode_global (same arguments, minus the stream)."""
     return PreparedDecode(KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, o, window=window, **kw)
+
+
+def prepare_decode_global_shared(q, kv_pool, w_k, block_table, seq_lens, o=None, *, window=0, **kw):
+    """PreparedDecode for attn_decode_global_shared (same arguments, minus the stream)."""
+    return PreparedDecode(KIND_GLOBAL, q, kv_pool, kv_pool, block_table, seq_lens, o, window=window, w_k=w_k, **kw)
 
 
 def attn_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=1024,
@@ -264,9 +277,19 @@ def attn_decode_global(q, k_pool, v_pool, block_table, seq_lens, o=None, *, wind
                  out_dtype, num_splits, workspace, status, stream)
 
 
+def attn_decode_global_shared(q, kv_pool, w_k, block_table, seq_lens, o=None, *, window=0,
+                              max_seq_len=None, out_dtype=torch.bfloat16, num_splits=0, workspace=None,
+                              status=None, stream=None):
+    """decodeGQA over a values-only cache: kv_pool [P,16,1,512] holds V; keys are
+    rebuilt in the kernel as bf16(rope(V * w_k)), w_k [512] bf16.  Otherwise as
+    attn_decode_global."""
+    return _call(KIND_GLOBAL, q, kv_pool, kv_pool, block_table, seq_lens, o, window, max_seq_len,
+                 out_dtype, num_splits, workspace, status, stream, w_k=w_k)
+
+
 def _append(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream):
     Hq, Hkv, D = SHAPES[kind]
-    batch, max_blocks, num_pages = qkv.shape[0], block_table.shape[1], k_pool.shape[0]
+    batch, max_blocks, num_pages = qkv.shape[0], block_table.shape[1], v_pool.shape[0]
     args = [_ptr(qkv, "qkv", torch.bfloat16, (batch, APPEND_ROW[kind])),
             _ptr(w_q, "w_q", torch.bfloat16, (D,)),
             _ptr(w_k, "w_k", torch.bfloat16, (D,)),
@@ -275,6 +298,7 @@ def _append(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, 
     if q_out is None:
         q_out = torch.empty((batch, Hq, D), dtype=torch.bfloat16, device=qkv.device)
     args += [_ptr(q_out, "q_out", torch.bfloat16, (batch, Hq, D)),
+             None if k_pool is None and kind == KIND_GLOBAL else
              _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
              _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))]
     st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
@@ -306,6 +330,7 @@ def attn_kv_append_global(qkv, w_q, w_k, block_table, positions, k_pool, v_pool,
 
     qkv [B, 8704] bf16 = [q 16x512 | x 512], x giving both key and value
     (values = keys); w_q, w_k [512] bf16.  Returns q_out [B,16,512].
+    k_pool None: a values-only cache (attn_decode_global_shared); only V is written.
     """
     return _append(KIND_GLOBAL, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream)
 

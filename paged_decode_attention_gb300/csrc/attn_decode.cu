@@ -224,6 +224,32 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, int threads, size_t smem, cudaS
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// 2*pi as three floats for the additive range reduction (Cody and Waite):
+// the first two keep 8 significant bits, so n * part is exact for n < 2^16
+// turns; the third is the float nearest to what remains.
+pda::TwoPi split_two_pi() {
+  const double two_pi = 6.283185307179586476925286766559;
+  pda::TwoPi out;
+  double rest = two_pi;
+  for (int k = 0; k < 2; ++k) {
+    int e;
+    const double m = std::frexp(rest, &e);  // rest = m * 2^e, 0.5 <= m < 1
+    const double part = std::ldexp(std::trunc(std::ldexp(m, 8)), e - 8);
+    out.part[k] = static_cast<float>(part);
+    rest -= part;
+  }
+  out.part[2] = static_cast<float>(rest);
+  out.inv = static_cast<float>(1.0 / two_pi);
+  return out;
+}
+
+pda::FloatPair split_float_pair(double f) {
+  pda::FloatPair fp;
+  fp.hi = static_cast<float>(f);
+  fp.lo = static_cast<float>(f - static_cast<double>(fp.hi));
+  return fp;
+}
+
 // ---------------------------------------------------------------------------
 // Common validation + launch
 // ---------------------------------------------------------------------------
@@ -231,14 +257,15 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
                    const int32_t* block_table, const int32_t* seq_lens, void* o, int32_t batch,
                    int32_t max_blocks, int64_t num_pages, int32_t max_seq_len, int32_t window,
                    int32_t out_dtype, int32_t num_splits, void* workspace, size_t workspace_bytes,
-                   int32_t* status, void* stream) {
+                   int32_t* status, void* stream, const void* w_k = nullptr) {
   g_err[0] = '\0';
   const bool sliding = kind == ATTN_KIND_SLIDING;
-  const char* name = sliding ? "attn_decode_sliding" : "attn_decode_global";
+  const bool shared = w_k != nullptr;  // values-only global cache (k_pool is v_pool)
+  const char* name = sliding ? "attn_decode_sliding" : shared ? "attn_decode_global_shared" : "attn_decode_global";
   if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !o)
     return fail(ATTN_ERR_INVALID_ARG, "%s: null array pointer", name);
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(block_table) ||
-      !aligned16(seq_lens) || !aligned16(o))
+      !aligned16(seq_lens) || !aligned16(o) || (shared && !aligned16(w_k)))
     return fail(ATTN_ERR_INVALID_ARG, "%s: every array must be 16-byte aligned", name);
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "%s: status must be 4-byte aligned", name);
@@ -311,6 +338,24 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
       e = launch_pdl(pda::combine_kernel<ATTN_SLIDING_D>,
                      dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, 0,
                      s, p);
+  } else if (shared) {
+    if ((st = encode_global_page_map(&tm_v, v_pool, num_pages))) return st;
+    pda::global::KeyRebuild kr;
+    kr.w_k = static_cast<const __nv_bfloat16*>(w_k);
+    kr.two_pi = split_two_pi();
+    for (int j = 0; j < pda::global::kRopePairs; ++j)
+      kr.freq[j] = split_float_pair(std::pow(ATTN_GLOBAL_ROPE_THETA, -2.0 * j / ATTN_GLOBAL_D));
+    static bool smem_set[kMaxDevices] = {false};
+    if ((st = ensure_smem(pda::global::decode_kernel_shared, pda::global::kSharedSmemBytes, dev, smem_set)))
+      return st;
+    static bool comb_set[kMaxDevices] = {false};
+    if ((st = ensure_smem(pda::combine_kernel<ATTN_GLOBAL_D>, 0, dev, comb_set))) return st;
+    e = launch_pdl(pda::global::decode_kernel_shared, dim3(plan.grid_x), pda::global::kThreads,
+                   pda::global::kSharedSmemBytes, s, tm_v, p, kr);
+    if (e == cudaSuccess)
+      e = launch_pdl(pda::combine_kernel<ATTN_GLOBAL_D>,
+                     dim3(ATTN_GLOBAL_HQ * (ATTN_GLOBAL_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, 0,
+                     s, p);
   } else {
     if ((st = encode_global_page_map(&tm_k, k_pool, num_pages))) return st;
     if ((st = encode_global_page_map(&tm_v, v_pool, num_pages))) return st;
@@ -356,6 +401,19 @@ int32_t attn_decode_global(const void* q, const void* k_pool, const void* v_pool
                     status, stream);
 }
 
+int32_t attn_decode_global_shared(const void* q, const void* kv_pool, const void* w_k,
+                                  const int32_t* block_table, const int32_t* seq_lens, void* o, int32_t batch,
+                                  int32_t max_blocks, int64_t num_pages, int32_t max_seq_len, int32_t window,
+                                  int32_t out_dtype, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* status, void* stream) {
+  if (!w_k) {
+    g_err[0] = '\0';
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_global_shared: null w_k");
+  }
+  return run_decode(ATTN_KIND_GLOBAL, q, kv_pool, kv_pool, block_table, seq_lens, o, batch, max_blocks, num_pages,
+                    max_seq_len, window, out_dtype, num_splits, workspace, workspace_bytes, status, stream, w_k);
+}
+
 int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
                          int32_t num_splits, int32_t num_sms, int32_t* out_num_splits,
                          size_t* out_workspace_bytes) {
@@ -389,29 +447,13 @@ int32_t attn_abi_version(void) { return ATTN_DECODE_ABI_VERSION; }
 // ---------------------------------------------------------------------------
 namespace {
 
-// 2*pi as three floats for the additive range reduction (Cody and Waite):
-// the first two keep 8 significant bits, so n * part is exact for n < 2^16
-// turns; the third is the float nearest to what remains.
-void split_two_pi(float out[3]) {
-  const double two_pi = 6.283185307179586476925286766559;
-  double rest = two_pi;
-  for (int k = 0; k < 2; ++k) {
-    int e;
-    const double m = std::frexp(rest, &e);  // rest = m * 2^e, 0.5 <= m < 1
-    const double part = std::ldexp(std::trunc(std::ldexp(m, 8)), e - 8);
-    out[k] = static_cast<float>(part);
-    rest -= part;
-  }
-  out[2] = static_cast<float>(rest);
-}
-
 int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w_k, const int32_t* block_table,
                    const int32_t* positions, void* q_out, void* k_pool, void* v_pool, int32_t batch,
                    int32_t max_blocks, int64_t num_pages, int32_t* status, void* stream) {
   g_err[0] = '\0';
   const bool sliding = kind == ATTN_KIND_SLIDING;
   const char* name = sliding ? "attn_kv_append_sliding" : "attn_kv_append_global";
-  if (!qkv || !w_q || !w_k || !block_table || !positions || !q_out || !k_pool || !v_pool)
+  if (!qkv || !w_q || !w_k || !block_table || !positions || !q_out || (sliding && !k_pool) || !v_pool)
     return fail(ATTN_ERR_INVALID_ARG, "%s: null pointer argument", name);
   auto aligned = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; };
   if (!aligned(qkv, 16) || !aligned(w_q, 16) || !aligned(w_k, 16) || !aligned(q_out, 16) || !aligned(k_pool, 16) ||
@@ -440,16 +482,10 @@ int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w
   p.batch = batch;
   p.max_blocks = max_blocks;
   p.eps = 1e-6f;
-  split_two_pi(p.two_pi);
-  p.inv_two_pi = static_cast<float>(1.0 / 6.283185307179586476925286766559);
+  p.two_pi = split_two_pi();
   // frequencies theta^(-2i/D), i = V*lane + j, as products of these factors
   const int V = D / 64;
-  auto split = [](double f) {
-    pda::append::FloatPair fp;
-    fp.hi = static_cast<float>(f);
-    fp.lo = static_cast<float>(f - static_cast<double>(fp.hi));
-    return fp;
-  };
+  auto split = split_float_pair;
   for (int k = 0; k < pda::append::kLaneBits; ++k) p.lane_factor[k] = split(std::pow(theta, -2.0 * V * (1 << k) / D));
   for (int j = 0; j < V; ++j) p.dim_factor[j] = split(std::pow(theta, -2.0 * j / D));
   static_assert(ATTN_SLIDING_D / 64 <= pda::append::kMaxV && ATTN_GLOBAL_D / 64 <= pda::append::kMaxV, "dims per lane");

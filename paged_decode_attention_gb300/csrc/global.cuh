@@ -22,9 +22,25 @@
 // Masking selects: logits of rows outside [lo, L) become -inf, and V rows
 // outside [lo, L) of a partial page are overwritten with zeros in shared
 // memory before the P*V product (0 * NaN would be NaN).
+//
+// Values-only cache (decode_kernel_shared).  On global layers keys and values
+// come from one head x (Gemma-4-12B model page, "What to watch for": values =
+// keys): V = rmsnormUnit(x) and K = rope(rmsnorm(x) * w_k) = rope(V * w_k),
+// so the cache may hold V alone and the kernel rebuilds each key, rounded
+// once to bf16, from the V page it already has in shared memory.  Only V is
+// copied (half the bytes per page).  The rebuilt K never goes to memory: the
+// S k-steps are dealt out so that each warp rebuilds exactly the B fragments
+// it multiplies.  Warp w takes dims [16w, 16w + 16) of every 64-dim chunk:
+// in the rotated chunk 0 and its partner chunk 4 (pairs (j, j + 256)) a lane
+// holds both halves of each of its 8 pairs; in chunks 1-3 and 5-7 the key is
+// the bf16 product V * w_k.
+// The 8 angles per lane and page come from rope.cuh.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
+#include "rope.cuh"
 
 namespace pda {
 namespace global {
@@ -39,49 +55,96 @@ constexpr int kChunks = kD / kChunk;                // 8
 constexpr int kChunkBytes = kPage * kChunk * 2;     // 2 KB
 constexpr int kPageBytes = kPage * kD * 2;          // 16 KB
 constexpr int kStages = 3;
+constexpr int kSharedStages = 6;  // values-only pages are half the size
 constexpr int kBlocksPerSm = 2;
+constexpr int kRopePairs = ATTN_GLOBAL_ROPE_PAIRS;  // 64: dims [0, 64) turn with [256, 320)
 constexpr int kMinPages = 4;
 constexpr int kWarmPages = 2;  // pages per block pulled into L2 before the wait (32 KB each)
 constexpr int kAhead = 2;  // ldmatrix fragments read ahead of their MMAs
 
 static_assert(kHq == 16, "the m16n8k16 tiling uses the 16 query heads as the M dimension");
+static_assert(kRopePairs == kChunk, "the rotated dims are exactly the first chunk and its partner chunk");
 
-struct Smem {
-  alignas(1024) uint8_t k[kStages][kPageBytes];  // kChunks tiles of [16 rows][64 dims], swizzled
-  alignas(1024) uint8_t v[kStages][kPageBytes];
-  alignas(16) float4 xs[2][kConsumerWarps][2][32];  // partial-S exchange, double-buffered
-  SeqTable table;
-  alignas(8) uint64_t full[kStages];
-  alignas(8) uint64_t empty[kStages];
+// Key rebuild of a values-only cache: w_k and the RoPE frequencies of the
+// 64 active pairs, theta^(-2j/D) as float pairs.
+struct KeyRebuild {
+  const __nv_bfloat16* w_k;  // [512]
+  TwoPi two_pi;
+  FloatPair freq[kRopePairs];
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
+struct KPages {
+  alignas(1024) uint8_t k[kStages][kPageBytes];  // kChunks tiles of [16 rows][64 dims], swizzled
+};
+struct KeyWeights {
+  uint32_t wk[kD / 2];  // w_k as bf16x2 words
+};
+
+template <bool kShared>
+struct Smem : std::conditional_t<kShared, KeyWeights, KPages> {
+  static constexpr int kNumStages = kShared ? kSharedStages : kStages;
+  alignas(1024) uint8_t v[kNumStages][kPageBytes];
+  alignas(16) float4 xs[2][kConsumerWarps][2][32];  // partial-S exchange, double-buffered
+  SeqTable table;
+  alignas(8) uint64_t full[kNumStages];
+  alignas(8) uint64_t empty[kNumStages];
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem<false>) + 1024;  // + alignment slack
+constexpr size_t kSharedSmemBytes = sizeof(Smem<true>) + 1024;
+// kBlocksPerSm blocks, each with 1 KB reserved by the system, in 228 KB
+static_assert(kBlocksPerSm * (kSmemBytes + 1024) <= 228 * 1024 &&
+                  kBlocksPerSm * (kSharedSmemBytes + 1024) <= 228 * 1024,
+              "shared memory of the resident blocks");
 
 // byte offset of 16-byte unit `unit` of row `row` in a 128B-swizzled [16][64] tile
 __device__ __forceinline__ uint32_t swz(int row, int unit) {
   return row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ DecodeParams p) {
+// bf16x2 product rounded to nearest even (the exact product of two bf16 fits
+// in fp32, so this is the product rounded once).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// First of the 16 dims of S k-step ks of consumer warp w.  Values-only
+// cache: dims [16w, 16w + 16) of every chunk, the rotated chunk 0 and its
+// partner chunk 4 first.
+template <bool kShared>
+__device__ __forceinline__ int s_kstep_dim(int w, int ks) {
+  if constexpr (kShared) {
+    constexpr int kChunkOrder = 0x76532140;  // chunks 0, 4, 1, 2, 3, 5, 6, 7 as nibbles
+    return ((kChunkOrder >> (4 * ks)) & 0xF) * kChunk + 16 * w;
+  } else {
+    return w * kDimsPerWarp + 16 * ks;
+  }
+}
+
+template <bool kShared>
+__device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v, const DecodeParams& p,
+                                            const KeyRebuild* kr) {
   extern __shared__ uint8_t smem_raw[];
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using S = Smem<kShared>;
+  constexpr int kNS = S::kNumStages;
+  S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int gb = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = 0; st < kNS; ++st) {
       mbar_init(&s.full[st], 1);
       mbar_init(&s.empty[st], kConsumerWarps);
     }
     fence_mbar_init();
   }
   if (warp == kConsumerWarps && lane == 0) {
-    prefetch_tensor_map(&tm_k);
-    prefetch_tensor_map(&tm_v);
+    if constexpr (!kShared) prefetch_tensor_map(tm_k);
+    prefetch_tensor_map(tm_v);
   }
   // With a programmatic launch this prologue overlaps the previous kernel in
   // the stream, whose writes (q, the cache, the tables, the workspace it
@@ -92,7 +155,7 @@ __global__ void __launch_bounds__(kThreads)
   if (warp == kConsumerWarps) {
     warm_first_pages(p, s.table, kWarmPages, [&](int32_t y) {
       // a page is 16 contiguous rows of D elements in each pool
-      bulk_prefetch_l2(p.k_pool + static_cast<size_t>(y) * kD, kPageBytes);
+      if constexpr (!kShared) bulk_prefetch_l2(p.k_pool + static_cast<size_t>(y) * kD, kPageBytes);
       bulk_prefetch_l2(p.v_pool + static_cast<size_t>(y) * kD, kPageBytes);
     });
   } else {
@@ -100,6 +163,12 @@ __global__ void __launch_bounds__(kThreads)
   }
   wait_for_primary_grid();
   allow_dependent_launch();
+  if constexpr (kShared) {
+    if (warp < kConsumerWarps) {  // w_k to shared memory; published by confirm_seq_table's barrier
+      const uint32_t* w32 = reinterpret_cast<const uint32_t*>(kr->w_k);
+      for (int k = threadIdx.x; k < kD / 2; k += kConsumerWarps * 32) s.wk[k] = __ldg(w32 + k);
+    }
+  }
   // The producer reads its first block-table entries while warp 0 confirms
   // the table; it reads them again if the table had to be rebuilt.
   int first = warp == kConsumerWarps ? page_entry(p, s.table, s.table.span, lane, false) : 0;
@@ -113,11 +182,17 @@ __global__ void __launch_bounds__(kThreads)
     // ---------------- producer ----------------
     const uint64_t policy = l2_policy_evict_first();
     if (t.rebuilt) first = page_entry(p, t, sp, lane, true);
-    produce_pages<kStages, 2 * kPageBytes>(p, t, sp, s.full, s.empty, first, [&](int stage, int32_t y) {
-      // one copy per pool: the page's 16 rows as kChunks tiles of [16][64]
-      tma_load_3d_hint(s.k[stage], &tm_k, 0, y, 0, &s.full[stage], policy);
-      tma_load_3d_hint(s.v[stage], &tm_v, 0, y, 0, &s.full[stage], policy);
-    });
+    if constexpr (kShared) {
+      produce_pages<kNS, kPageBytes>(p, t, sp, s.full, s.empty, first, [&](int stage, int32_t y) {
+        tma_load_3d_hint(s.v[stage], tm_v, 0, y, 0, &s.full[stage], policy);
+      });
+    } else {
+      produce_pages<kNS, 2 * kPageBytes>(p, t, sp, s.full, s.empty, first, [&](int stage, int32_t y) {
+        // one copy per pool: the page's 16 rows as kChunks tiles of [16][64]
+        tma_load_3d_hint(s.k[stage], tm_k, 0, y, 0, &s.full[stage], policy);
+        tma_load_3d_hint(s.v[stage], tm_v, 0, y, 0, &s.full[stage], policy);
+      });
+    }
     return;
   }
 
@@ -131,14 +206,14 @@ __global__ void __launch_bounds__(kThreads)
   PageCursor cur;
   cur.start(p, t, sp);
 
-  // q as m16n8k16 A fragments over this warp's 128 dims (8 k-steps of 16)
+  // q as m16n8k16 A fragments over this warp's 128 S dims (8 k-steps of 16)
   uint32_t qa[8][4];
   auto load_q = [&]() {
     const uint32_t* q_g = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(cur.b) * kHq + g) * kD);
     const uint32_t* q_g8 = q_g + 8 * kD / 2;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int d = dim0 + ks * 16 + 2 * tq;
+      const int d = s_kstep_dim<kShared>(warp, ks) + 2 * tq;
       qa[ks][0] = __ldg(q_g + d / 2);
       qa[ks][1] = __ldg(q_g8 + d / 2);
       qa[ks][2] = __ldg(q_g + (d + 8) / 2);
@@ -169,6 +244,25 @@ __global__ void __launch_bounds__(kThreads)
   reset();
   bool ok = true;
 
+  // Values-only cache: this lane's share of the key rebuild.  wk(ks, h): w_k
+  // at dims (d + 2 tq, +1) for h = 0 and (d + 8 + 2 tq, +1) for h = 1, d the
+  // k-step's first dim; freq[e]: pair j = 16 w + 2 tq + (e & 1) + 8 (e >> 1).
+  auto wk = [&](int ks, int h) -> uint32_t {
+    if constexpr (kShared) return s.wk[(s_kstep_dim<kShared>(warp, ks) + 8 * h + 2 * tq) / 2];
+    return 0u;
+  };
+  FloatPair freq[4];
+  if constexpr (kShared) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) freq[e] = kr->freq[16 * warp + 2 * tq + (e & 1) + 8 * (e >> 1)];
+  }
+  // byte offset of this lane's ldmatrix row in the tile of S k-step ks
+  auto kstep_offset = [&](int ks) -> uint32_t {
+    const int d = s_kstep_dim<kShared>(warp, ks);
+    const int row = ((mi >> 1) << 3) + lr;
+    return (d / kChunk) * kChunkBytes + swz(row, 2 * ((d % kChunk) / 16) + (mi & 1));
+  };
+
   for (int i = 0; i < n_pages; ++i) {
     const int f = sp.begin + i;
     if (f >= t.prefix[cur.b + 1]) {
@@ -176,26 +270,68 @@ __global__ void __launch_bounds__(kThreads)
       load_q();
       prefetch_next_q();
     }
-    const int stage = i % kStages;
+    const int stage = i % kNS;
+    const int pos0 = cur.pos0(t, f);
     if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kStages) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kNS) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     }
-    const int pos0 = cur.pos0(t, f);
-    const uint32_t kst = smem_addr(s.k[stage]);
     const uint32_t vst = smem_addr(s.v[stage]);
+    uint32_t kst = vst;
+    if constexpr (!kShared) kst = smem_addr(s.k[stage]);
 
     // ---- partial S over this warp's dims: two n-tiles of 8 positions; even
     //      and odd k-steps accumulate separately (two chains of 4 MMAs) ----
     //      The K fragments are read kAhead k-steps before their MMAs.
     float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
+    if constexpr (kShared) {
+      // K fragments rebuilt from the V page: k-steps 0 and 1 rotate together,
+      // the rest are V * w_k.  Fragment register r holds position
+      // pos0 + g + 8 (r >> 1) and dims (d + 8 (r & 1) + 2 tq, +1).
+      uint32_t ka[4], kb[4];
+      {
+        uint32_t va[4], vb[4];
+        ldmatrix_x4(vst + kstep_offset(0), va[0], va[1], va[2], va[3]);
+        ldmatrix_x4(vst + kstep_offset(1), vb[0], vb[1], vb[2], vb[3]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float2 a = bf16x2_to_float2(va[r]), b = bf16x2_to_float2(vb[r]);
+          const float2 wa = bf16x2_to_float2(wk(0, r & 1)), wb = bf16x2_to_float2(wk(1, r & 1));
+          const float a0 = a.x * wa.x, a1 = a.y * wa.y;  // exact
+          const float b0 = b.x * wb.x, b1 = b.y * wb.y;
+          const int pos = pos0 + g + 8 * (r >> 1), e = 2 * (r & 1);
+          float c0, s0, c1, s1;
+          rope_angle(kr->two_pi, freq[e], pos, c0, s0);
+          rope_angle(kr->two_pi, freq[e + 1], pos, c1, s1);
+          ka[r] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+          kb[r] = pack_bf16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+        }
+      }
+      mma_bf16_16816(se[0], qa[0], ka[0], ka[1]);
+      mma_bf16_16816(se[1], qa[0], ka[2], ka[3]);
+      mma_bf16_16816(so[0], qa[1], kb[0], kb[1]);
+      mma_bf16_16816(so[1], qa[1], kb[2], kb[3]);
       auto k_frag = [&](int ks, uint32_t (&b)[4]) {
-        const int ch = 2 * warp + (ks >> 2);
-        const int row = ((mi >> 1) << 3) + lr;
-        const int unit = 2 * (ks & 3) + (mi & 1);
-        ldmatrix_x4(kst + ch * kChunkBytes + swz(row, unit), b[0], b[1], b[2], b[3]);
+        ldmatrix_x4(vst + kstep_offset(ks), b[0], b[1], b[2], b[3]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) b[r] = bf16x2_mul(b[r], wk(ks, r & 1));
+      };
+      uint32_t kf[kAhead + 1][4];
+#pragma unroll
+      for (int ks = 2; ks < 2 + kAhead; ++ks) k_frag(ks, kf[ks % (kAhead + 1)]);
+#pragma unroll
+      for (int ks = 2; ks < 8; ++ks) {
+        if (ks + kAhead < 8) k_frag(ks + kAhead, kf[(ks + kAhead) % (kAhead + 1)]);
+        const uint32_t (&b)[4] = kf[ks % (kAhead + 1)];
+        float (&s0)[4] = (ks & 1) ? so[0] : se[0];
+        float (&s1)[4] = (ks & 1) ? so[1] : se[1];
+        mma_bf16_16816(s0, qa[ks], b[0], b[1]);
+        mma_bf16_16816(s1, qa[ks], b[2], b[3]);
+      }
+    } else {
+      auto k_frag = [&](int ks, uint32_t (&b)[4]) {
+        ldmatrix_x4(kst + kstep_offset(ks), b[0], b[1], b[2], b[3]);
       };
       uint32_t kb[kAhead + 1][4];
 #pragma unroll
@@ -288,6 +424,8 @@ __global__ void __launch_bounds__(kThreads)
                             pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
 
     // ---- zero V rows outside [lo, L) in this warp's two chunks ----
+    //      (after the exchange barrier: with a values-only cache every warp
+    //      has read these chunks for its keys by then)
     if (pos0 < cur.lo || pos0 + kPage > cur.L) {
 #pragma unroll 1
       for (int rr = 0; rr < kPage; ++rr) {
@@ -360,6 +498,19 @@ __global__ void __launch_bounds__(kThreads)
       reset();
     }
   }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ DecodeParams p) {
+  decode_body<false>(&tm_k, &tm_v, p, nullptr);
+}
+
+// Values-only cache: p.v_pool holds V; keys are rebuilt as rope(V * w_k).
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+    decode_kernel_shared(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ DecodeParams p,
+                         const __grid_constant__ KeyRebuild kr) {
+  decode_body<true>(nullptr, &tm_v, p, &kr);
 }
 
 }  // namespace global

@@ -16,13 +16,9 @@
 // never leaves its lane; each half is one 8- or 16-byte access.  Sums of
 // squares are reduced with shuffles in fp32.
 //
-// RoPE angles.  pos * f_i rounded to fp32 is off by up to 0.016 rad at
-// pos = 262143, so f_i is carried as a pair of floats hi + lo (about 46
-// significant bits), pos * f_i as a float plus its exact fma remainder, and
-// the turns are removed with a three-part 2*pi (Cody and Waite's additive
-// range reduction) before __sincosf of an argument in [-pi, pi].  f_i is not
-// looked up per lane (a kernel-parameter table read at 32 different offsets
-// is served one offset at a time): lane l forms it as
+// RoPE angles as in rope.cuh.  f_i is not looked up per lane (a kernel-
+// parameter table read at 32 different offsets is served one offset at a
+// time): lane l forms it as
 //   theta^(-2 V l / D) * theta^(-2 j / D),  j = i - V l,
 // the first factor the product of theta^(-2 V 2^k / D) over the set bits k
 // of l, every factor a host-computed float pair read at the same offset by
@@ -36,16 +32,13 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "rope.cuh"
 
 namespace pda {
 namespace append {
 
 constexpr int kLaneBits = 5;  // lanes 0..31
 constexpr int kMaxV = 8;      // D / 64 for D = 512
-
-struct FloatPair {  // hi + lo, |lo| <= ulp(hi) / 2
-  float hi, lo;
-};
 
 struct AppendParams {
   const __nv_bfloat16* qkv;    // [B, row_len]
@@ -54,27 +47,17 @@ struct AppendParams {
   const int32_t* block_table;  // [B, max_blocks]
   const int32_t* positions;    // [B]
   __nv_bfloat16* q_out;        // [B, Hq, D]
-  __nv_bfloat16* k_pool;       // [num_pages, 16, Hkv, D]
+  __nv_bfloat16* k_pool;       // [num_pages, 16, Hkv, D]; null: values-only global cache
   __nv_bfloat16* v_pool;
   int32_t* status;             // optional ATTN_DEV_* word
   int64_t num_pages;
   int32_t batch;
   int32_t max_blocks;
   float eps;
-  float two_pi[3];                  // 2*pi = two_pi[0] + two_pi[1] + two_pi[2]; [0], [1] with 8 significant bits
-  float inv_two_pi;
+  TwoPi two_pi;
   FloatPair lane_factor[kLaneBits];  // theta^(-2 V 2^k / D)
   FloatPair dim_factor[kMaxV];       // theta^(-2 j / D), j < V
 };
-
-// a * b in double-float arithmetic: relative error about 2^-46.
-__device__ __forceinline__ FloatPair df_mul(FloatPair a, FloatPair b) {
-  const float p = a.hi * b.hi;
-  float e = fmaf(a.hi, b.hi, -p);  // exact error of p
-  e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
-  const float hi = p + e;
-  return {hi, e - (hi - p)};
-}
 
 // theta^(-2 V lane / D): the lane's share of its frequencies.
 __device__ __forceinline__ FloatPair lane_frequency(const AppendParams& p, int lane) {
@@ -85,20 +68,6 @@ __device__ __forceinline__ FloatPair lane_frequency(const AppendParams& p, int l
     f = df_mul(f, m);
   }
   return f;
-}
-
-// cos and sin of pos * (f.hi + f.lo) for an integer 0 <= pos < 2^24.
-__device__ __forceinline__ void rope_angle(const AppendParams& p, FloatPair f, int pos, float& c, float& s) {
-  const float fp = static_cast<float>(pos);  // exact
-  const float hi = fp * f.hi;
-  const float err = fmaf(fp, f.hi, -hi);  // pos * f.hi - hi, exactly
-  const float small = fmaf(fp, f.lo, err);
-  const float n = rintf(hi * p.inv_two_pi);
-  float r = fmaf(-n, p.two_pi[0], hi);  // n * two_pi[0] and n * two_pi[1] are exact for n < 2^16
-  r = fmaf(-n, p.two_pi[1], r);
-  r = fmaf(-n, p.two_pi[2], r);
-  r += small;
-  __sincosf(r, &s, &c);
 }
 
 template <int kD>
@@ -190,7 +159,7 @@ __device__ __forceinline__ void rotate(const AppendParams& p, Row<kD>& r, int po
 #pragma unroll
   for (int j = 0; j < kV; ++j) {
     float c, s;
-    rope_angle(p, df_mul(fl, p.dim_factor[j]), pos, c, s);
+    rope_angle(p.two_pi, df_mul(fl, p.dim_factor[j]), pos, c, s);
     const float a = r.lo[j], b = r.hi[j];
     r.lo[j] = a * c - b * s;
     r.hi[j] = b * c + a * s;
@@ -247,7 +216,7 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
 
   normalise<kD>(x, p.eps);
   if (is_value || kShared) store_row<kD>(p.v_pool + (slot * kHkv + c) * kD, x);  // v_norm: no weights
-  if (is_value) return;
+  if (is_value || (kShared && p.k_pool == nullptr)) return;  // a values-only cache rebuilds keys when read
   scale<kD>(x, w);
   rotate<kD, kPairs>(p, x, pos);
   store_row<kD>(p.k_pool + (slot * kHkv + c) * kD, x);

@@ -27,6 +27,13 @@ def test_algorithmic_bytes_per_position():
     assert bench.algorithmic_bytes("global", [0, 0], 0) == 2 * 16 * 512 * 2 * 2
 
 
+def test_values_only_cache_reads_half_the_bytes_per_position():
+    # V only: 512 bf16 per visible position; q, o and w_k on top
+    assert bench.shared_bytes([10], 0) - bench.shared_bytes([9], 0) == 1024
+    assert bench.shared_bytes([5000], 100) == bench.shared_bytes([100], 100)
+    assert bench.shared_bytes([0], 0) == 16 * 512 * 2 * 2 + 512 * 2
+
+
 def test_append_bytes_per_token():
     # sliding: qkv row 8192 x 2 read, q 16 x 256 x 2 written, k and v 8 x 256 x 2 each written
     assert bench.append_bytes("sliding", 2) - bench.append_bytes("sliding", 1) == 16384 + 8192 + 8192

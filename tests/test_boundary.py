@@ -122,10 +122,12 @@ def call(lib, name="attn_decode_sliding", **kw):
               a["ws"], a["ws_bytes"], a["status"], a["stream"])
 
 
-@pytest.mark.parametrize("name", ["attn_decode_sliding", "attn_decode_global"])
+# attn_decode_global_shared takes (q, kv_pool, w_k, ...): k is its pool, v its w_k
+@pytest.mark.parametrize("name", ["attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared"])
 @pytest.mark.parametrize("bad,code", [
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(bt=None), 1), (dict(sl=None), 1),
-    (dict(o=None), 1), (dict(q=FAKE + 8), 1), (dict(o=FAKE + 2), 1), (dict(status=FAKE + 2), 1),
+    (dict(o=None), 1), (dict(q=FAKE + 8), 1), (dict(v=FAKE + 8), 1), (dict(o=FAKE + 2), 1),
+    (dict(status=FAKE + 2), 1),
     (dict(batch=0), 1), (dict(batch=257), 2), (dict(max_blocks=0), 1), (dict(num_pages=0), 1),
     (dict(num_pages=1 << 27), 2), (dict(max_seq_len=-1), 1), (dict(max_seq_len=70 * 16 + 1), 1),
     (dict(max_blocks=20000, max_seq_len=262145), 2), (dict(out_dtype=2), 1), (dict(num_splits=-1), 1),

@@ -127,6 +127,11 @@ def _norm_weight(D, gen, device):
     return (1.0 + 0.1 * torch.randn(D, generator=gen, device=device)).to(torch.bfloat16)
 
 
+def key_weight(D, seed, device="cpu"):
+    """A seeded qk_norm weight w_k ~ N(1, 0.1), bf16 [D] (values-only cache cases)."""
+    return _norm_weight(D, torch.Generator(device=device).manual_seed(int(seed)), device)
+
+
 def _allocated_pages(L, window, window_only):
     """Logical page indices that hold a cached position this call may need."""
     if L <= 0:
