@@ -61,12 +61,15 @@ NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 # only while the sources still hash to that value (profiles/ has the
 # captures and their commands).
 NCU_TRAFFIC = {
-    ("global", "2"): (65_390_080, "241d4fbd50da2f47"),
-    ("global", "4b"): (2_153_037_312, "241d4fbd50da2f47"),
+    ("global", "2"): (65_354_752, "eea333647ca0b4ec"),
+    ("global", "4b"): (2_153_049_856, "eea333647ca0b4ec"),
+    ("global_shared", "2"): (32_063_488, "eea333647ca0b4ec"),
+    ("global_shared", "4b"): (1_077_322_496, "eea333647ca0b4ec"),
     ("sliding", "3"): (2_186_832_384, "46bb46920450f09a"),
 }
 KERNEL_SOURCES = {
-    "global": ["global.cuh", "common.cuh", "ptx.cuh"],
+    "global": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
+    "global_shared": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
     "sliding": ["sliding.cuh", "common.cuh", "ptx.cuh"],
 }
 
@@ -487,14 +490,55 @@ def run_ours(args, rank, world, local_rank):
     prefill = None if args.no_prefill else time_prefill(stream, dev)
     # --- the global calls again over a values-only cache ---
     shared = time_global_shared(plans, n_sets, stream, status, dev)
+    if shared is not None:
+        shared["traffic"] = recorded_traffic("global_shared", args.config)
+    # --- the step as the library's own one-launch object ---
+    whole = time_whole_step(plans, n_sets, stream, status, max(3, min(args.steps, 200)))
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the cache append" % int(status.item()))
 
-    res.update(per_type=per_type, append=append, prefill=prefill, shared=shared)
+    res.update(per_type=per_type, append=append, prefill=prefill, shared=shared, whole_step=whole)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
                heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
                launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
     return res
+
+
+def time_whole_step(plans, n_sets, stream, status, steps):
+    """The step's decode calls recorded into one pda.Step per input set and
+    launched with one attn_step_launch per step (one CUDA graph of the step's
+    calls), `steps` launches back to back between CUDA events."""
+    import torch
+    import paged_decode_attention_gb300 as pda
+    objs = []
+    for pl in plans:
+        st = pda.Step()
+        for c, ws, o in pl:
+            add = st.add_decode_sliding if c.kind == "sliding" else st.add_decode_global
+            add(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window, max_seq_len=c.max_seq_len,
+                workspace=ws, status=status, num_splits=NUM_SPLITS)
+        objs.append(st.finalize())
+    for i in range(max(3, n_sets)):
+        objs[i % n_sets].launch(stream)
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            objs[i % n_sets].launch(stream)
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    calls = [c for c, _, _ in plans[0]]
+    nbytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c in calls)
+    out = {"calls_per_step": len(calls), "kernels_per_step": objs[0].num_kernels, "us_per_step": round(ms * 1e3, 3),
+           "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "launch": "one attn_step_launch (one CUDA graph of the step's calls) per step, %d steps back to back"
+                     % steps}
+    for st in objs:
+        st.close()
+    return out
 
 
 def time_global_shared(plans, n_sets, stream, status, dev, rounds=5):
@@ -924,6 +968,8 @@ def main(argv=None):
                            for k, v in r0["prefill"].items()}
     if r0.get("append"):
         line["append"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4)) for k, v in r0["append"].items()}
+    if r0.get("whole_step"):
+        line["whole_step_launch"] = dict(r0["whole_step"], frac_of_peak=round(r0["whole_step"]["value"] / peak, 4))
     if r0.get("shared"):
         line["global_values_only_cache"] = dict(r0["shared"], frac_of_peak=round(r0["shared"]["value"] / peak, 4))
     line["e2e"] = r0["e2e"]

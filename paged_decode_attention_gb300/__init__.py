@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared", "attn_decode_plan",
     "attn_decode_workspace_size",
-    "PreparedDecode", "prepare_decode_sliding", "prepare_decode_global", "prepare_decode_global_shared",
+    "PreparedDecode", "prepare_decode_sliding", "prepare_decode_global", "prepare_decode_global_shared", "Step",
     "attn_last_error", "load", "library_path", "AttnDecodeError",
     "KIND_SLIDING", "KIND_GLOBAL", "DEV_WAIT_TIMEOUT", "DEV_BAD_PAGE", "DEV_BAD_SEQ_LEN",
 ]
@@ -38,6 +38,9 @@ SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
 EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared", "attn_decode_plan",
            "attn_decode_workspace_size", "attn_kv_append_sliding", "attn_kv_append_global",
            "attn_prefill_sliding", "attn_prefill_global",
+           "attn_step_create", "attn_step_destroy", "attn_step_add_decode_sliding", "attn_step_add_decode_global",
+           "attn_step_add_decode_global_shared", "attn_step_add_kv_append_sliding", "attn_step_add_kv_append_global",
+           "attn_step_num_calls", "attn_step_num_kernels", "attn_step_finalize", "attn_step_launch",
            "attn_last_error", "attn_abi_version")
 APPEND_ROW = {KIND_SLIDING: 16 * 256 + 2 * 8 * 256, KIND_GLOBAL: 16 * 512 + 512}  # qkv row length
 
@@ -93,6 +96,25 @@ def load(path=None):
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = pre
+    c_step = ctypes.c_void_p
+    lib.attn_step_create.restype = c_i32
+    lib.attn_step_create.argtypes = [ctypes.POINTER(c_step)]
+    lib.attn_step_destroy.restype = None
+    lib.attn_step_destroy.argtypes = [c_step]
+    for name in ("attn_step_add_decode_sliding", "attn_step_add_decode_global", "attn_step_add_decode_global_shared"):
+        fn = getattr(lib, name)
+        fn.restype = c_i32
+        fn.argtypes = [c_step] + call[:-1]
+    for name in ("attn_step_add_kv_append_sliding", "attn_step_add_kv_append_global"):
+        fn = getattr(lib, name)
+        fn.restype = c_i32
+        fn.argtypes = [c_step] + app[:-1]
+    for name in ("attn_step_num_calls", "attn_step_num_kernels", "attn_step_finalize"):
+        fn = getattr(lib, name)
+        fn.restype = c_i32
+        fn.argtypes = [c_step]
+    lib.attn_step_launch.restype = c_i32
+    lib.attn_step_launch.argtypes = [c_step, c_vp]
     lib.attn_selftest_delayed_copy.restype = c_i32
     lib.attn_selftest_delayed_copy.argtypes = [c_vp, c_vp, c_i64, c_i32, c_vp]
     lib.attn_last_error.restype = ctypes.c_char_p
@@ -144,8 +166,12 @@ def _ptr(t, name, dtype, shape=None):
     return t.data_ptr()
 
 
-def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len, out_dtype,
-          num_splits, workspace, status, stream, w_k=None):
+def _decode_args(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len, out_dtype,
+                 num_splits, workspace, status, w_k=None):
+    """Checked, marshalled arguments of one decode call (everything but the stream).
+
+    Returns (args, keep, o, fn_name): the C arguments, the tensors they point
+    into (to be kept alive), the output tensor and the C entry point."""
     Hq, Hkv, D = SHAPES[kind]
     if q.dim() != 3:
         raise ValueError("q must be [batch, %d, %d]" % (Hq, D))
@@ -170,22 +196,34 @@ def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len
     args_o = _ptr(o, "o", o.dtype, (batch, Hq, D))
     if max_seq_len is None:
         max_seq_len = max_blocks * PAGE_SIZE
-    lib = load()
     if workspace is None:
         with torch.cuda.device(q.device):
             need = attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     ws_ptr = _ptr(workspace, "workspace", torch.uint8)
     st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
+    fn_name = ("attn_decode_sliding" if kind == KIND_SLIDING else
+               "attn_decode_global" if w_k is None else "attn_decode_global_shared")
+    args = (args_q, args_k, args_v, args_bt, args_sl, args_o, batch, max_blocks, num_pages, int(max_seq_len),
+            int(window), OUT_F32 if o.dtype == torch.float32 else OUT_BF16, int(num_splits), ws_ptr,
+            workspace.numel(), st_ptr)
+    keep = (q, k_pool, v_pool, block_table, seq_lens, o, workspace, status, w_k)
+    return args, keep, o, fn_name
+
+
+def _stream_ptr(stream, device):
     if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    fn = (lib.attn_decode_sliding if kind == KIND_SLIDING else
-          lib.attn_decode_global if w_k is None else lib.attn_decode_global_shared)
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _call(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len, out_dtype,
+          num_splits, workspace, status, stream, w_k=None):
+    args, _, o, fn_name = _decode_args(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len,
+                                       out_dtype, num_splits, workspace, status, w_k)
+    s_ptr = _stream_ptr(stream, q.device)
     with torch.cuda.device(q.device):
-        st = fn(args_q, args_k, args_v, args_bt, args_sl, args_o, batch, max_blocks, num_pages,
-                int(max_seq_len), int(window), OUT_F32 if o.dtype == torch.float32 else OUT_BF16,
-                int(num_splits), ws_ptr, workspace.numel(), st_ptr, s_ptr)
+        st = getattr(load(), fn_name)(*args, s_ptr)
     if st != ATTN_OK:
         raise AttnDecodeError(st, attn_last_error())
     return o
@@ -203,33 +241,10 @@ class PreparedDecode:
 
     def __init__(self, kind, q, k_pool, v_pool, block_table, seq_lens, o=None, *, window, max_seq_len=None,
                  out_dtype=torch.bfloat16, num_splits=0, workspace=None, status=None, w_k=None):
-        Hq, Hkv, D = SHAPES[kind]
-        batch, num_pages, max_blocks = q.shape[0], k_pool.shape[0], block_table.shape[1]
-        ptrs = [_ptr(q, "q", torch.bfloat16, (batch, Hq, D)),
-                _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
-                _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))
-                if w_k is None else _ptr(w_k, "w_k", torch.bfloat16, (D,)),
-                _ptr(block_table, "block_table", torch.int32, (batch, max_blocks)),
-                _ptr(seq_lens, "seq_lens", torch.int32, (batch,))]
-        if o is None:
-            o = torch.empty((batch, Hq, D), dtype=out_dtype, device=q.device)
-        ptrs.append(_ptr(o, "o", o.dtype, (batch, Hq, D)))
-        if max_seq_len is None:
-            max_seq_len = max_blocks * PAGE_SIZE
-        lib = load()
-        if workspace is None:
-            with torch.cuda.device(q.device):
-                need = attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits)
-            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-        ws_ptr = _ptr(workspace, "workspace", torch.uint8)
-        st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
-        self._keep = (q, k_pool, v_pool, block_table, seq_lens, o, workspace, status, w_k)
-        self.o = o
-        self._fn = (lib.attn_decode_sliding if kind == KIND_SLIDING else
-                    lib.attn_decode_global if w_k is None else lib.attn_decode_global_shared)
-        self._args = tuple(ptrs) + (batch, max_blocks, num_pages, int(max_seq_len), int(window),
-                                    OUT_F32 if o.dtype == torch.float32 else OUT_BF16, int(num_splits),
-                                    ws_ptr, workspace.numel(), st_ptr)
+        self._args, self._keep, self.o, fn_name = _decode_args(
+            kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len, out_dtype, num_splits,
+            workspace, status, w_k)
+        self._fn = getattr(load(), fn_name)
 
     def run(self, stream):
         """Enqueue the call on `stream` (a torch.cuda.Stream or a raw cudaStream_t); returns o."""
@@ -238,6 +253,103 @@ class PreparedDecode:
         if st != ATTN_OK:
             raise AttnDecodeError(st, attn_last_error())
         return self.o
+
+
+class Step:
+    """The attention calls of a decode step, recorded once and launched as one CUDA graph.
+
+    ``add_*`` take the arguments of the one-shot function of the same name
+    (minus the stream), validate them at once and return the call's output
+    tensor (o, or q_out for the appends).  ``finalize()`` captures the calls,
+    in the order added, on the current CUDA device; ``launch(stream)`` then
+    enqueues the whole step with one C call and one graph launch.  The
+    tensors are used in place (the object keeps references to them); their
+    contents may change between launches.
+    """
+
+    def __init__(self):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        self._check(self._lib.attn_step_create(ctypes.byref(h)))
+        self._h = h
+        self._keep = []
+        self.device = None
+
+    def _check(self, rc):
+        if rc != ATTN_OK:
+            raise AttnDecodeError(rc, attn_last_error())
+
+    def _add_decode(self, kind, fn_name, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len=None,
+                    out_dtype=torch.bfloat16, num_splits=0, workspace=None, status=None, w_k=None):
+        args, keep, o, name = _decode_args(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len,
+                                           out_dtype, num_splits, workspace, status, w_k)
+        with torch.cuda.device(q.device):
+            self._check(getattr(self._lib, fn_name)(self._h, *args))
+        self._keep.append(keep)
+        self.device = q.device
+        return o
+
+    def add_decode_sliding(self, q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=1024, **kw):
+        return self._add_decode(KIND_SLIDING, "attn_step_add_decode_sliding", q, k_pool, v_pool, block_table,
+                                seq_lens, o, window, **kw)
+
+    def add_decode_global(self, q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=0, **kw):
+        return self._add_decode(KIND_GLOBAL, "attn_step_add_decode_global", q, k_pool, v_pool, block_table,
+                                seq_lens, o, window, **kw)
+
+    def add_decode_global_shared(self, q, kv_pool, w_k, block_table, seq_lens, o=None, *, window=0, **kw):
+        return self._add_decode(KIND_GLOBAL, "attn_step_add_decode_global_shared", q, kv_pool, kv_pool, block_table,
+                                seq_lens, o, window, w_k=w_k, **kw)
+
+    def _add_append(self, kind, fn_name, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status):
+        args, keep, q_out, _ = _append_args(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out,
+                                            status)
+        with torch.cuda.device(qkv.device):
+            self._check(getattr(self._lib, fn_name)(self._h, *args))
+        self._keep.append(keep)
+        self.device = qkv.device
+        return q_out
+
+    def add_kv_append_sliding(self, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out=None, *,
+                              status=None):
+        return self._add_append(KIND_SLIDING, "attn_step_add_kv_append_sliding", qkv, w_q, w_k, block_table,
+                                positions, k_pool, v_pool, q_out, status)
+
+    def add_kv_append_global(self, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out=None, *,
+                             status=None):
+        return self._add_append(KIND_GLOBAL, "attn_step_add_kv_append_global", qkv, w_q, w_k, block_table,
+                                positions, k_pool, v_pool, q_out, status)
+
+    @property
+    def num_calls(self):
+        return self._lib.attn_step_num_calls(self._h)
+
+    @property
+    def num_kernels(self):
+        return self._lib.attn_step_num_kernels(self._h)
+
+    def finalize(self):
+        if self.device is None:
+            raise AttnDecodeError(1, "no calls recorded")
+        with torch.cuda.device(self.device):
+            self._check(self._lib.attn_step_finalize(self._h))
+        return self
+
+    def launch(self, stream=None):
+        """Enqueue the whole step on `stream` (default: the current stream of its device)."""
+        self._check(self._lib.attn_step_launch(self._h, _stream_ptr(stream, self.device)))
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            self._lib.attn_step_destroy(self._h)
+        self._h = None
+        self._keep = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def prepare_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, window=1024, **kw):
@@ -287,7 +399,8 @@ def attn_decode_global_shared(q, kv_pool, w_k, block_table, seq_lens, o=None, *,
                  out_dtype, num_splits, workspace, status, stream, w_k=w_k)
 
 
-def _append(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream):
+def _append_args(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status):
+    """Checked, marshalled arguments of one append call: (args, keep, q_out, fn_name)."""
     Hq, Hkv, D = SHAPES[kind]
     batch, max_blocks, num_pages = qkv.shape[0], block_table.shape[1], v_pool.shape[0]
     args = [_ptr(qkv, "qkv", torch.bfloat16, (batch, APPEND_ROW[kind])),
@@ -302,12 +415,16 @@ def _append(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, 
              _ptr(k_pool, "k_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D)),
              _ptr(v_pool, "v_pool", torch.bfloat16, (num_pages, PAGE_SIZE, Hkv, D))]
     st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
-    if stream is None:
-        stream = torch.cuda.current_stream(qkv.device)
-    s_ptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    lib = load()
-    fn = lib.attn_kv_append_sliding if kind == KIND_SLIDING else lib.attn_kv_append_global
-    rc = fn(*args, batch, max_blocks, num_pages, st_ptr, s_ptr)
+    args += [batch, max_blocks, num_pages, st_ptr]
+    fn_name = "attn_kv_append_sliding" if kind == KIND_SLIDING else "attn_kv_append_global"
+    keep = (qkv, w_q, w_k, block_table, positions, q_out, k_pool, v_pool, status)
+    return tuple(args), keep, q_out, fn_name
+
+
+def _append(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out, status, stream):
+    args, _, q_out, fn_name = _append_args(kind, qkv, w_q, w_k, block_table, positions, k_pool, v_pool, q_out,
+                                           status)
+    rc = getattr(load(), fn_name)(*args, _stream_ptr(stream, qkv.device))
     if rc != ATTN_OK:
         raise AttnDecodeError(rc, attn_last_error())
     return q_out

@@ -20,6 +20,9 @@
 namespace {
 
 thread_local char g_err[512] = "";
+// Set while attn_step_add_* validates a call: run_decode and run_append
+// return after their host checks, before anything is encoded or launched.
+thread_local bool g_validate_only = false;
 
 int32_t fail(int32_t code, const char* fmt, ...) {
   va_list ap;
@@ -321,6 +324,7 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
                 (sliding ? ATTN_SLIDING_HQ : ATTN_GLOBAL_HQ);
   p.out_f32 = out_dtype == ATTN_OUT_F32;
 
+  if (g_validate_only) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tm_k, tm_v;
   cudaError_t e;
@@ -491,6 +495,7 @@ int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w
   static_assert(ATTN_SLIDING_D / 64 <= pda::append::kMaxV && ATTN_GLOBAL_D / 64 <= pda::append::kMaxV, "dims per lane");
   const int rows = sliding ? ATTN_SLIDING_HQ + 2 * ATTN_SLIDING_HKV : ATTN_GLOBAL_HQ + 1;
   const dim3 grid((batch * rows + 3) / 4);
+  if (g_validate_only) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (sliding)
@@ -731,3 +736,5 @@ extern "C" int32_t attn_decode_sliding_noalloc(const void* q, const void* k_pool
                     num_pages, max_seq_len, window, out_dtype, num_splits, scratch, kNoAllocScratchBytes,
                     status, stream);
 }
+
+#include "step.cuh"

@@ -12,7 +12,8 @@ import paged_decode_attention_gb300 as pda
 from paged_decode_attention_gb300 import _build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "attn_decode.h")
+INCLUDE = os.path.join(ROOT, "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +23,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
 
@@ -30,13 +31,14 @@ def declared_functions():
 def test_header_declares_the_operations():
     names = declared_functions()
     for n in ("attn_decode_sliding", "attn_decode_global", "attn_decode_plan",
-              "attn_decode_workspace_size", "attn_last_error", "attn_abi_version"):
+              "attn_decode_workspace_size", "attn_last_error", "attn_abi_version",
+              "attn_decode_global_shared", "attn_step_create", "attn_step_launch"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for n in declared_functions():
-        assert hasattr(lib, n), "symbol %s declared in attn_decode.h but not exported" % n
+        assert hasattr(lib, n), "symbol %s declared in include/ but not exported" % n
 
 
 def test_binding_covers_the_exports(lib):
@@ -49,7 +51,8 @@ def test_abi_version(lib):
 
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "use.c"
-    src.write_text('#include "attn_decode.h"\nint main(void){return ATTN_OK;}\n')
+    src.write_text('#include "attn_decode.h"\n#include "attn_step.h"\n'
+                   'int main(void){attn_step* s = 0; return ATTN_OK + attn_step_num_calls(s);}\n')
     import subprocess
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
                     "-c", str(src), "-o", str(tmp_path / "use.o")], check=True)
@@ -151,3 +154,65 @@ def test_binding_refuses_cpu_tensors(lib):
     sl = torch.ones(1, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         pda.attn_decode_sliding(q, pool, pool, bt, sl)
+
+
+# ---------------------------------------------------------------------------
+# whole-step object: recording validates each call; nothing needs a GPU until
+# a valid call queries the device
+# ---------------------------------------------------------------------------
+
+def _step_add(lib, step, name, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, o=FAKE, batch=4, max_blocks=70,
+             num_pages=300, max_seq_len=1100, window=1024, out_dtype=0, num_splits=0,
+             ws=None, ws_bytes=0, status=None)
+    a.update(kw)
+    return getattr(lib, name)(step, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["o"], a["batch"], a["max_blocks"],
+                              a["num_pages"], a["max_seq_len"], a["window"], a["out_dtype"], a["num_splits"],
+                              a["ws"], a["ws_bytes"], a["status"])
+
+
+@pytest.mark.parametrize("name", ["attn_step_add_decode_sliding", "attn_step_add_decode_global",
+                                  "attn_step_add_decode_global_shared"])
+@pytest.mark.parametrize("bad,code", [(dict(q=None), 1), (dict(o=FAKE + 2), 1), (dict(batch=257), 2),
+                                      (dict(num_splits=-1), 1), (dict(out_dtype=7), 1)])
+def test_step_rejects_a_bad_call_and_records_nothing(lib, name, bad, code):
+    h = ctypes.c_void_p()
+    assert lib.attn_step_create(ctypes.byref(h)) == 0
+    try:
+        assert _step_add(lib, h, name, **bad) == code
+        assert pda.attn_last_error() != ""
+        assert lib.attn_step_num_calls(h) == 0 and lib.attn_step_num_kernels(h) == 0
+    finally:
+        lib.attn_step_destroy(h)
+
+
+def test_step_without_calls_or_handle(lib):
+    h = ctypes.c_void_p()
+    assert lib.attn_step_create(ctypes.byref(h)) == 0
+    try:
+        assert lib.attn_step_finalize(h) == 1 and "no calls" in pda.attn_last_error()
+        assert lib.attn_step_launch(h, None) == 1 and "not finalized" in pda.attn_last_error()
+    finally:
+        lib.attn_step_destroy(h)
+    assert lib.attn_step_create(None) == 1
+    assert lib.attn_step_finalize(None) == 1
+    assert lib.attn_step_launch(None, None) == 1
+    assert lib.attn_step_num_calls(None) == 0
+    lib.attn_step_destroy(None)  # ignored
+
+
+def test_step_append_validation(lib):
+    h = ctypes.c_void_p()
+    assert lib.attn_step_create(ctypes.byref(h)) == 0
+    try:
+        # sliding needs a key pool; a batch outside the domain is refused
+        assert lib.attn_step_add_kv_append_sliding(h, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4, 70, 300,
+                                                   None) == 1
+        assert lib.attn_step_add_kv_append_global(h, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, 70, 300,
+                                                  None) == 2
+        # a values-only global append passes the host checks (no device query) and is recorded
+        assert lib.attn_step_add_kv_append_global(h, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4, 70, 300,
+                                                  None) == 0
+        assert lib.attn_step_num_calls(h) == 1 and lib.attn_step_num_kernels(h) == 1
+    finally:
+        lib.attn_step_destroy(h)
