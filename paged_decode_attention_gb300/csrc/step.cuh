@@ -29,7 +29,11 @@ int32_t record(attn_step* step, int32_t kernels, std::function<int32_t(void*)> c
   const int32_t st = call(nullptr);
   g_validate_only = false;
   if (st != ATTN_OK) return st;
-  step->calls.push_back(std::move(call));
+  try {
+    step->calls.push_back(std::move(call));
+  } catch (...) {  // no exception may leave the C ABI
+    return fail(ATTN_ERR_INVALID_ARG, "%s: out of host memory", name);
+  }
   step->kernels += kernels;
   return ATTN_OK;
 }
