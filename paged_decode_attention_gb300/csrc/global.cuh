@@ -55,7 +55,7 @@ constexpr int kChunks = kD / kChunk;                // 8
 constexpr int kChunkBytes = kPage * kChunk * 2;     // 2 KB
 constexpr int kPageBytes = kPage * kD * 2;          // 16 KB
 constexpr int kStages = 3;
-constexpr int kSharedStages = 6;  // values-only pages are half the size
+constexpr int kSharedStages = 4;  // values-only pages are half the size
 constexpr int kBlocksPerSm = 2;
 constexpr int kRopePairs = ATTN_GLOBAL_ROPE_PAIRS;  // 64: dims [0, 64) turn with [256, 320)
 constexpr int kMinPages = 4;
@@ -77,14 +77,16 @@ struct KPages {
   alignas(1024) uint8_t k[kStages][kPageBytes];  // kChunks tiles of [16 rows][64 dims], swizzled
 };
 struct KeyWeights {
-  uint32_t wk[kD / 2];  // w_k as bf16x2 words
+  alignas(16) uint4 qfrag[kConsumerWarps][8][32];  // q A fragments: per warp and S k-step, one word per lane
+  uint32_t wk[kD / 2];                             // w_k as bf16x2 words
+  FloatPair freq[kRopePairs];                      // RoPE frequencies of the active pairs
 };
 
 template <bool kShared>
 struct Smem : std::conditional_t<kShared, KeyWeights, KPages> {
   static constexpr int kNumStages = kShared ? kSharedStages : kStages;
   alignas(1024) uint8_t v[kNumStages][kPageBytes];
-  alignas(16) float4 xs[2][kConsumerWarps][2][32];  // partial-S exchange, double-buffered
+  alignas(16) float4 xs[2][kConsumerWarps][kShared ? 4 : 2][32];  // partial-S exchange (n-tiles), double-buffered
   SeqTable table;
   alignas(8) uint64_t full[kNumStages];
   alignas(8) uint64_t empty[kNumStages];
@@ -167,6 +169,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
     if (warp < kConsumerWarps) {  // w_k to shared memory; published by confirm_seq_table's barrier
       const uint32_t* w32 = reinterpret_cast<const uint32_t*>(kr->w_k);
       for (int k = threadIdx.x; k < kD / 2; k += kConsumerWarps * 32) s.wk[k] = __ldg(w32 + k);
+      if (threadIdx.x < kRopePairs) s.freq[threadIdx.x] = kr->freq[threadIdx.x];
     }
   }
   // The producer reads its first block-table entries while warp 0 confirms
@@ -207,17 +210,33 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
   cur.start(p, t, sp);
 
   // q as m16n8k16 A fragments over this warp's 128 S dims (8 k-steps of 16)
-  uint32_t qa[8][4];
+  // With a values-only cache each lane parks its fragments in shared memory
+  // (it alone reads them back), which frees 32 registers for two-page groups.
+  uint32_t qa_reg[kShared ? 1 : 8][4];
+  uint32_t qfrag_addr = 0;
+  if constexpr (kShared) qfrag_addr = smem_addr(&s.qfrag[warp][0][lane]);
   auto load_q = [&]() {
     const uint32_t* q_g = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(cur.b) * kHq + g) * kD);
     const uint32_t* q_g8 = q_g + 8 * kD / 2;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int d = s_kstep_dim<kShared>(warp, ks) + 2 * tq;
-      qa[ks][0] = __ldg(q_g + d / 2);
-      qa[ks][1] = __ldg(q_g8 + d / 2);
-      qa[ks][2] = __ldg(q_g + (d + 8) / 2);
-      qa[ks][3] = __ldg(q_g8 + (d + 8) / 2);
+      const uint4 v = make_uint4(__ldg(q_g + d / 2), __ldg(q_g8 + d / 2), __ldg(q_g + (d + 8) / 2),
+                                 __ldg(q_g8 + (d + 8) / 2));
+      if constexpr (kShared) {
+        st_shared_v4(qfrag_addr + ks * 512, v);
+      } else {
+        qa_reg[ks][0] = v.x; qa_reg[ks][1] = v.y; qa_reg[ks][2] = v.z; qa_reg[ks][3] = v.w;
+      }
+    }
+  };
+  // the A fragment of S k-step ks
+  auto qa = [&](int ks, uint32_t (&a)[4]) {
+    if constexpr (kShared) {
+      const uint4 v = ld_shared_v4(qfrag_addr + ks * 512);
+      a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+    } else {
+      a[0] = qa_reg[ks][0]; a[1] = qa_reg[ks][1]; a[2] = qa_reg[ks][2]; a[3] = qa_reg[ks][3];
     }
   };
   // Pull q of the span's next sequence into L2 while this one runs, so its
@@ -246,16 +265,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
 
   // Values-only cache: this lane's share of the key rebuild.  wk(ks, h): w_k
   // at dims (d + 2 tq, +1) for h = 0 and (d + 8 + 2 tq, +1) for h = 1, d the
-  // k-step's first dim; freq[e]: pair j = 16 w + 2 tq + (e & 1) + 8 (e >> 1).
+  // k-step's first dim; freq(e): pair j = 16 w + 2 tq + (e & 1) + 8 (e >> 1).
   auto wk = [&](int ks, int h) -> uint32_t {
     if constexpr (kShared) return s.wk[(s_kstep_dim<kShared>(warp, ks) + 8 * h + 2 * tq) / 2];
     return 0u;
   };
-  FloatPair freq[4];
-  if constexpr (kShared) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) freq[e] = kr->freq[16 * warp + 2 * tq + (e & 1) + 8 * (e >> 1)];
-  }
+  auto freq = [&](int e) -> FloatPair {
+    if constexpr (kShared) return s.freq[16 * warp + 2 * tq + (e & 1) + 8 * (e >> 1)];
+    return FloatPair{0.f, 0.f};
+  };
   // byte offset of this lane's ldmatrix row in the tile of S k-step ks
   auto kstep_offset = [&](int ks) -> uint32_t {
     const int d = s_kstep_dim<kShared>(warp, ks);
@@ -263,126 +281,148 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
     return (d / kChunk) * kChunkBytes + swz(row, 2 * ((d % kChunk) / 16) + (mi & 1));
   };
 
-  for (int i = 0; i < n_pages; ++i) {
-    const int f = sp.begin + i;
-    if (f >= t.prefix[cur.b + 1]) {
-      cur.advance(p, t, sp, f);
-      load_q();
-      prefetch_next_q();
-    }
-    const int stage = i % kNS;
-    const int pos0 = cur.pos0(t, f);
+  // the full-barrier wait of page i in stage st (a timeout is reported once and ends the waits)
+  auto wait_page = [&](int i, int st) {
     if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kNS) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s.full[st], (i / kNS) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     }
-    const uint32_t vst = smem_addr(s.v[stage]);
-    uint32_t kst = vst;
-    if constexpr (!kShared) kst = smem_addr(s.k[stage]);
+  };
 
-    // ---- partial S over this warp's dims: two n-tiles of 8 positions; even
-    //      and odd k-steps accumulate separately (two chains of 4 MMAs) ----
+  // Values-only cache: NP (1 or 2) consecutive pages of one segment, with one
+  // partial-S exchange and one softmax pass for all of them.  (The separate-
+  // pool kernel runs its own one-page loop below.)
+  auto page_group = [&](auto np_c, int i, int f, int it) {
+    constexpr int NP = decltype(np_c)::value;
+    constexpr int kEO = NP == 1 ? 2 : 1;  // accumulators per n-tile: even/odd k-steps, or one chain
+    int pos0[NP], stage[NP];
+    uint32_t vst[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      stage[j] = j == 0 ? i % kNS : (stage[0] + j == kNS ? 0 : stage[0] + j);
+      pos0[j] = cur.pos0(t, f + j);
+      vst[j] = smem_addr(s.v[stage[j]]);
+    }
+
+    // ---- partial S over this warp's dims, per page: two n-tiles of 8 positions ----
     //      The K fragments are read kAhead k-steps before their MMAs.
-    float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if constexpr (kShared) {
-      // K fragments rebuilt from the V page: k-steps 0 and 1 rotate together,
-      // the rest are V * w_k.  Fragment register r holds position
-      // pos0 + g + 8 (r >> 1) and dims (d + 8 (r & 1) + 2 tq, +1).
-      uint32_t ka[4], kb[4];
-      {
-        uint32_t va[4], vb[4];
-        ldmatrix_x4(vst + kstep_offset(0), va[0], va[1], va[2], va[3]);
-        ldmatrix_x4(vst + kstep_offset(1), vb[0], vb[1], vb[2], vb[3]);
+    float sa[NP][kEO][2][4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float2 a = bf16x2_to_float2(va[r]), b = bf16x2_to_float2(vb[r]);
-          const float2 wa = bf16x2_to_float2(wk(0, r & 1)), wb = bf16x2_to_float2(wk(1, r & 1));
-          const float a0 = a.x * wa.x, a1 = a.y * wa.y;  // exact
-          const float b0 = b.x * wb.x, b1 = b.y * wb.y;
-          const int pos = pos0 + g + 8 * (r >> 1), e = 2 * (r & 1);
-          float c0, s0, c1, s1;
-          rope_angle(kr->two_pi, freq[e], pos, c0, s0);
-          rope_angle(kr->two_pi, freq[e + 1], pos, c1, s1);
-          ka[r] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
-          kb[r] = pack_bf16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int eo = 0; eo < kEO; ++eo)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sa[j][eo][nt][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      wait_page(i + j, stage[j]);
+      auto acc_of = [&](int ks, int nt) -> float (&)[4] { return sa[j][kEO == 2 ? (ks & 1) : 0][nt]; };
+      if constexpr (kShared) {
+        // K fragments rebuilt from the V page: k-steps 0 and 1 rotate together,
+        // the rest are V * w_k.  Fragment register r holds position
+        // pos0 + g + 8 (r >> 1) and dims (d + 8 (r & 1) + 2 tq, +1).
+        uint32_t ka[4], kb[4];
+        {
+          uint32_t va[4], vb[4];
+          ldmatrix_x4(vst[j] + kstep_offset(0), va[0], va[1], va[2], va[3]);
+          ldmatrix_x4(vst[j] + kstep_offset(1), vb[0], vb[1], vb[2], vb[3]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float2 a = bf16x2_to_float2(va[r]), b = bf16x2_to_float2(vb[r]);
+            const float2 wa = bf16x2_to_float2(wk(0, r & 1)), wb = bf16x2_to_float2(wk(1, r & 1));
+            const float a0 = a.x * wa.x, a1 = a.y * wa.y;  // exact
+            const float b0 = b.x * wb.x, b1 = b.y * wb.y;
+            const int pos = pos0[j] + g + 8 * (r >> 1), e = 2 * (r & 1);
+            float c0, s0, c1, s1;
+            rope_angle(kr->two_pi, freq(e), pos, c0, s0);
+            rope_angle(kr->two_pi, freq(e + 1), pos, c1, s1);
+            ka[r] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+            kb[r] = pack_bf16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+          }
         }
-      }
-      mma_bf16_16816(se[0], qa[0], ka[0], ka[1]);
-      mma_bf16_16816(se[1], qa[0], ka[2], ka[3]);
-      mma_bf16_16816(so[0], qa[1], kb[0], kb[1]);
-      mma_bf16_16816(so[1], qa[1], kb[2], kb[3]);
-      auto k_frag = [&](int ks, uint32_t (&b)[4]) {
-        ldmatrix_x4(vst + kstep_offset(ks), b[0], b[1], b[2], b[3]);
+        {
+          uint32_t a[4];
+          qa(0, a);
+          mma_bf16_16816(acc_of(0, 0), a, ka[0], ka[1]);
+          mma_bf16_16816(acc_of(0, 1), a, ka[2], ka[3]);
+          qa(1, a);
+          mma_bf16_16816(acc_of(1, 0), a, kb[0], kb[1]);
+          mma_bf16_16816(acc_of(1, 1), a, kb[2], kb[3]);
+        }
+        auto k_frag = [&](int ks, uint32_t (&b)[4]) {
+          ldmatrix_x4(vst[j] + kstep_offset(ks), b[0], b[1], b[2], b[3]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) b[r] = bf16x2_mul(b[r], wk(ks, r & 1));
-      };
-      uint32_t kf[kAhead + 1][4];
+          for (int r = 0; r < 4; ++r) b[r] = bf16x2_mul(b[r], wk(ks, r & 1));
+        };
+        constexpr int kAh = kAhead;
+        uint32_t kf[kAh + 1][4];
 #pragma unroll
-      for (int ks = 2; ks < 2 + kAhead; ++ks) k_frag(ks, kf[ks % (kAhead + 1)]);
+        for (int ks = 2; ks < 2 + kAh; ++ks) k_frag(ks, kf[ks % (kAh + 1)]);
 #pragma unroll
-      for (int ks = 2; ks < 8; ++ks) {
-        if (ks + kAhead < 8) k_frag(ks + kAhead, kf[(ks + kAhead) % (kAhead + 1)]);
-        const uint32_t (&b)[4] = kf[ks % (kAhead + 1)];
-        float (&s0)[4] = (ks & 1) ? so[0] : se[0];
-        float (&s1)[4] = (ks & 1) ? so[1] : se[1];
-        mma_bf16_16816(s0, qa[ks], b[0], b[1]);
-        mma_bf16_16816(s1, qa[ks], b[2], b[3]);
-      }
-    } else {
-      auto k_frag = [&](int ks, uint32_t (&b)[4]) {
-        ldmatrix_x4(kst + kstep_offset(ks), b[0], b[1], b[2], b[3]);
-      };
-      uint32_t kb[kAhead + 1][4];
-#pragma unroll
-      for (int ks = 0; ks < kAhead; ++ks) k_frag(ks, kb[ks]);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (ks + kAhead < 8) k_frag(ks + kAhead, kb[(ks + kAhead) % (kAhead + 1)]);
-        const uint32_t (&b)[4] = kb[ks % (kAhead + 1)];
-        float (&s0)[4] = (ks & 1) ? so[0] : se[0];
-        float (&s1)[4] = (ks & 1) ? so[1] : se[1];
-        mma_bf16_16816(s0, qa[ks], b[0], b[1]);
-        mma_bf16_16816(s1, qa[ks], b[2], b[3]);
+        for (int ks = 2; ks < 8; ++ks) {
+          if (ks + kAh < 8) k_frag(ks + kAh, kf[(ks + kAh) % (kAh + 1)]);
+          const uint32_t (&b)[4] = kf[ks % (kAh + 1)];
+          uint32_t a[4];
+          qa(ks, a);
+          mma_bf16_16816(acc_of(ks, 0), a, b[0], b[1]);
+          mma_bf16_16816(acc_of(ks, 1), a, b[2], b[3]);
+        }
       }
     }
 
     // ---- sum the four partials in a fixed order ----
-    const int buf = i & 1;
-    s.xs[buf][warp][0][lane] =
-        make_float4(se[0][0] + so[0][0], se[0][1] + so[0][1], se[0][2] + so[0][2], se[0][3] + so[0][3]);
-    s.xs[buf][warp][1][lane] =
-        make_float4(se[1][0] + so[1][0], se[1][1] + so[1][1], se[1][2] + so[1][2], se[1][3] + so[1][3]);
+    const int buf = it & 1;
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float4 v = make_float4(sa[j][0][nt][0], sa[j][0][nt][1], sa[j][0][nt][2], sa[j][0][nt][3]);
+        if constexpr (kEO == 2) {
+          v.x += sa[j][1][nt][0]; v.y += sa[j][1][nt][1]; v.z += sa[j][1][nt][2]; v.w += sa[j][1][nt][3];
+        }
+        s.xs[buf][warp][2 * j + nt][lane] = v;
+      }
     named_barrier_sync(1, kConsumerWarps * 32);
-    float sc[2][4];
-    {
-      float4 a0 = s.xs[buf][0][0][lane], a1 = s.xs[buf][0][1][lane];
+    float sc[NP][2][4];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      float4 a0 = s.xs[buf][0][2 * j][lane], a1 = s.xs[buf][0][2 * j + 1][lane];
 #pragma unroll
       for (int w = 1; w < kConsumerWarps; ++w) {
-        const float4 c0 = s.xs[buf][w][0][lane], c1 = s.xs[buf][w][1][lane];
+        const float4 c0 = s.xs[buf][w][2 * j][lane], c1 = s.xs[buf][w][2 * j + 1][lane];
         a0.x += c0.x; a0.y += c0.y; a0.z += c0.z; a0.w += c0.w;
         a1.x += c1.x; a1.y += c1.y; a1.z += c1.z; a1.w += c1.w;
       }
-      sc[0][0] = a0.x; sc[0][1] = a0.y; sc[0][2] = a0.z; sc[0][3] = a0.w;
-      sc[1][0] = a1.x; sc[1][1] = a1.y; sc[1][2] = a1.z; sc[1][3] = a1.w;
+      sc[j][0][0] = a0.x; sc[j][0][1] = a0.y; sc[j][0][2] = a0.z; sc[j][0][3] = a0.w;
+      sc[j][1][0] = a1.x; sc[j][1][1] = a1.y; sc[j][1][2] = a1.z; sc[j][1][3] = a1.w;
     }
 
     // ---- masked online softmax (log2 units) ----
-    // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*tq + (e&1).
+    // sc[j][nt][e]: head g + 8*(e>>1), position pos0[j] + 8*nt + 2*tq + (e&1).
     // Positions outside [lo, L) get -inf (pages inside the range skip the
     // test); the factor log2(e) is applied inside the exponent.
-    if (pos0 < cur.lo || pos0 + kPage > cur.L) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int j = 0; j < NP; ++j) {
+      if (pos0[j] < cur.lo || pos0[j] + kPage > cur.L) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int pos = pos0 + 8 * nt + 2 * tq + (e & 1);
-          if (pos < cur.lo || pos >= cur.L) sc[nt][e] = -INFINITY;
-        }
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pos = pos0[j] + 8 * nt + 2 * tq + (e & 1);
+            if (pos < cur.lo || pos >= cur.L) sc[j][nt][e] = -INFINITY;
+          }
+      }
     }
     float mx[2];
-    mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-    mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+    mx[0] = fmaxf(fmaxf(sc[0][0][0], sc[0][0][1]), fmaxf(sc[0][1][0], sc[0][1][1]));
+    mx[1] = fmaxf(fmaxf(sc[0][0][2], sc[0][0][3]), fmaxf(sc[0][1][2], sc[0][1][3]));
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+      mx[0] = fmaxf(mx[0], fmaxf(fmaxf(sc[j][0][0], sc[j][0][1]), fmaxf(sc[j][1][0], sc[j][1][1])));
+      mx[1] = fmaxf(mx[1], fmaxf(fmaxf(sc[j][0][2], sc[j][0][3]), fmaxf(sc[j][1][2], sc[j][1][3])));
+    }
     // The running max of a row changes only when some score exceeds it, which
     // after a sequence's first pages is rare: one vote decides whether the
     // row maxima over the four lanes that share a row are needed at all.
@@ -402,13 +442,22 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
     float m_use[2];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) m_use[rr] = m[rr] == -INFINITY ? 0.f : m[rr];
-    float pr[2][4];
+    float pr[NP][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int j = 0; j < NP; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pr[nt][e] = ex2_approx(fmaf(sc[nt][e], kLog2e, -m_use[e >> 1]));
-    l[0] = l[0] * scale[0] + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-    l[1] = l[1] * scale[1] + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[j][nt][e] = ex2_approx(fmaf(sc[j][nt][e], kLog2e, -m_use[e >> 1]));
+    float ls[2] = {(pr[0][0][0] + pr[0][0][1]) + (pr[0][1][0] + pr[0][1][1]),
+                   (pr[0][0][2] + pr[0][0][3]) + (pr[0][1][2] + pr[0][1][3])};
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+      ls[0] += (pr[j][0][0] + pr[j][0][1]) + (pr[j][1][0] + pr[j][1][1]);
+      ls[1] += (pr[j][0][2] + pr[j][0][3]) + (pr[j][1][2] + pr[j][1][3]);
+    }
+    l[0] = l[0] * scale[0] + ls[0];
+    l[1] = l[1] * scale[1] + ls[1];
     // rescale only when some row's running max moved (multiplying by 1 is exact)
     if (__any_sync(0xffffffffu, scale[0] != 1.f || scale[1] != 1.f)) {
 #pragma unroll
@@ -419,33 +468,35 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         acc[n][3] *= scale[1];
       }
     }
-    // P as the A fragment of one k16 step (k = the page's 16 positions)
-    const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
-                            pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
 
-    // ---- zero V rows outside [lo, L) in this warp's two chunks ----
-    //      (after the exchange barrier: with a values-only cache every warp
-    //      has read these chunks for its keys by then)
-    if (pos0 < cur.lo || pos0 + kPage > cur.L) {
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      // P of page j as the A fragment of one k16 step (k = its 16 positions)
+      const uint32_t pa[4] = {pack_bf16x2(pr[j][0][0], pr[j][0][1]), pack_bf16x2(pr[j][0][2], pr[j][0][3]),
+                              pack_bf16x2(pr[j][1][0], pr[j][1][1]), pack_bf16x2(pr[j][1][2], pr[j][1][3])};
+
+      // ---- zero V rows outside [lo, L) in this warp's two chunks ----
+      //      (after the exchange barrier: with a values-only cache every warp
+      //      has read these chunks for its keys by then)
+      if (pos0[j] < cur.lo || pos0[j] + kPage > cur.L) {
 #pragma unroll 1
-      for (int rr = 0; rr < kPage; ++rr) {
-        const int pos = pos0 + rr;
-        if ((pos < cur.lo || pos >= cur.L) && lane < 16) {
-          const int ch = 2 * warp + (lane >> 3);
-          st_shared_v4(vst + ch * kChunkBytes + rr * 128 + (lane & 7) * 16, make_uint4(0, 0, 0, 0));
+        for (int rr = 0; rr < kPage; ++rr) {
+          const int pos = pos0[j] + rr;
+          if ((pos < cur.lo || pos >= cur.L) && lane < 16) {
+            const int ch = 2 * warp + (lane >> 3);
+            st_shared_v4(vst[j] + ch * kChunkBytes + rr * 128 + (lane & 7) * 16, make_uint4(0, 0, 0, 0));
+          }
         }
+        fence_proxy_async_smem();  // before TMA rewrites this stage
+        __syncwarp();
       }
-      fence_proxy_async_smem();  // before TMA rewrites this stage
-      __syncwarp();
-    }
 
-    // ---- O += P V over this warp's 128 dims ----
-    {
+      // ---- O += P V over this warp's 128 dims ----
       auto v_frag = [&](int np, uint32_t (&b)[4]) {
         const int ch = 2 * warp + (np >> 2);
         const int row = ((mi & 1) << 3) + lr;
         const int unit = 2 * (np & 3) + (mi >> 1);
-        ldmatrix_x4_trans(vst + ch * kChunkBytes + swz(row, unit), b[0], b[1], b[2], b[3]);
+        ldmatrix_x4_trans(vst[j] + ch * kChunkBytes + swz(row, unit), b[0], b[1], b[2], b[3]);
       };
       uint32_t vb[kAhead + 1][4];
 #pragma unroll
@@ -457,11 +508,11 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         mma_bf16_16816(acc[2 * np], pa, b[0], b[1]);
         mma_bf16_16816(acc[2 * np + 1], pa, b[2], b[3]);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[stage[j]]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s.empty[stage]);
 
-    if (f + 1 == cur.seg_end) {
+    if (f + NP == cur.seg_end) {
       // ---------------- finish this sequence's segment ----------------
       float lt[2];
 #pragma unroll
@@ -496,6 +547,214 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         }
       }
       reset();
+    }
+  };
+
+  if constexpr (kShared) {
+    int it = 0;  // page groups so far (parity of the exchange buffer)
+    for (int i = 0; i < n_pages; ++it) {
+      const int f = sp.begin + i;
+      if (f >= t.prefix[cur.b + 1]) {
+        cur.advance(p, t, sp, f);
+        load_q();
+        prefetch_next_q();
+      }
+      if (i + 1 < n_pages && f + 1 < cur.seg_end) {  // two pages of this segment
+        page_group(std::integral_constant<int, 2>{}, i, f, it);
+        i += 2;
+      } else {
+        page_group(std::integral_constant<int, 1>{}, i, f, it);
+        i += 1;
+      }
+    }
+  } else {
+    for (int i = 0; i < n_pages; ++i) {
+      const int f = sp.begin + i;
+      if (f >= t.prefix[cur.b + 1]) {
+        cur.advance(p, t, sp, f);
+        load_q();
+        prefetch_next_q();
+      }
+      const int stage = i % kNS;
+      const int pos0 = cur.pos0(t, f);
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s.full[stage], (i / kNS) & 1));
+        if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      }
+      const uint32_t vst = smem_addr(s.v[stage]);
+      const uint32_t kst = smem_addr(s.k[stage]);
+
+      // ---- partial S over this warp's dims: two n-tiles of 8 positions; even
+      //      and odd k-steps accumulate separately (two chains of 4 MMAs) ----
+      //      The K fragments are read kAhead k-steps before their MMAs.
+      float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+      auto k_frag = [&](int ks, uint32_t (&b)[4]) {
+        ldmatrix_x4(kst + kstep_offset(ks), b[0], b[1], b[2], b[3]);
+      };
+      uint32_t kb[kAhead + 1][4];
+#pragma unroll
+      for (int ks = 0; ks < kAhead; ++ks) k_frag(ks, kb[ks]);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        if (ks + kAhead < 8) k_frag(ks + kAhead, kb[(ks + kAhead) % (kAhead + 1)]);
+        const uint32_t (&b)[4] = kb[ks % (kAhead + 1)];
+        float (&s0)[4] = (ks & 1) ? so[0] : se[0];
+        float (&s1)[4] = (ks & 1) ? so[1] : se[1];
+        mma_bf16_16816(s0, qa_reg[ks], b[0], b[1]);
+        mma_bf16_16816(s1, qa_reg[ks], b[2], b[3]);
+      }
+      }
+
+      // ---- sum the four partials in a fixed order ----
+      const int buf = i & 1;
+      s.xs[buf][warp][0][lane] =
+          make_float4(se[0][0] + so[0][0], se[0][1] + so[0][1], se[0][2] + so[0][2], se[0][3] + so[0][3]);
+      s.xs[buf][warp][1][lane] =
+          make_float4(se[1][0] + so[1][0], se[1][1] + so[1][1], se[1][2] + so[1][2], se[1][3] + so[1][3]);
+      named_barrier_sync(1, kConsumerWarps * 32);
+      float sc[2][4];
+      {
+        float4 a0 = s.xs[buf][0][0][lane], a1 = s.xs[buf][0][1][lane];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) {
+          const float4 c0 = s.xs[buf][w][0][lane], c1 = s.xs[buf][w][1][lane];
+          a0.x += c0.x; a0.y += c0.y; a0.z += c0.z; a0.w += c0.w;
+          a1.x += c1.x; a1.y += c1.y; a1.z += c1.z; a1.w += c1.w;
+        }
+        sc[0][0] = a0.x; sc[0][1] = a0.y; sc[0][2] = a0.z; sc[0][3] = a0.w;
+        sc[1][0] = a1.x; sc[1][1] = a1.y; sc[1][2] = a1.z; sc[1][3] = a1.w;
+      }
+
+      // ---- masked online softmax (log2 units) ----
+      // sc[nt][e]: head g + 8*(e>>1), position pos0 + 8*nt + 2*tq + (e&1).
+      // Positions outside [lo, L) get -inf (pages inside the range skip the
+      // test); the factor log2(e) is applied inside the exponent.
+      if (pos0 < cur.lo || pos0 + kPage > cur.L) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pos = pos0 + 8 * nt + 2 * tq + (e & 1);
+            if (pos < cur.lo || pos >= cur.L) sc[nt][e] = -INFINITY;
+          }
+      }
+      float mx[2];
+      mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      // The running max of a row changes only when some score exceeds it, which
+      // after a sequence's first pages is rare: one vote decides whether the
+      // row maxima over the four lanes that share a row are needed at all.
+      // Tracking the exact max keeps the largest weight at exactly 1, so the
+      // dominant term of P carries no bf16 rounding.
+      float scale[2] = {1.f, 1.f};
+      if (__any_sync(0xffffffffu, mx[0] * kLog2e > m[0] || mx[1] * kLog2e > m[1])) {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+          mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+          const float m_new = fmaxf(m[rr], mx[rr] * kLog2e);
+          scale[rr] = m_new == m[rr] ? 1.f : ex2_approx(m[rr] - m_new);  // 0 on the first visible page
+          m[rr] = m_new;
+        }
+      }
+      float m_use[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) m_use[rr] = m[rr] == -INFINITY ? 0.f : m[rr];
+      float pr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[nt][e] = ex2_approx(fmaf(sc[nt][e], kLog2e, -m_use[e >> 1]));
+      l[0] = l[0] * scale[0] + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+      l[1] = l[1] * scale[1] + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+      // rescale only when some row's running max moved (multiplying by 1 is exact)
+      if (__any_sync(0xffffffffu, scale[0] != 1.f || scale[1] != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          acc[n][0] *= scale[0];
+          acc[n][1] *= scale[0];
+          acc[n][2] *= scale[1];
+          acc[n][3] *= scale[1];
+        }
+      }
+      // P as the A fragment of one k16 step (k = the page's 16 positions)
+      const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
+                              pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
+
+      // ---- zero V rows outside [lo, L) in this warp's two chunks ----
+      if (pos0 < cur.lo || pos0 + kPage > cur.L) {
+#pragma unroll 1
+        for (int rr = 0; rr < kPage; ++rr) {
+          const int pos = pos0 + rr;
+          if ((pos < cur.lo || pos >= cur.L) && lane < 16) {
+            const int ch = 2 * warp + (lane >> 3);
+            st_shared_v4(vst + ch * kChunkBytes + rr * 128 + (lane & 7) * 16, make_uint4(0, 0, 0, 0));
+          }
+        }
+        fence_proxy_async_smem();  // before TMA rewrites this stage
+        __syncwarp();
+      }
+
+      // ---- O += P V over this warp's 128 dims ----
+      {
+        auto v_frag = [&](int np, uint32_t (&b)[4]) {
+          const int ch = 2 * warp + (np >> 2);
+          const int row = ((mi & 1) << 3) + lr;
+          const int unit = 2 * (np & 3) + (mi >> 1);
+          ldmatrix_x4_trans(vst + ch * kChunkBytes + swz(row, unit), b[0], b[1], b[2], b[3]);
+        };
+        uint32_t vb[kAhead + 1][4];
+#pragma unroll
+        for (int np = 0; np < kAhead; ++np) v_frag(np, vb[np]);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+          if (np + kAhead < 8) v_frag(np + kAhead, vb[(np + kAhead) % (kAhead + 1)]);
+          const uint32_t (&b)[4] = vb[np % (kAhead + 1)];
+          mma_bf16_16816(acc[2 * np], pa, b[0], b[1]);
+          mma_bf16_16816(acc[2 * np + 1], pa, b[2], b[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[stage]);
+
+      if (f + 1 == cur.seg_end) {
+        // ---------------- finish this sequence's segment ----------------
+        float lt[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          lt[rr] = l[rr] + __shfl_xor_sync(0xffffffffu, l[rr], 1);
+          lt[rr] += __shfl_xor_sync(0xffffffffu, lt[rr], 2);
+        }
+        if (cur.whole(t, sp)) {
+          const size_t row0 = static_cast<size_t>(cur.b) * kHq + g;
+          const float inv0 = lt[0] > 0.f ? 1.f / lt[0] : 0.f;
+          const float inv1 = lt[1] > 0.f ? 1.f / lt[1] : 0.f;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            const int d = dim0 + 8 * n + 2 * tq;
+            store_out2(p, row0 * kD + d, acc[n][0] * inv0, acc[n][1] * inv0);
+            store_out2(p, (row0 + 8) * kD + d, acc[n][2] * inv1, acc[n][3] * inv1);
+          }
+        } else if ((static_cast<int64_t>(gb) + cur.b + 1) * kHq > p.part_rows) {
+          if (lane == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: slot beyond the workspace
+        } else {
+          const size_t slot0 = (static_cast<size_t>(gb) + cur.b) * kHq + g;
+          const size_t slot1 = slot0 + 8;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            const int d = dim0 + 8 * n + 2 * tq;
+            *reinterpret_cast<float2*>(p.part_o + slot0 * kD + d) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2*>(p.part_o + slot1 * kD + d) = make_float2(acc[n][2], acc[n][3]);
+          }
+          if (warp == 0 && tq == 0) {
+            p.part_ml[slot0] = make_float2(m[0], lt[0]);
+            p.part_ml[slot1] = make_float2(m[1], lt[1]);
+          }
+        }
+        reset();
+      }
     }
   }
 }
