@@ -61,10 +61,10 @@ NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 # only while the sources still hash to that value (profiles/ has the
 # captures and their commands).
 NCU_TRAFFIC = {
-    ("global", "2"): (65_354_752, "eea333647ca0b4ec"),
-    ("global", "4b"): (2_153_049_856, "eea333647ca0b4ec"),
-    ("global_shared", "2"): (32_063_488, "eea333647ca0b4ec"),
-    ("global_shared", "4b"): (1_077_322_496, "eea333647ca0b4ec"),
+    ("global", "2"): (65_204_480, "015bd8087f2f0392"),
+    ("global", "4b"): (2_152_527_104, "015bd8087f2f0392"),
+    ("global_shared", "2"): (32_076_288, "015bd8087f2f0392"),
+    ("global_shared", "4b"): (1_077_165_312, "015bd8087f2f0392"),
     ("sliding", "3"): (2_186_832_384, "46bb46920450f09a"),
 }
 KERNEL_SOURCES = {
