@@ -34,7 +34,10 @@
 // in the rotated chunk 0 and its partner chunk 4 (pairs (j, j + 256)) a lane
 // holds both halves of each of its 8 pairs; in chunks 1-3 and 5-7 the key is
 // the bf16 product V * w_k.
-// The 8 angles per lane and page come from rope.cuh.
+// The 8 angles per lane and page come from rope.cuh.  Two consecutive pages
+// of a segment share one partial-S exchange and one softmax pass; the q
+// fragments, w_k and the RoPE frequencies live in shared memory (each lane
+// reads back only what it wrote) so that two pages fit in the registers.
 #pragma once
 
 #include <type_traits>
