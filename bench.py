@@ -61,11 +61,11 @@ NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 # only while the sources still hash to that value (profiles/ has the
 # captures and their commands).
 NCU_TRAFFIC = {
-    ("global", "2"): (65_204_480, "015bd8087f2f0392"),
-    ("global", "4b"): (2_152_527_104, "015bd8087f2f0392"),
-    ("global_shared", "2"): (32_076_288, "015bd8087f2f0392"),
-    ("global_shared", "4b"): (1_077_165_312, "015bd8087f2f0392"),
-    ("sliding", "3"): (2_186_832_384, "46bb46920450f09a"),
+    ("global", "2"): (65_204_480, "c4b886e54e6f3244"),
+    ("global", "4b"): (2_152_527_104, "c4b886e54e6f3244"),
+    ("global_shared", "2"): (32_076_288, "c4b886e54e6f3244"),
+    ("global_shared", "4b"): (1_077_165_312, "c4b886e54e6f3244"),
+    ("sliding", "3"): (2_186_832_384, "6f83cfc0ff1d0610"),
 }
 KERNEL_SOURCES = {
     "global": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
@@ -74,12 +74,20 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """C++ source without comments, trailing blanks or empty lines (a comment edit keeps the hash)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.split("\n") if ln.strip())
+
+
 def kernel_source_hash(kind):
     import hashlib
     m = hashlib.sha256()
     for f in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "paged_decode_attention_gb300", "csrc", f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(ROOT, "paged_decode_attention_gb300", "csrc", f)) as fh:
+            m.update(_code_only(fh.read()).encode())
     return m.hexdigest()[:16]
 
 

@@ -123,3 +123,9 @@ def test_recorded_traffic_tracks_the_kernel_sources():
         assert got in (None, nbytes)
         assert (got is not None) == (bench.kernel_source_hash(kind) == sha)
     assert bench.recorded_traffic("global", "no-such-workload") is None
+
+
+def test_source_hash_ignores_comments_only():
+    code = "int f(int x) {\n  return x + 1;  // one more\n}\n"
+    assert bench._code_only(code) == bench._code_only("/* header */\n" + code.replace("// one more", "// changed"))
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))
