@@ -502,26 +502,43 @@ def run_ours(args, rank, world, local_rank):
         shared["traffic"] = recorded_traffic("global_shared", args.config)
     # --- the step as the library's own one-launch object ---
     whole = time_whole_step(plans, n_sets, stream, status, max(3, min(args.steps, 200)))
+    whole_append = time_whole_step(plans, n_sets, stream, status, max(3, min(args.steps, 200)), with_append=True)
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the cache append" % int(status.item()))
 
-    res.update(per_type=per_type, append=append, prefill=prefill, shared=shared, whole_step=whole)
+    res.update(per_type=per_type, append=append, prefill=prefill, shared=shared, whole_step=whole,
+               whole_step_append=whole_append)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
                heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
                launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
     return res
 
 
-def time_whole_step(plans, n_sets, stream, status, steps):
+def time_whole_step(plans, n_sets, stream, status, steps, with_append=False):
     """The step's decode calls recorded into one pda.Step per input set and
     launched with one attn_step_launch per step (one CUDA graph of the step's
-    calls), `steps` launches back to back between CUDA events."""
+    calls), `steps` launches back to back between CUDA events.
+
+    with_append: each layer's cache append runs first, as in a real decode
+    step: it writes the token at position seq_len - 1 into the layer's pools
+    and the decode's q, which the decode then reads."""
     import torch
     import paged_decode_attention_gb300 as pda
+    from workloads import append_row_len, key_weight
     objs = []
+    gen = torch.Generator(device=stream.device)
+    gen.manual_seed(78)
+    w = {k: key_weight(D, 79 + D, device=stream.device) for k, D in (("sliding", 256), ("global", 512))}
+    keep = []
     for pl in plans:
         st = pda.Step()
         for c, ws, o in pl:
+            if with_append:
+                qkv = torch.randn((c.B, append_row_len(c.kind)), generator=gen, device=stream.device).to(torch.bfloat16)
+                positions = (c.seq_lens - 1).clamp(min=0).to(torch.int32)
+                keep.append((qkv, positions))
+                add_app = st.add_kv_append_sliding if c.kind == "sliding" else st.add_kv_append_global
+                add_app(qkv, w[c.kind], w[c.kind], c.block_table, positions, c.k_pool, c.v_pool, c.q, status=status)
             add = st.add_decode_sliding if c.kind == "sliding" else st.add_decode_global
             add(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window, max_seq_len=c.max_seq_len,
                 workspace=ws, status=status, num_splits=NUM_SPLITS)
@@ -537,6 +554,8 @@ def time_whole_step(plans, n_sets, stream, status, steps):
             objs[i % n_sets].launch(stream)
         e1.record(stream)
     e1.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the step launch" % int(status.item()))
     ms = e0.elapsed_time(e1) / steps
     calls = [c for c, _, _ in plans[0]]
     nbytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c in calls)
@@ -544,6 +563,11 @@ def time_whole_step(plans, n_sets, stream, status, steps):
            "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "launch": "one attn_step_launch (one CUDA graph of the step's calls) per step, %d steps back to back"
                      % steps}
+    if with_append:
+        app = sum(append_bytes(c.kind, c.B) for c in calls)
+        out["append_bytes_per_step"] = app
+        out["value_with_append_bytes"] = round((nbytes + app) / (ms * 1e-3) / 1e9, 2)
+        out["note"] = "value counts the decode bytes only; each layer's append precedes its decode in the graph"
     for st in objs:
         st.close()
     return out
@@ -978,6 +1002,9 @@ def main(argv=None):
         line["append"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4)) for k, v in r0["append"].items()}
     if r0.get("whole_step"):
         line["whole_step_launch"] = dict(r0["whole_step"], frac_of_peak=round(r0["whole_step"]["value"] / peak, 4))
+    if r0.get("whole_step_append"):
+        line["whole_step_launch_with_append"] = dict(r0["whole_step_append"],
+                                                     frac_of_peak=round(r0["whole_step_append"]["value"] / peak, 4))
     if r0.get("shared"):
         line["global_values_only_cache"] = dict(r0["shared"], frac_of_peak=round(r0["shared"]["value"] / peak, 4))
     line["e2e"] = r0["e2e"]

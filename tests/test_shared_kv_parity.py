@@ -209,3 +209,16 @@ def test_long_context_full_size(cuda_lib, variant):
     want = _oracle_rows_shared(case, w, rows)
     got = o.reshape(-1, case.D)[rows].double().cpu().numpy()
     assert_within_tolerance(got, want, "values-only long context %s" % variant)
+
+
+@pytest.mark.slow
+def test_decode_step_mix_global_layer_full_size(cuda_lib):
+    # a global layer of the 48-layer step: B = 64, lengths log-uniform in [16, 262144]
+    case = config_case(5, device=DEV, layer=5)
+    w = key_weight(512, 13)
+    o, st = run(case, w)
+    assert st == 0
+    rows = sample_rows(case, 48, 3)
+    want = _oracle_rows_shared(case, w, rows)
+    got = o.reshape(-1, case.D)[rows].double().cpu().numpy()
+    assert_within_tolerance(got, want, "values-only step mix")

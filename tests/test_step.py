@@ -139,3 +139,30 @@ def test_step_rejects_calls_after_finalize(cuda_lib):
         pda.Step().add_decode_global(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
                                      workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
     step.close()
+
+
+def test_step_with_a_values_only_global_layer(cuda_lib):
+    """A global layer over a values-only cache inside a step: the append writes V only and the
+    decode rebuilds the keys; both match the direct calls bitwise and the oracle's append and decode."""
+    positions = [0, 16, 333, 1023, 1024, 2500]
+    a = make_append_case("global", positions, seed=1340, full_cache=True).to(DEV)
+    b = make_append_case("global", positions, seed=1340, full_cache=True).to(DEV)
+    seq_lens = torch.tensor([p + 1 for p in positions], dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    step = pda.Step()
+    q = step.add_kv_append_global(a.qkv, a.w_q, a.w_k, a.cache.block_table, a.positions, None, a.cache.v_pool,
+                                  status=status)
+    o = step.add_decode_global_shared(q, a.cache.v_pool, a.w_k, a.cache.block_table, seq_lens,
+                                      out_dtype=torch.float32, status=status)
+    step.finalize()
+    step.launch()
+    qb = pda.attn_kv_append_global(b.qkv, b.w_q, b.w_k, b.cache.block_table, b.positions, None, b.cache.v_pool)
+    ob = pda.attn_decode_global_shared(qb, b.cache.v_pool, b.w_k, b.cache.block_table, seq_lens,
+                                       out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(q, qb) and torch.equal(a.cache.v_pool, b.cache.v_pool) and torch.equal(o, ob)
+    want = oracle.decode_paged_shared(bits(q), bits(a.cache.v_pool), bits(a.w_k), a.cache.block_table.cpu().numpy(),
+                                      seq_lens.cpu().numpy(), 0, 1.0e6, 64)
+    assert_within_tolerance(o.double().cpu().numpy(), want, "step values-only layer")
+    step.close()
