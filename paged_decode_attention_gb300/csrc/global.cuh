@@ -9,10 +9,11 @@
 //
 // Grid (grid_x): block g streams its span of the flattened visible pages
 // (balanced schedule, common.cuh):
-//   * warp 4 (producer) issues, per page, 8 TMA tensor copies for K and 8
-//     for V: boxes of 16 rows x 64 dims (2 KB) of the pool viewed as
-//     [num_pages*16 rows, 512], written with the 128-byte swizzle so that the
-//     ldmatrix reads below are free of bank conflicts;
+//   * warp 4 (producer) issues, per page, one 3-D TMA tensor copy for K and
+//     one for V: the pool viewed as [8 chunks][num_pages*16 rows][64 dims],
+//     a box of 8 x 16 x 64 (16 KB) that lands as eight [16 rows][64 dims]
+//     tiles with the 128-byte swizzle, so that the ldmatrix reads below are
+//     free of bank conflicts;
 //   * warps 0..3 (consumers) each own 128 of the 512 dims: a warp computes
 //     its partial S over its dims, the four partials are summed through
 //     shared memory in a fixed order (so every warp holds the bitwise-same
