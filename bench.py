@@ -61,10 +61,10 @@ NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 # only while the sources still hash to that value (profiles/ has the
 # captures and their commands).
 NCU_TRAFFIC = {
-    ("global", "2"): (65_204_480, "c4b886e54e6f3244"),
-    ("global", "4b"): (2_152_527_104, "c4b886e54e6f3244"),
-    ("global_shared", "2"): (32_076_288, "c4b886e54e6f3244"),
-    ("global_shared", "4b"): (1_077_165_312, "c4b886e54e6f3244"),
+    ("global", "2"): (65_291_776, "8cb53a1d861c2d40"),
+    ("global", "4b"): (2_152_939_008, "8cb53a1d861c2d40"),
+    ("global_shared", "2"): (32_074_752, "8cb53a1d861c2d40"),
+    ("global_shared", "4b"): (1_077_190_400, "8cb53a1d861c2d40"),
     ("sliding", "3"): (2_186_832_384, "6f83cfc0ff1d0610"),
 }
 KERNEL_SOURCES = {
