@@ -216,3 +216,19 @@ def test_step_append_validation(lib):
         assert lib.attn_step_num_calls(h) == 1 and lib.attn_step_num_kernels(h) == 1
     finally:
         lib.attn_step_destroy(h)
+
+
+def test_step_binding_refuses_cpu_tensors_and_empty_finalize(lib):
+    import torch
+    step = pda.Step()
+    q = torch.zeros(1, 16, 512, dtype=torch.bfloat16)
+    pool = torch.zeros(2, 16, 1, 512, dtype=torch.bfloat16)
+    bt = torch.zeros(1, 1, dtype=torch.int32)
+    sl = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        step.add_decode_global(q, pool, pool, bt, sl)
+    assert step.num_calls == 0
+    with pytest.raises(pda.AttnDecodeError):
+        step.finalize()
+    step.close()
+    step.close()  # idempotent
