@@ -2,11 +2,14 @@
 """Decode-attention benchmark on GB300: achieved HBM GB/s and attention calls/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config 1|2|3|4|4b|5]
+                    [--config 1|2|3|4|4b|5] [--sub 2,3,4,4b | --no-sub]
 
 A step is one decode-attention call (for workload 5: one whole decode step,
 40 sliding + 8 global layer calls) over synthetic inputs already resident in
-HBM.  The default workload is the global decode at B=8, seq_lens U[1, 8192].
+HBM.  The default workload is workload 5, the Gemma-4-12B decode step at
+B=64 with seq_lens log-uniform in [16, 262144], the largest configuration
+that fits one GPU; its JSON line also carries one object per target
+workload (2, 3, 4a and 4b), each timed with CUDA events the same way.
 Throughput counts algorithmic bytes only: the visible K and V rows, q and o.
 
 Inputs larger than L2 are used as they are; smaller ones are rotated over
@@ -41,6 +44,13 @@ METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and attention cal
 UNIT = "GB/s"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+# NVIDIA's nominal HBM3e bandwidth of a GB300.  The measured peak above is a
+# device-to-device copy, which a pure read stream can exceed; fractions are
+# also given against this figure (ncu's DRAM peak on this GPU agrees with it:
+# 6.87 TB/s of DRAM traffic reads as 87 % of peak).
+NOMINAL_DRAM_GBS = 7900.0
+# Workloads timed beside the headline (workload 5): the other targets.
+DEFAULT_SUBS = ["2", "3", "4", "4b"]
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # Multi-query (prefill) workloads timed beside the decode: new tokens whose
@@ -71,6 +81,8 @@ KERNEL_SOURCES = {
     "global": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
     "global_shared": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
     "sliding": ["sliding.cuh", "common.cuh", "ptx.cuh"],
+    # a whole decode step: both decode kernels and the combine
+    "step": ["sliding.cuh", "global.cuh", "combine.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
 }
 
 
@@ -227,7 +239,7 @@ class ClockSampler:
         self.gpu = gpu_id
         self.proc = None
         self.lines = []
-        self.t0 = self.t1 = None
+        self.windows = {}  # key -> [t0, t1]: the timed regions (None: the main one)
 
     def start(self):
         try:
@@ -245,11 +257,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def mark(self, begin):
-        if begin:
-            self.t0 = time.time()
-        else:
-            self.t1 = time.time()
+    def mark(self, begin, key=None):
+        w = self.windows.setdefault(key, [None, None])
+        w[0 if begin else 1] = time.time()
 
     def stop(self):
         time.sleep(0.25)
@@ -259,9 +269,9 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-        return self.summary()
+            self.proc = None
 
-    def summary(self):
+    def summary(self, key=None):
         rows = []
         for t, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -270,8 +280,9 @@ class ClockSampler:
             rows.append((t, parts))
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
-        lo = (self.t0 or 0) - 0.15
-        hi = (self.t1 or time.time()) + 0.15
+        t0, t1 = self.windows.get(key, [None, None])
+        lo = (t0 or 0) - 0.15
+        hi = (t1 or time.time()) + 0.15
         inside = [p for t, p in rows if lo <= t <= hi] or [min(rows, key=lambda r: abs(r[0] - lo))[1]]
 
         def num(x):
@@ -315,24 +326,17 @@ def workload_name(cfg):
 # our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, rank, world, local_rank):
+def prepare_workload(cfg, dev):
+    """The calls of one step of workload `cfg` and their per-call buffers, over
+    enough rotating input sets that consecutive reuse of a set is separated by
+    more than 3x L2 (one set when a step's cache alone exceeds that)."""
     import torch
     import paged_decode_attention_gb300 as pda
-    from workloads import config_case, N_LAYERS
-
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    pda.load()
-    stream = torch.cuda.Stream(device=dev)
-
-    # --- inputs: one or more rotating sets of the step's calls ---
-    calls0 = workload_calls(args.config, dev)
+    calls0 = workload_calls(cfg, dev)
     step_bytes = sum(algorithmic_bytes(c.kind, c.seq_lens_host, c.window) for c in calls0)
     kv_bytes = sum(c.k_pool.numel() * 2 * 2 for c in calls0)
     n_sets = rotation_count(kv_bytes)
-    sets = [calls0] + [workload_calls(args.config, dev, seed_offset=100000 * k) for k in range(1, n_sets)]
-
-    # per-call buffers: outputs, workspaces, status
+    sets = [calls0] + [workload_calls(cfg, dev, seed_offset=100000 * k) for k in range(1, n_sets)]
     plans = []
     for cs in sets:
         pl = []
@@ -343,14 +347,136 @@ def run_ours(args, rank, world, local_rank):
             o = torch.empty((c.B, c.Hq, c.D), dtype=torch.bfloat16, device=dev)
             pl.append((c, ws, o))
         plans.append(pl)
+    return dict(calls0=calls0, plans=plans, n_sets=n_sets, step_bytes=step_bytes, kv_bytes=kv_bytes)
+
+
+def launch_calls(pl, status, stream, idx=None):
+    """The decode calls of one step (or those listed in idx), on `stream`."""
+    import paged_decode_attention_gb300 as pda
+    for j, (c, ws, o) in enumerate(pl):
+        if idx is not None and j not in idx:
+            continue
+        fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
+        fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
+           max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
+           num_splits=NUM_SPLITS)
+
+
+def time_graph(launch_i, n, rounds, stream, use_graph=True):
+    """ms per launch_i(i) call: a CUDA graph of launch_i(0..n-1) back to back,
+    replayed `rounds` times between CUDA events on `stream` after a warm replay
+    (direct calls with use_graph=False)."""
+    import torch
+    g = None
+    if use_graph:
+        with torch.cuda.stream(stream):
+            for i in range(min(n, 2)):
+                launch_i(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                launch_i(i)
+
+    def one_round():
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(n):
+                launch_i(i)
+    with torch.cuda.stream(stream):
+        one_round()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(rounds):
+            one_round()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / (rounds * n)
+    del g
+    return ms
+
+
+def hbm_roofline(nbytes, ms, peak, peak_src, kernel, traffic=None):
+    """The roofline object of an HBM-bound measurement: algorithmic bytes over
+    the event-timed duration, against the measured copy peak and, beside it,
+    NVIDIA's nominal DRAM peak (a read stream may exceed the copy figure)."""
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+           "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic_bytes": nbytes,
+           "peak_source": peak_src, "kernel": kernel,
+           "frac_of_dram_peak": round(achieved / NOMINAL_DRAM_GBS, 4),
+           "dram_peak": NOMINAL_DRAM_GBS, "dram_peak_source": "nominal HBM3e (NVIDIA)"}
+    if achieved > peak:
+        out["note"] = ("above the copy-based peak: a pure read stream exceeds a device-to-device copy; "
+                       "frac_of_dram_peak is the fraction of the nominal DRAM bandwidth")
+    return out
+
+
+def measure_sub(cfg, dev, stream, status, args, peak, peak_src, sampler=None):
+    """One target workload timed on its own: ms per call from a CUDA graph of
+    back-to-back calls over the rotating input sets, its HBM roofline, and for
+    global layers the values-only cache and (workload 2) the library's
+    one-launch step object on the same calls."""
+    import torch
+    W = prepare_workload(cfg, dev)
+    plans, n_sets, calls0 = W["plans"], W["n_sets"], W["calls0"]
+    n = max(8, 2 * n_sets)
+    est_ms = W["step_bytes"] / (peak * 1e6)
+    rounds = max(3, min(200, int(math.ceil(50.0 / max(est_ms * n, 1e-3)))))
+    if sampler:
+        sampler.mark(True, key=cfg)
+    ms = time_graph(lambda i: launch_calls(plans[i % n_sets], status, stream), n, rounds, stream,
+                    use_graph=not args.no_graph)
+    if sampler:
+        sampler.mark(False, key=cfg)
+    kind = calls0[0].kind
+    kernels = "%s decode + combine (2 launches per call, timed together)" % kind
+    out = {"workload": workload_name(cfg), "calls_per_step": len(calls0), "ms_per_call": round(ms, 6),
+           "calls_per_s": round(1e3 / ms, 1), "value": round(W["step_bytes"] / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+           "roofline": hbm_roofline(W["step_bytes"], ms, peak, peak_src, kernels,
+                                    recorded_traffic(kind, cfg)),
+           "l2": ("inputs %.0f MB > L2; 1 set" % (W["kv_bytes"] / 1e6) if n_sets == 1 else
+                  "rotating %d input sets (%.0f MB in all) so every call reads HBM" % (n_sets, n_sets * W["kv_bytes"] / 1e6)),
+           "launch": "%d calls back to back in one CUDA graph, %d replays, CUDA events" % (n, rounds)}
+    if kind == "global":
+        sh = time_global_shared(plans, n_sets, stream, status, dev)
+        sh["traffic"] = recorded_traffic("global_shared", cfg)
+        sh["frac_of_peak"] = round(sh["value"] / peak, 4)
+        sh["frac_of_dram_peak"] = round(sh["value"] / NOMINAL_DRAM_GBS, 4)
+        out["values_only_cache"] = sh
+    if cfg == "2":
+        ws = time_whole_step(plans, n_sets, stream, status, max(50, min(args.steps, 400)))
+        ws["frac_of_peak"] = round(ws["value"] / peak, 4)
+        ws["graph_replayed_us_per_step"] = round(ms * 1e3, 3)
+        out["whole_step_launch"] = ws
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in workload %s" % (int(status.item()), cfg))
+    del W, plans, calls0
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_decode_attention_gb300 as pda
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pda.load()
+    stream = torch.cuda.Stream(device=dev)
+
+    # --- inputs: one or more rotating sets of the step's calls ---
+    W = prepare_workload(args.config, dev)
+    calls0, plans, n_sets = W["calls0"], W["plans"], W["n_sets"]
+    step_bytes, kv_bytes = W["step_bytes"], W["kv_bytes"]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def launch(pl):
-        for c, ws, o in pl:
-            fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
-            fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
-               max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
-               num_splits=NUM_SPLITS)
+        launch_calls(pl, status, stream)
 
     # every call launches the decode kernel and its combine kernel
     kernels_per_call = [2 for _ in calls0]
@@ -405,7 +531,6 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier(world)
     ms = ev0.elapsed_time(ev1)
-    clocks = sampler.stop() if sampler else None
     st = int(status.item())
     if st != 0:
         raise RuntimeError("device status %d during the benchmark" % st)
@@ -417,37 +542,9 @@ def run_ours(args, rank, world, local_rank):
     heavy = max(range(len(calls0)), key=lambda j: algorithmic_bytes(calls0[j].kind, calls0[j].seq_lens_host,
                                                                     calls0[j].window))
     reps = 2 * n_sets if n_sets > 1 else 8
-
-    def launch_heavy(i):
-        c, ws, o = plans[i % n_sets][heavy]
-        fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
-        fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
-           max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
-           num_splits=NUM_SPLITS)
-
-    if args.no_graph:
-        heavy_step = launch_heavy
-        rounds = max(8, min(200, args.steps))
-    else:
-        hg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(hg, stream=stream):
-            for i in range(reps):
-                launch_heavy(i)
-        heavy_step = lambda i: hg.replay()  # noqa: E731
-        rounds = max(3, min(50, args.steps // reps + 1))
-    with torch.cuda.stream(stream):
-        for i in range(2):
-            heavy_step(i)
-    stream.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(rounds):
-            heavy_step(i)
-        e1.record(stream)
-    e1.synchronize()
-    heavy_ms = e0.elapsed_time(e1) / (rounds * (1 if args.no_graph else reps))
+    rounds = max(8, min(200, args.steps)) if args.no_graph else max(3, min(50, args.steps // reps + 1))
+    heavy_ms = time_graph(lambda i: launch_calls(plans[i % n_sets], status, stream, idx=(heavy,)), reps, rounds,
+                          stream, use_graph=not args.no_graph)
     hc = calls0[heavy]
     heavy_bytes = algorithmic_bytes(hc.kind, hc.seq_lens_host, hc.window)
 
@@ -456,34 +553,9 @@ def run_ours(args, rank, world, local_rank):
     kinds = sorted(set(c.kind for c in calls0))
     if len(kinds) > 1:
         for kind in kinds:
-            idx = [j for j, c in enumerate(calls0) if c.kind == kind]
-
-            def launch_kind(i, idx=idx):
-                for j in idx:
-                    c, ws, o = plans[i % n_sets][j]
-                    fn = pda.attn_decode_sliding if c.kind == "sliding" else pda.attn_decode_global
-                    fn(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, o, window=c.window,
-                       max_seq_len=c.max_seq_len, workspace=ws, status=status, stream=stream,
-                       num_splits=NUM_SPLITS)
-            kg = None
-            if not args.no_graph:
-                kg = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(kg, stream=stream):
-                    launch_kind(0)
-            kind_step = (lambda i: kg.replay()) if kg is not None else launch_kind  # noqa: E731
-            with torch.cuda.stream(stream):
-                kind_step(0)
-            stream.synchronize()
-            k0 = torch.cuda.Event(enable_timing=True)
-            k1 = torch.cuda.Event(enable_timing=True)
-            krounds = 5
-            with torch.cuda.stream(stream):
-                k0.record(stream)
-                for i in range(krounds):
-                    kind_step(i)
-                k1.record(stream)
-            k1.synchronize()
-            kms = k0.elapsed_time(k1) / krounds
+            idx = tuple(j for j, c in enumerate(calls0) if c.kind == kind)
+            kms = time_graph(lambda i, idx=idx: launch_calls(plans[i % n_sets], status, stream, idx=idx), 1, 5,
+                             stream, use_graph=not args.no_graph)
             kbytes = sum(algorithmic_bytes(calls0[j].kind, calls0[j].seq_lens_host, calls0[j].window) for j in idx)
             per_type[kind] = {"calls_per_step": len(idx), "ms_per_step": round(kms, 6),
                               "value": round(kbytes / (kms * 1e-3) / 1e9, 2), "unit": UNIT}
@@ -509,8 +581,25 @@ def run_ours(args, rank, world, local_rank):
     res.update(per_type=per_type, append=append, prefill=prefill, shared=shared, whole_step=whole,
                whole_step_append=whole_append)
     res.update(heavy_ms=heavy_ms, heavy_bytes=heavy_bytes, heavy_kind=hc.kind,
-               heavy_kernels=kernels_per_call[heavy], clocks=clocks, e2e=e2e, n_sets=n_sets,
-               launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes)
+               heavy_kernels=kernels_per_call[heavy], e2e=e2e, n_sets=n_sets,
+               launches_per_step=sum(kernels_per_call), kv_bytes=kv_bytes,
+               timed_ms_per_step=ms / args.steps)
+
+    # --- the other target workloads, one at a time (rank 0 reports them) ---
+    del W, plans, calls0
+    torch.cuda.empty_cache()
+    subs = {}
+    for cfg in args.sub:
+        if cfg == args.config:
+            continue
+        subs[cfg] = measure_sub(cfg, dev, stream, status, args, *load_peaks(), sampler=sampler)
+    res["subs"] = subs
+    res["clocks"] = None
+    if sampler:
+        sampler.stop()
+        res["clocks"] = sampler.summary()
+        for cfg, d in subs.items():
+            d["clocks"] = sampler.summary(key=cfg)
     return res
 
 
@@ -942,10 +1031,14 @@ def gather_results(res, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4b", "5"])
+    ap.add_argument("--config", default="5", choices=["1", "2", "3", "4", "4b", "5"])
+    ap.add_argument("--sub", default=None,
+                    help="comma-separated workloads timed beside the headline (default with --config 5: "
+                         "2,3,4,4b; otherwise none)")
+    ap.add_argument("--no-sub", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-graph", action="store_true", help="launch every call directly (no CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill timing")
@@ -956,6 +1049,15 @@ def main(argv=None):
     NUM_SPLITS = args.num_splits
     if args.warmup < 3:
         args.warmup = 3
+    if args.no_sub:
+        args.sub = []
+    elif args.sub is None:
+        args.sub = list(DEFAULT_SUBS) if args.config == "5" else []
+    else:
+        args.sub = [s for s in args.sub.split(",") if s]
+        bad = [s for s in args.sub if s not in ("1", "2", "3", "4", "4b", "5")]
+        if bad:
+            ap.error("unknown workload(s) in --sub: %s" % ",".join(bad))
     rank, world, local_rank = init_dist()
 
     if args.impl == "reference":
@@ -969,9 +1071,20 @@ def main(argv=None):
     allres = gather_results(res, world)
     if rank != 0:
         return 0
+    print(json.dumps(make_line(args, allres)), flush=True)
+    return 0
+
+
+def sub_key(cfg):
+    """JSON key of a workload: 4a and 4b are the two variants of workload 4."""
+    return "4a" if cfg == "4" else cfg
+
+
+def make_line(args, allres):
+    """The JSON line of our arm from every rank's results (rank 0)."""
     peak, peak_src = load_peaks()
     r0 = allres[0]
-    config = {"workload": workload_name(args.config), "config_id": args.config,
+    config = {"workload": workload_name(args.config), "config_id": sub_key(args.config),
               "l2": ("inputs %.0f MB > L2; %d set(s)" % (r0["kv_bytes"] / 1e6, r0["n_sets"])
                      if r0["n_sets"] == 1 else
                      "rotating %d input sets (%.0f MB in all) so every step reads HBM"
@@ -979,19 +1092,32 @@ def main(argv=None):
               "launch": ("the K timed steps replayed as one CUDA graph" if not args.no_graph
                          else "direct calls")}
     line = aggregate(allres, args.steps, args.warmup, args.gpus, config)
-    achieved = r0["heavy_bytes"] / (r0["heavy_ms"] * 1e-3) / 1e9
-    line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(achieved / peak, 4),
-                        "traffic": recorded_traffic(r0["heavy_kind"], args.config),
-                        "algorithmic_bytes": r0["heavy_bytes"],
-                        "peak_source": peak_src,
-                        "kernel": "%s decode (%d launch%s per call, timed together)"
-                        % (r0["heavy_kind"], r0["heavy_kernels"], "es" if r0["heavy_kernels"] > 1 else "")}
+    # The roofline of the whole step: its algorithmic bytes over its event-timed
+    # duration on the launching stream (for a one-call workload, that call).
+    n_calls = r0["calls"] // args.steps
+    step_kernel = ("the whole decode step: %d decode calls (%s), each a decode kernel and its combine "
+                   "(%d launches), timed together" % (
+                       n_calls, ", ".join("%d %s" % (v["calls_per_step"], k) for k, v in sorted(r0["per_type"].items()))
+                       if r0.get("per_type") else r0["heavy_kind"], r0["launches_per_step"]))
+    line["roofline"] = hbm_roofline(r0["bytes"] / args.steps, r0["timed_ms_per_step"], peak, peak_src, step_kernel,
+                                    recorded_traffic("step", args.config) if n_calls > 1 else
+                                    recorded_traffic(r0["heavy_kind"], args.config))
+    # the heaviest call of the step on its own (the dominant kernel)
+    line["dominant_kernel"] = hbm_roofline(
+        r0["heavy_bytes"], r0["heavy_ms"], peak, peak_src,
+        "%s decode (%d launch%s per call, timed together)"
+        % (r0["heavy_kind"], r0["heavy_kernels"], "es" if r0["heavy_kernels"] > 1 else ""),
+        recorded_traffic(r0["heavy_kind"], args.config))
+    line["dominant_kernel"]["ms_per_call"] = round(r0["heavy_ms"], 6)
     line["hbm_frac_of_peak"] = round(line["value"] / peak, 4)
+    line["hbm_frac_of_dram_peak"] = round(line["value"] / NOMINAL_DRAM_GBS, 4)
     if r0.get("per_type"):
-        line["per_layer_type"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4))
+        line["per_layer_type"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4),
+                                          frac_of_dram_peak=round(v["value"] / NOMINAL_DRAM_GBS, 4))
                                   for k, v in r0["per_type"].items()}
     line["gpu_launches"] = r0["launches_per_step"] * args.steps
+    if r0.get("subs"):
+        line["workloads"] = {sub_key(k): v for k, v in r0["subs"].items()}
     if r0.get("prefill"):
         tpeak, tsrc = load_bf16_peak()
         line["prefill"] = {k: dict(v, roofline={"bound": "tensor", "achieved": v["value"], "peak": tpeak,
@@ -1001,7 +1127,8 @@ def main(argv=None):
     if r0.get("append"):
         line["append"] = {k: dict(v, frac_of_peak=round(v["value"] / peak, 4)) for k, v in r0["append"].items()}
     if r0.get("whole_step"):
-        line["whole_step_launch"] = dict(r0["whole_step"], frac_of_peak=round(r0["whole_step"]["value"] / peak, 4))
+        line["whole_step_launch"] = dict(r0["whole_step"], frac_of_peak=round(r0["whole_step"]["value"] / peak, 4),
+                                         graph_replayed_us_per_step=round(r0["timed_ms_per_step"] * 1e3, 3))
     if r0.get("whole_step_append"):
         line["whole_step_launch_with_append"] = dict(r0["whole_step_append"],
                                                      frac_of_peak=round(r0["whole_step_append"]["value"] / peak, 4))
@@ -1011,8 +1138,7 @@ def main(argv=None):
     line["clocks"] = r0["clocks"]
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config)
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 if __name__ == "__main__":

@@ -230,7 +230,9 @@ size_t attn_decode_workspace_size(int32_t kind, int32_t batch, int32_t max_seq_l
  *
  * - The first call on a device (with that device current) looks up the
  *   array's device address with cudaGetSymbolAddress; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept for the life of the
+ *   process, so this entry point must not be used on a device after
+ *   cudaDeviceReset on it (the array may then sit elsewhere).
  * - Calls whose plan needs more than 8 MiB of scratch are rejected with
  *   ATTN_ERR_UNSUPPORTED and a message; nothing is launched.  The automatic
  *   plan (num_splits = 0) fits for every batch up to ATTN_MAX_BATCH; large

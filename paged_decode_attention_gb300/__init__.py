@@ -40,8 +40,11 @@ EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_global_shar
            "attn_prefill_sliding", "attn_prefill_global",
            "attn_step_create", "attn_step_destroy", "attn_step_add_decode_sliding", "attn_step_add_decode_global",
            "attn_step_add_decode_global_shared", "attn_step_add_kv_append_sliding", "attn_step_add_kv_append_global",
-           "attn_step_num_calls", "attn_step_num_kernels", "attn_step_finalize", "attn_step_launch",
-           "attn_last_error", "attn_abi_version")
+           "attn_step_num_calls", "attn_step_num_kernels", "attn_step_set_launch_mode", "attn_step_launch_mode",
+           "attn_step_finalize", "attn_step_launch", "attn_last_error", "attn_abi_version")
+# attn_step launch modes (attn_step.h)
+STEP_LAUNCH_AUTO, STEP_LAUNCH_GRAPH, STEP_LAUNCH_DIRECT = 0, 1, 2
+STEP_LAUNCH_MODES = {"auto": STEP_LAUNCH_AUTO, "graph": STEP_LAUNCH_GRAPH, "direct": STEP_LAUNCH_DIRECT}
 APPEND_ROW = {KIND_SLIDING: 16 * 256 + 2 * 8 * 256, KIND_GLOBAL: 16 * 512 + 512}  # qkv row length
 
 
@@ -113,6 +116,10 @@ def load(path=None):
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = [c_step]
+    lib.attn_step_set_launch_mode.restype = c_i32
+    lib.attn_step_set_launch_mode.argtypes = [c_step, c_i32]
+    lib.attn_step_launch_mode.restype = c_i32
+    lib.attn_step_launch_mode.argtypes = [c_step]
     lib.attn_step_launch.restype = c_i32
     lib.attn_step_launch.argtypes = [c_step, c_vp]
     lib.attn_selftest_delayed_copy.restype = c_i32
@@ -256,15 +263,17 @@ class PreparedDecode:
 
 
 class Step:
-    """The attention calls of a decode step, recorded once and launched as one CUDA graph.
+    """The attention calls of a decode step, recorded once and replayed with one call.
 
     ``add_*`` take the arguments of the one-shot function of the same name
     (minus the stream), validate them at once and return the call's output
-    tensor (o, or q_out for the appends).  ``finalize()`` captures the calls,
-    in the order added, on the current CUDA device; ``launch(stream)`` then
-    enqueues the whole step with one C call and one graph launch.  The
-    tensors are used in place (the object keeps references to them); their
-    contents may change between launches.
+    tensor (o, or q_out for the appends).  ``finalize(mode)`` records the
+    calls' kernel launches, in the order added, on the current CUDA device;
+    ``launch(stream)`` then enqueues the whole step with one C call: one CUDA
+    graph launch (mode "graph"), or the recorded launches back to back (mode
+    "direct"); "auto" picks direct for steps of up to two calls.  The tensors
+    are used in place (the object keeps references to them); their contents
+    may change between launches.
     """
 
     def __init__(self):
@@ -328,12 +337,22 @@ class Step:
     def num_kernels(self):
         return self._lib.attn_step_num_kernels(self._h)
 
-    def finalize(self):
+    def finalize(self, mode="auto"):
+        """Record the step's launches; mode is "auto", "graph" or "direct"."""
+        if mode not in STEP_LAUNCH_MODES:
+            raise ValueError("mode must be one of %s" % ", ".join(STEP_LAUNCH_MODES))
         if self.device is None:
             raise AttnDecodeError(1, "no calls recorded")
+        self._check(self._lib.attn_step_set_launch_mode(self._h, STEP_LAUNCH_MODES[mode]))
         with torch.cuda.device(self.device):
             self._check(self._lib.attn_step_finalize(self._h))
         return self
+
+    @property
+    def launch_mode(self):
+        """"graph" or "direct" once finalized (before: the mode requested)."""
+        m = self._lib.attn_step_launch_mode(self._h)
+        return {v: k for k, v in STEP_LAUNCH_MODES.items()}.get(m)
 
     def launch(self, stream=None):
         """Enqueue the whole step on `stream` (default: the current stream of its device)."""

@@ -8,7 +8,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "attn_decode.h"
 #include "combine.cuh"
@@ -23,6 +25,12 @@ thread_local char g_err[512] = "";
 // Set while attn_step_add_* validates a call: run_decode and run_append
 // return after their host checks, before anything is encoded or launched.
 thread_local bool g_validate_only = false;
+// One kernel launch with all its arguments bound (tensor maps included),
+// ready to be enqueued on any stream of its device.
+using RecordedLaunch = std::function<cudaError_t(cudaStream_t)>;
+// Set while attn_step_finalize records a step: launch_pdl appends each launch
+// to this list instead of enqueuing it.
+thread_local std::vector<RecordedLaunch>* g_record = nullptr;
 
 int32_t fail(int32_t code, const char* fmt, ...) {
   va_list ap;
@@ -213,7 +221,7 @@ int32_t ensure_smem(Kernel kernel, size_t bytes, int dev, bool* done) {
 // results the same way, and lets the next kernel launch once it is merging.
 // Following anything but a kernel, the attribute has no effect.
 template <typename Kernel, typename... Args>
-cudaError_t launch_pdl(Kernel kernel, dim3 grid, int threads, size_t smem, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl_now(Kernel kernel, dim3 grid, int threads, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
@@ -225,6 +233,20 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, int threads, size_t smem, cudaS
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, int threads, size_t smem, cudaStream_t s, Args... args) {
+  if (g_record) {
+    try {
+      g_record->emplace_back(
+          [=](cudaStream_t st) { return launch_pdl_now(kernel, grid, threads, smem, st, args...); });
+    } catch (...) {  // no exception may leave the C ABI
+      return cudaErrorMemoryAllocation;
+    }
+    return cudaSuccess;
+  }
+  return launch_pdl_now(kernel, grid, threads, smem, s, args...);
 }
 
 // 2*pi as three floats for the additive range reduction (Cody and Waite):

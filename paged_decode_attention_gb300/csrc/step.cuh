@@ -1,7 +1,8 @@
 // step.cuh -- host side of include/attn_step.h: the attention calls of a
-// decode step recorded once, captured in order into one CUDA graph, and
-// replayed with one launch.  Included at the end of attn_decode.cu, whose
-// validation (g_validate_only) and error reporting it shares.
+// decode step recorded once and replayed with one call, either as one CUDA
+// graph or as the recorded kernel launches enqueued back to back.  Included
+// at the end of attn_decode.cu, whose validation (g_validate_only), launch
+// recording (g_record) and error reporting it shares.
 #pragma once
 
 #include <functional>
@@ -14,7 +15,11 @@
 struct attn_step {
   std::vector<std::function<int32_t(void*)>> calls;  // each enqueues one call on the given stream
   int32_t kernels = 0;
-  cudaGraph_t graph = nullptr;
+  int32_t mode = ATTN_STEP_LAUNCH_AUTO;  // as requested; resolved by attn_step_finalize
+  bool finalized = false;
+  int device = -1;                       // the device the step was finalized on
+  std::vector<RecordedLaunch> launches;  // every kernel launch of the step, arguments bound
+  cudaGraph_t graph = nullptr;           // ATTN_STEP_LAUNCH_GRAPH only
   cudaGraphExec_t exec = nullptr;
 };
 
@@ -24,7 +29,7 @@ namespace {
 int32_t record(attn_step* step, int32_t kernels, std::function<int32_t(void*)> call, const char* name) {
   g_err[0] = '\0';
   if (!step) return fail(ATTN_ERR_INVALID_ARG, "%s: null step", name);
-  if (step->exec) return fail(ATTN_ERR_INVALID_ARG, "%s: the step is already finalized", name);
+  if (step->finalized) return fail(ATTN_ERR_INVALID_ARG, "%s: the step is already finalized", name);
   g_validate_only = true;
   const int32_t st = call(nullptr);
   g_validate_only = false;
@@ -116,48 +121,100 @@ int32_t attn_step_num_calls(const attn_step* step) { return step ? static_cast<i
 
 int32_t attn_step_num_kernels(const attn_step* step) { return step ? step->kernels : 0; }
 
+int32_t attn_step_set_launch_mode(attn_step* step, int32_t mode) {
+  g_err[0] = '\0';
+  const char* name = "attn_step_set_launch_mode";
+  if (!step) return fail(ATTN_ERR_INVALID_ARG, "%s: null step", name);
+  if (step->finalized) return fail(ATTN_ERR_INVALID_ARG, "%s: the step is already finalized", name);
+  if (mode != ATTN_STEP_LAUNCH_AUTO && mode != ATTN_STEP_LAUNCH_GRAPH && mode != ATTN_STEP_LAUNCH_DIRECT)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: unknown mode %d", name, mode);
+  step->mode = mode;
+  return ATTN_OK;
+}
+
+int32_t attn_step_launch_mode(const attn_step* step) { return step ? step->mode : -1; }
+
 int32_t attn_step_finalize(attn_step* step) {
   g_err[0] = '\0';
   const char* name = "attn_step_finalize";
   if (!step) return fail(ATTN_ERR_INVALID_ARG, "%s: null step", name);
-  if (step->exec) return fail(ATTN_ERR_INVALID_ARG, "%s: already finalized", name);
+  if (step->finalized) return fail(ATTN_ERR_INVALID_ARG, "%s: already finalized", name);
   if (step->calls.empty()) return fail(ATTN_ERR_INVALID_ARG, "%s: no calls recorded", name);
-  cudaStream_t cs = nullptr;
-  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
-  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: cudaStreamCreate: %s", name, cudaGetErrorString(e));
-  // Relaxed: the calls may set kernel attributes the first time they run.
-  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
-  if (e != cudaSuccess) {
-    cudaStreamDestroy(cs);
-    return fail(ATTN_ERR_CUDA, "%s: cudaStreamBeginCapture: %s", name, cudaGetErrorString(e));
-  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: cudaGetDevice: %s", name, cudaGetErrorString(e));
+
+  // Run every call once more with its launches recorded instead of enqueued:
+  // host validation, tensor maps and kernel attributes are done here, once.
+  std::vector<RecordedLaunch> launches;
   int32_t st = ATTN_OK;
-  for (size_t i = 0; i < step->calls.size() && st == ATTN_OK; ++i) st = step->calls[i](cs);
+  g_record = &launches;
+  for (size_t i = 0; i < step->calls.size() && st == ATTN_OK; ++i) st = step->calls[i](nullptr);
+  g_record = nullptr;
+  if (st != ATTN_OK) return st;
+  if (launches.size() != static_cast<size_t>(step->kernels))
+    return fail(ATTN_ERR_INVALID_ARG, "%s: recorded %zu launches for %d kernels", name, launches.size(),
+                step->kernels);
+
+  int32_t mode = step->mode;
+  if (mode == ATTN_STEP_LAUNCH_AUTO)
+    mode = step->kernels <= ATTN_STEP_DIRECT_MAX_KERNELS ? ATTN_STEP_LAUNCH_DIRECT : ATTN_STEP_LAUNCH_GRAPH;
   cudaGraph_t graph = nullptr;
-  e = cudaStreamEndCapture(cs, &graph);
-  if (st == ATTN_OK && e != cudaSuccess)
-    st = fail(ATTN_ERR_CUDA, "%s: cudaStreamEndCapture: %s", name, cudaGetErrorString(e));
   cudaGraphExec_t exec = nullptr;
-  if (st == ATTN_OK) {
-    e = cudaGraphInstantiate(&exec, graph, 0);
-    if (e != cudaSuccess) st = fail(ATTN_ERR_CUDA, "%s: cudaGraphInstantiate: %s", name, cudaGetErrorString(e));
+  if (mode == ATTN_STEP_LAUNCH_GRAPH) {
+    cudaStream_t cs = nullptr;
+    e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: cudaStreamCreate: %s", name, cudaGetErrorString(e));
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) {
+      cudaStreamDestroy(cs);
+      return fail(ATTN_ERR_CUDA, "%s: cudaStreamBeginCapture: %s", name, cudaGetErrorString(e));
+    }
+    // The kernels keep their programmatic-serialisation attribute, so the
+    // graph holds programmatic edges between consecutive kernels.
+    for (size_t i = 0; i < launches.size() && st == ATTN_OK; ++i) {
+      const cudaError_t le = launches[i](cs);
+      if (le != cudaSuccess) st = fail(ATTN_ERR_CUDA, "%s: launch %zu: %s", name, i, cudaGetErrorString(le));
+    }
+    e = cudaStreamEndCapture(cs, &graph);
+    if (st == ATTN_OK && e != cudaSuccess)
+      st = fail(ATTN_ERR_CUDA, "%s: cudaStreamEndCapture: %s", name, cudaGetErrorString(e));
+    if (st == ATTN_OK) {
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      if (e != cudaSuccess) st = fail(ATTN_ERR_CUDA, "%s: cudaGraphInstantiate: %s", name, cudaGetErrorString(e));
+    }
+    cudaStreamDestroy(cs);
+    if (st != ATTN_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      cudaGetLastError();  // a failed capture leaves no sticky error; clear the non-sticky one
+      return st;
+    }
   }
-  cudaStreamDestroy(cs);
-  if (st != ATTN_OK) {
-    if (graph) cudaGraphDestroy(graph);
-    cudaGetLastError();  // a failed capture leaves no sticky error; clear the non-sticky one
-    return st;
-  }
+  step->launches = std::move(launches);
   step->graph = graph;
   step->exec = exec;
+  step->mode = mode;
+  step->device = dev;
+  step->finalized = true;
   return ATTN_OK;
 }
 
 int32_t attn_step_launch(attn_step* step, void* stream) {
   g_err[0] = '\0';
   if (!step) return fail(ATTN_ERR_INVALID_ARG, "attn_step_launch: null step");
-  if (!step->exec) return fail(ATTN_ERR_INVALID_ARG, "attn_step_launch: the step is not finalized");
-  const cudaError_t e = cudaGraphLaunch(step->exec, static_cast<cudaStream_t>(stream));
+  if (!step->finalized) return fail(ATTN_ERR_INVALID_ARG, "attn_step_launch: the step is not finalized");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (step->exec) {
+    const cudaError_t e = cudaGraphLaunch(step->exec, s);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attn_step_launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+  }
+  // Direct mode: the recorded launches, back to back, on the step's device.
+  int cur = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e == cudaSuccess && cur != step->device) e = cudaSetDevice(step->device);
+  for (size_t i = 0; i < step->launches.size() && e == cudaSuccess; ++i) e = step->launches[i](s);
+  if (cur != step->device) cudaSetDevice(cur);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attn_step_launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }

@@ -201,6 +201,24 @@ def test_step_without_calls_or_handle(lib):
     lib.attn_step_destroy(None)  # ignored
 
 
+def test_step_launch_mode_is_checked_and_kept(lib):
+    h = ctypes.c_void_p()
+    assert lib.attn_step_create(ctypes.byref(h)) == 0
+    try:
+        assert lib.attn_step_launch_mode(h) == pda.STEP_LAUNCH_AUTO
+        assert lib.attn_step_set_launch_mode(h, 7) == 1 and "unknown mode" in pda.attn_last_error()
+        assert lib.attn_step_set_launch_mode(h, -1) == 1
+        assert lib.attn_step_launch_mode(h) == pda.STEP_LAUNCH_AUTO
+        for m in (pda.STEP_LAUNCH_DIRECT, pda.STEP_LAUNCH_GRAPH):
+            assert lib.attn_step_set_launch_mode(h, m) == 0 and lib.attn_step_launch_mode(h) == m
+    finally:
+        lib.attn_step_destroy(h)
+    assert lib.attn_step_set_launch_mode(None, 0) == 1
+    assert lib.attn_step_launch_mode(None) == -1
+    with pytest.raises(ValueError):
+        pda.Step().finalize("sometimes")
+
+
 def test_step_append_validation(lib):
     h = ctypes.c_void_p()
     assert lib.attn_step_create(ctypes.byref(h)) == 0

@@ -62,18 +62,22 @@ def _direct(app, seq_lens, glob, shared, w_k, status):
     return o1, o2, o3
 
 
-def test_step_equals_the_direct_calls_bitwise(cuda_lib):
+@pytest.mark.parametrize("mode", ["graph", "direct", "auto"])
+def test_step_equals_the_direct_calls_bitwise(cuda_lib, mode):
     a = _layer_inputs(1300)
     b = _layer_inputs(1300)  # the same inputs, for the direct calls
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     step = pda.Step()
     outs = _record(step, *a, status)
     assert step.num_calls == 4 and step.num_kernels == 7
-    for o in outs:  # recording launches nothing
+    for o in outs:  # recording and finalizing launch nothing
         o.fill_(7.0)
     torch.cuda.synchronize()
+    step.finalize(mode)
+    torch.cuda.synchronize()
     assert all(torch.all(o == 7.0) for o in outs)
-    step.finalize()
+    # seven kernels: auto takes the graph
+    assert step.launch_mode == ("graph" if mode == "auto" else mode)
     step.launch()
     torch.cuda.synchronize()
     want = _direct(*b, torch.zeros(1, dtype=torch.int32, device=DEV))
@@ -87,13 +91,14 @@ def test_step_equals_the_direct_calls_bitwise(cuda_lib):
     step.close()
 
 
-def test_step_follows_inputs_changed_in_place(cuda_lib):
+@pytest.mark.parametrize("mode", ["graph", "direct"])
+def test_step_follows_inputs_changed_in_place(cuda_lib, mode):
     app, seq_lens, glob, shared, w_k = _layer_inputs(1310)
     other = make_case("global", [17, 700, 3000], seed=1399).to(DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     step = pda.Step()
     _, o2, o3 = _record(step, app, seq_lens, glob, shared, w_k, status)
-    step.finalize()
+    step.finalize(mode)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         step.launch(s)
@@ -112,12 +117,13 @@ def test_step_follows_inputs_changed_in_place(cuda_lib):
     step.close()
 
 
-def test_step_reports_device_status(cuda_lib):
+@pytest.mark.parametrize("mode", ["graph", "direct"])
+def test_step_reports_device_status(cuda_lib, mode):
     case = make_case("global", [100, 40], seed=1320).to(DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     step = pda.Step()
     step.add_decode_global(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, status=status)
-    step.finalize()
+    step.finalize(mode)
     step.launch()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -166,3 +172,30 @@ def test_step_with_a_values_only_global_layer(cuda_lib):
                                       seq_lens.cpu().numpy(), 0, 1.0e6, 64)
     assert_within_tolerance(o.double().cpu().numpy(), want, "step values-only layer")
     step.close()
+
+
+def test_one_call_step_launches_directly_back_to_back(cuda_lib):
+    """A one-call step takes the direct mode by default; many launches in a row,
+    with the inputs rotating between two buffers, equal the direct calls each time."""
+    cases = [make_case("global", [5, 700, 2049, 8192], seed=1350 + i).to(DEV) for i in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    steps, outs = [], []
+    for c in cases:
+        st = pda.Step()
+        outs.append(st.add_decode_global(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens,
+                                         max_seq_len=c.max_seq_len, out_dtype=torch.float32, status=status))
+        st.finalize()
+        assert st.launch_mode == "direct"
+        steps.append(st)
+    want = [pda.attn_decode_global(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, max_seq_len=c.max_seq_len,
+                                   out_dtype=torch.float32) for c in cases]
+    s = torch.cuda.Stream()
+    for _ in range(3):
+        for k in range(20):
+            steps[k % 2].launch(s)
+        s.synchronize()
+        assert int(status.item()) == 0
+        for got, ref in zip(outs, want):
+            assert torch.equal(got, ref)
+    for st in steps:
+        st.close()

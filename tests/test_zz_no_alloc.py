@@ -4,8 +4,12 @@ built-in scratch array holds the partial results).
 
 Called through the C ABI with ctypes, twice in a row on different inputs (the
 second call runs on whatever the first left in the shared scratch), and
-compared with attn_decode_sliding given a workspace, within the parity
-tolerance of the other tests.  This file is named to be collected last.
+compared both with the fp64 oracle and with attn_decode_sliding given a
+workspace, within the parity tolerance of the other tests.  A call with many
+forced splits followed by one with the automatic plan checks that a call
+never reads partial rows left by an earlier call's layout; the same kernels
+given a NaN-filled workspace check that nothing in the scratch needs to start
+at zero.  This file is named to be collected last.
 """
 
 import ctypes
@@ -17,7 +21,7 @@ import torch
 import paged_decode_attention_gb300 as pda
 from workloads import make_case
 
-from _helpers import ATOL, RTOL
+from _helpers import ATOL, RTOL, assert_within_tolerance, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +63,37 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cuda_lib):
         got, want = o.double().cpu().numpy(), ref.double().cpu().numpy()
         assert np.isfinite(got).all(), "call %d" % i
         assert np.all(np.abs(got - want) <= ATOL + RTOL * np.abs(want)), "call %d" % i
+        assert_within_tolerance(got, oracle_full(case), "no-alloc call %d against the oracle" % i)
+
+
+def test_noalloc_after_a_call_with_another_split_layout(cuda_lib):
+    """Many forced splits leave partial rows all over the scratch; the next
+    call (automatic plan, other lengths) must not read any of them."""
+    fn = _noalloc(pda.load())
+    first = make_case("sliding", [1100, 3000, 17, 2500], seed=904).to(DEV)
+    second = make_case("sliding", [5, 1024, 1500, 40, 777, 2049], seed=905).to(DEV)
+    for case, ns in ((first, 200), (second, 0)):
+        o = torch.full((case.B, 16, 256), float("nan"), dtype=torch.float32, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        assert _call_noalloc(fn, case, o, status, num_splits=ns) == 0, pda.attn_last_error()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert_within_tolerance(o.double().cpu().numpy(), oracle_full(case), "no-alloc, %d splits" % ns)
+
+
+def test_the_kernels_read_only_rows_their_call_wrote(cuda_lib):
+    """The workspace entry point given a NaN-filled workspace (the kernels the
+    no-alloc entry point runs): a read of any row this call did not write
+    would turn the output into NaN."""
+    case = make_case("sliding", [1, 17, 300, 1100, 5000, 0, 2047], seed=906).to(DEV)
+    for ns in (0, 64):
+        ws_bytes = pda.attn_decode_workspace_size(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns)
+        ws = torch.full(((ws_bytes + 3) // 4,), float("nan"), dtype=torch.float32, device=DEV).view(torch.uint8)
+        o = pda.attn_decode_sliding(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                    window=case.window, max_seq_len=case.max_seq_len, out_dtype=torch.float32,
+                                    workspace=ws, num_splits=ns)
+        torch.cuda.synchronize()
+        assert_within_tolerance(o.double().cpu().numpy(), oracle_full(case), "NaN workspace, %d splits" % ns)
 
 
 def test_noalloc_rejects_a_plan_beyond_its_scratch(cuda_lib):
