@@ -343,7 +343,7 @@ def prepare_workload(cfg, dev):
         for c in cs:
             kind = pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL
             ws_bytes = pda.attn_decode_workspace_size(kind, c.B, c.max_seq_len, c.window, NUM_SPLITS)
-            ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+            ws = pda.new_workspace(ws_bytes, dev)
             o = torch.empty((c.B, c.Hq, c.D), dtype=torch.bfloat16, device=dev)
             pl.append((c, ws, o))
         plans.append(pl)
@@ -422,6 +422,7 @@ def measure_sub(cfg, dev, stream, status, args, peak, peak_src, sampler=None):
     global layers the values-only cache and (workload 2) the library's
     one-launch step object on the same calls."""
     import torch
+    import paged_decode_attention_gb300 as pda
     W = prepare_workload(cfg, dev)
     plans, n_sets, calls0 = W["plans"], W["n_sets"], W["calls0"]
     n = max(8, 2 * n_sets)
@@ -434,7 +435,11 @@ def measure_sub(cfg, dev, stream, status, args, peak, peak_src, sampler=None):
     if sampler:
         sampler.mark(False, key=cfg)
     kind = calls0[0].kind
-    kernels = "%s decode + combine (2 launches per call, timed together)" % kind
+    c0 = calls0[0]
+    nk = pda.attn_decode_launches(pda.KIND_SLIDING if kind == "sliding" else pda.KIND_GLOBAL, c0.B, c0.max_seq_len,
+                                  c0.window, NUM_SPLITS)
+    kernels = ("%s decode + combine (2 launches per call, timed together)" % kind if nk == 2 else
+               "%s decode, split sequences merged in the grid (1 launch per call)" % kind)
     out = {"workload": workload_name(cfg), "calls_per_step": len(calls0), "ms_per_call": round(ms, 6),
            "calls_per_s": round(1e3 / ms, 1), "value": round(W["step_bytes"] / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
            "roofline": hbm_roofline(W["step_bytes"], ms, peak, peak_src, kernels,
@@ -478,8 +483,9 @@ def run_ours(args, rank, world, local_rank):
     def launch(pl):
         launch_calls(pl, status, stream)
 
-    # every call launches the decode kernel and its combine kernel
-    kernels_per_call = [2 for _ in calls0]
+    # the decode kernel, and a combine kernel unless the call merges in the grid
+    kernels_per_call = [pda.attn_decode_launches(pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL,
+                                                 c.B, c.max_seq_len, c.window, NUM_SPLITS) for c in calls0]
 
     # Warm-up with direct calls; then the W warm-up steps and the K timed steps
     # are each captured as one CUDA graph (step i reads input set i % n_sets),
@@ -1095,8 +1101,8 @@ def make_line(args, allres):
     # The roofline of the whole step: its algorithmic bytes over its event-timed
     # duration on the launching stream (for a one-call workload, that call).
     n_calls = r0["calls"] // args.steps
-    step_kernel = ("the whole decode step: %d decode calls (%s), each a decode kernel and its combine "
-                   "(%d launches), timed together" % (
+    step_kernel = ("the whole decode step: %d decode calls (%s), each a decode kernel and, where split "
+                   "sequences are not merged in the grid, a combine (%d launches), timed together" % (
                        n_calls, ", ".join("%d %s" % (v["calls_per_step"], k) for k, v in sorted(r0["per_type"].items()))
                        if r0.get("per_type") else r0["heavy_kind"], r0["launches_per_step"]))
     line["roofline"] = hbm_roofline(r0["bytes"] / args.steps, r0["timed_ms_per_step"], peak, peak_src, step_kernel,

@@ -104,6 +104,12 @@ extern "C" {
 #define ATTN_MAX_BATCH 256
 #define ATTN_MAX_SEQ_LEN 262144
 
+/* The first ATTN_WORKSPACE_ZERO_BYTES of every decode workspace hold the
+ * arrival counters of the in-grid merge (see num_splits below).  They must be
+ * zero before a workspace is first used; every call leaves them zero.  The
+ * rest of the workspace needs no initialisation. */
+#define ATTN_WORKSPACE_ZERO_BYTES 8192
+
 /*
  * attn_decode_sliding -- slidingDecodeGQA (Gemma-4-12B sliding layers).
  *
@@ -124,12 +130,20 @@ extern "C" {
  * num_splits   0 = automatic (one wave of resident thread blocks); > 0 forces
  *              that many thread blocks per KV head (at most 1024).  The
  *              visible pages of all sequences, concatenated, are cut into
- *              that many equal spans; a sequence cut by a span boundary is
- *              finished by a second kernel that merges the partial softmax
- *              results.  The result does not depend on this value beyond
+ *              that many equal spans; each block of a sequence cut by a span
+ *              boundary leaves a partial softmax result.  When the plan
+ *              bounds the blocks that can share a sequence to at most 24
+ *              (sliding calls whose window, or max_seq_len, caps a sequence
+ *              at 92 visible pages or fewer; the node's window of 1024 caps
+ *              it at 65 pages, 18 blocks), the last of them to finish
+ *              merges the partials inside the decode kernel;
+ *              otherwise a second kernel merges them.  attn_decode_launches
+ *              tells which.  The result does not depend on this value beyond
  *              floating-point regrouping.
  * workspace    device scratch of at least attn_decode_workspace_size(...)
- *              bytes for those partial results; contents need no
+ *              bytes for those partial results; its first
+ *              ATTN_WORKSPACE_ZERO_BYTES must be zero before its first use
+ *              (every call leaves them zero), the rest needs no
  *              initialisation; must not be shared by calls that may overlap
  * status       optional device int32 for ATTN_DEV_* bits, or NULL
  * stream       cudaStream_t, as void*
@@ -203,6 +217,15 @@ int32_t attn_decode_global_shared(const void* q, const void* kv_pool, const void
 int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
                          int32_t num_splits, int32_t num_sms, int32_t* out_num_splits,
                          size_t* out_workspace_bytes);
+
+/*
+ * attn_decode_launches -- kernels one decode call with these arguments
+ * launches (host arithmetic only): 1 when the split sequences are merged
+ * inside the decode kernel, 2 when a combine kernel follows it; -1 (and
+ * attn_last_error) on bad arguments.
+ */
+int32_t attn_decode_launches(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
+                             int32_t num_splits);
 
 /*
  * attn_decode_workspace_size -- attn_decode_plan's workspace size for the

@@ -20,7 +20,7 @@ from . import _build
 
 __all__ = [
     "attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared", "attn_decode_plan",
-    "attn_decode_workspace_size",
+    "attn_decode_workspace_size", "attn_decode_launches", "new_workspace", "WORKSPACE_ZERO_BYTES",
     "PreparedDecode", "prepare_decode_sliding", "prepare_decode_global", "prepare_decode_global_shared", "Step",
     "attn_last_error", "load", "library_path", "AttnDecodeError",
     "KIND_SLIDING", "KIND_GLOBAL", "DEV_WAIT_TIMEOUT", "DEV_BAD_PAGE", "DEV_BAD_SEQ_LEN",
@@ -33,10 +33,11 @@ OUT_BF16, OUT_F32 = 0, 1
 KIND_SLIDING, KIND_GLOBAL = 0, 1
 DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN, DEV_INTERNAL = 1, 2, 4, 8
 PAGE_SIZE = 16
+WORKSPACE_ZERO_BYTES = 8192  # ATTN_WORKSPACE_ZERO_BYTES: zero before a workspace's first use, kept zero
 SHAPES = {KIND_SLIDING: (16, 8, 256), KIND_GLOBAL: (16, 1, 512)}  # Hq, Hkv, D
 
 EXPORTS = ("attn_decode_sliding", "attn_decode_global", "attn_decode_global_shared", "attn_decode_plan",
-           "attn_decode_workspace_size", "attn_kv_append_sliding", "attn_kv_append_global",
+           "attn_decode_workspace_size", "attn_decode_launches", "attn_kv_append_sliding", "attn_kv_append_global",
            "attn_prefill_sliding", "attn_prefill_global",
            "attn_step_create", "attn_step_destroy", "attn_step_add_decode_sliding", "attn_step_add_decode_global",
            "attn_step_add_decode_global_shared", "attn_step_add_kv_append_sliding", "attn_step_add_kv_append_global",
@@ -86,6 +87,8 @@ def load(path=None):
                                      ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]
     lib.attn_decode_workspace_size.restype = c_sz
     lib.attn_decode_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32]
+    lib.attn_decode_launches.restype = c_i32
+    lib.attn_decode_launches.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32]
     app = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,  # qkv w_q w_k block_table positions q_out k_pool v_pool
            c_i32, c_i32, c_i64, c_vp, c_vp]                 # batch max_blocks num_pages status stream
     for name in ("attn_kv_append_sliding", "attn_kv_append_global"):
@@ -159,6 +162,21 @@ def attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits=0):
     return n
 
 
+def attn_decode_launches(kind, batch, max_seq_len, window, num_splits=0):
+    """Kernels one decode call launches: 1 (split sequences merged in the decode kernel) or 2 (and a combine)."""
+    n = load().attn_decode_launches(kind, batch, max_seq_len, window, num_splits)
+    if n < 0:
+        raise AttnDecodeError(1, attn_last_error())
+    return n
+
+
+def new_workspace(nbytes, device):
+    """A decode workspace of nbytes: its first WORKSPACE_ZERO_BYTES zeroed, as a first use requires."""
+    ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+    ws[:WORKSPACE_ZERO_BYTES].zero_()
+    return ws
+
+
 def _ptr(t, name, dtype, shape=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
@@ -206,7 +224,7 @@ def _decode_args(kind, q, k_pool, v_pool, block_table, seq_lens, o, window, max_
     if workspace is None:
         with torch.cuda.device(q.device):
             need = attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits)
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        workspace = new_workspace(need, q.device)
     ws_ptr = _ptr(workspace, "workspace", torch.uint8)
     st_ptr = None if status is None else _ptr(status, "status", torch.int32, (1,))
     fn_name = ("attn_decode_sliding" if kind == KIND_SLIDING else
@@ -392,8 +410,9 @@ def attn_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o=None, *, win
     """slidingDecodeGQA: q [B,16,256], pools [P,16,8,256] bf16 -> o [B,16,256].
 
     max_seq_len: host bound on seq_lens for the split plan (default max_blocks*16).
-    workspace:   uint8 CUDA tensor of at least attn_decode_workspace_size(...) bytes
-                 (allocated per call when None).
+    workspace:   uint8 CUDA tensor of at least attn_decode_workspace_size(...) bytes whose first
+                 WORKSPACE_ZERO_BYTES were zero at its first use (new_workspace); allocated per
+                 call when None.
     status:      optional int32 [1] CUDA tensor receiving ATTN_DEV_* bits.
     """
     return _call(KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, o, window, max_seq_len,

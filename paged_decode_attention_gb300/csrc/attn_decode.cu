@@ -25,6 +25,8 @@ thread_local char g_err[512] = "";
 // Set while attn_step_add_* validates a call: run_decode and run_append
 // return after their host checks, before anything is encoded or launched.
 thread_local bool g_validate_only = false;
+// Kernels the last call validated by run_decode or run_append launches.
+thread_local int32_t g_last_launches = 0;
 // One kernel launch with all its arguments bound (tensor maps included),
 // ready to be enqueued on any stream of its device.
 using RecordedLaunch = std::function<cudaError_t(cudaStream_t)>;
@@ -59,9 +61,18 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Plan {
   int grid_x;
   int min_pages;
+  bool merge_in_grid;  // cut sequences merged by their last block; no combine kernel
   size_t part_o_bytes;
   size_t workspace_bytes;
 };
+
+// Cut sequences are merged inside the sliding decode grid when at most this
+// many blocks can share one sequence: the last of them reads the others'
+// partial rows (2 KB each per KV head) in groups of four.
+constexpr int kMergeInGridMax = 24;
+
+// Workspace layout: [counters, ATTN_WORKSPACE_ZERO_BYTES][partial rows][(max, sum) pairs].
+static_assert(ATTN_WORKSPACE_ZERO_BYTES >= ATTN_MAX_BATCH * ATTN_SLIDING_HKV * 4, "a counter per (sequence, KV head)");
 
 int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
                   int32_t forced_blocks, int32_t num_sms, Plan* out) {
@@ -97,9 +108,14 @@ int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t wind
   if (gx < 1) gx = 1;
   out->grid_x = static_cast<int>(gx);
   out->min_pages = min_pages;
+  // Blocks that can share one sequence of at most max_pages visible pages:
+  // every span holds at least min_pages weighted pages, so a run of n pages
+  // meets at most (n - 1) / min_pages + 2 spans.
+  const int64_t sharing = max_pages > 0 ? (max_pages - 1) / min_pages + 2 : 1;
+  out->merge_in_grid = sliding && sharing <= kMergeInGridMax;
   const size_t rows = (static_cast<size_t>(gx) + batch) * Hq;
   out->part_o_bytes = align256(rows * D * sizeof(float));
-  out->workspace_bytes = out->part_o_bytes + align256(rows * sizeof(float2));
+  out->workspace_bytes = ATTN_WORKSPACE_ZERO_BYTES + out->part_o_bytes + align256(rows * sizeof(float2));
   return ATTN_OK;
 }
 
@@ -333,8 +349,11 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
   p.o = o;
   p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
   p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
-  p.part_o = static_cast<float*>(workspace);
-  p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + plan.part_o_bytes);
+  p.counters = static_cast<int32_t*>(workspace);
+  p.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ATTN_WORKSPACE_ZERO_BYTES);
+  p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ATTN_WORKSPACE_ZERO_BYTES +
+                                        plan.part_o_bytes);
+  p.merge_in_grid = plan.merge_in_grid;
   p.status = status;
   p.num_pages = num_pages;
   p.batch = batch;
@@ -346,6 +365,7 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
                 (sliding ? ATTN_SLIDING_HQ : ATTN_GLOBAL_HQ);
   p.out_f32 = out_dtype == ATTN_OUT_F32;
 
+  g_last_launches = plan.merge_in_grid ? 1 : 2;
   if (g_validate_only) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tm_k, tm_v;
@@ -360,7 +380,7 @@ int32_t run_decode(int32_t kind, const void* q, const void* k_pool, const void* 
     if ((st = ensure_smem(pda::combine_kernel<ATTN_SLIDING_D>, 0, dev, comb_set))) return st;
     e = launch_pdl(pda::sliding::decode_kernel, dim3(plan.grid_x, ATTN_SLIDING_HKV), pda::sliding::kThreads,
                    pda::sliding::kSmemBytes, s, tm_k, tm_v, p);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !plan.merge_in_grid)
       e = launch_pdl(pda::combine_kernel<ATTN_SLIDING_D>,
                      dim3(ATTN_SLIDING_HQ * (ATTN_SLIDING_D / pda::kCombineCols), batch), pda::kCombineWarps * 32, 0,
                      s, p);
@@ -452,6 +472,15 @@ int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32
   return ATTN_OK;
 }
 
+int32_t attn_decode_launches(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
+                             int32_t num_splits) {
+  g_err[0] = '\0';
+  Plan plan;
+  // the SM count changes the grid, not whether the merge runs in the grid
+  if (make_plan(kind, batch, max_seq_len, window, num_splits, 1, &plan) != ATTN_OK) return -1;
+  return plan.merge_in_grid ? 1 : 2;
+}
+
 size_t attn_decode_workspace_size(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
                                   int32_t num_splits) {
   g_err[0] = '\0';
@@ -517,6 +546,7 @@ int32_t run_append(int32_t kind, const void* qkv, const void* w_q, const void* w
   static_assert(ATTN_SLIDING_D / 64 <= pda::append::kMaxV && ATTN_GLOBAL_D / 64 <= pda::append::kMaxV, "dims per lane");
   const int rows = sliding ? ATTN_SLIDING_HQ + 2 * ATTN_SLIDING_HKV : ATTN_GLOBAL_HQ + 1;
   const dim3 grid((batch * rows + 3) / 4);
+  g_last_launches = 1;
   if (g_validate_only) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -85,18 +85,30 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     }
   }
   __syncthreads();
+  // A block with nothing to merge returns at once, except block (0, 0),
+  // which first waits for the decode grid: the combine grid then cannot
+  // complete before the decode grid, so the next kernel in the stream, which
+  // waits for the combine grid, also finds the decode grid's work done.
+  const auto done = [&]() {
+    if (blockIdx.x == 0 && blockIdx.y == 0) wait_for_primary_grid();
+  };
   const int before = s_sched[0], mine = s_sched[1], total = s_sched[2];
   if (mine == 0) {
     if (warp == 0) store_out4(p, row * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
+    done();
     return;
   }
   const int per = span_pages(total, p.grid_x, p.min_pages);
   const int g0 = (before + kSeqWeight) / per;
   const int g1 = (before + kSeqWeight + mine - 1) / per;
-  if (g0 == g1) return;  // one block held the whole sequence and wrote o
+  if (g0 == g1) {  // one block held the whole sequence and wrote o
+    done();
+    return;
+  }
   const int ns = g1 - g0 + 1;
   if (ns > kMaxSplits || (static_cast<int64_t>(g1) + b + 1) * Hq > p.part_rows) {
     if (threadIdx.x == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: partials beyond the workspace
+    done();
     return;
   }
 

@@ -33,6 +33,8 @@ struct DecodeParams {
   int32_t min_pages;           // smallest span a block is given
   int32_t out_f32;
   int64_t part_rows;           // rows [Hq-row granularity] the workspace holds: (grid_x + batch) * Hq
+  int32_t* counters;           // [batch][Hkv] arrivals per cut sequence (zero between calls)
+  int32_t merge_in_grid;       // cut sequences are merged by their last block (no combine kernel)
 };
 
 // ---------------------------------------------------------------------------
@@ -63,6 +65,7 @@ struct Span {
 struct SeqTable {
   int32_t prefix[kMaxBatch + 1];  // prefix[b] = visible pages of sequences < b
   int32_t len[kMaxBatch];         // L_b, clamped (clamp_len)
+  int32_t per;                    // weighted pages per block
   Span span;                      // this block's pages
   int32_t rebuilt;                // confirm_seq_table found seq_lens changed since the hint pass
 };
@@ -152,6 +155,7 @@ __device__ __forceinline__ void scan_seq_lens(const DecodeParams& p, SeqTable& t
       before += __popc(ne);
     }
     if (lane == 0) {
+      t.per = per;
       const int o0 = w0 - wp0 - kSeqWeight, o1 = w1 - wp1 - kSeqWeight;
       t.span.begin = w0 >= total ? carry : t.prefix[own0] + (o0 > 0 ? o0 : 0);
       t.span.end = w1 >= total ? carry : t.prefix[own1] + (o1 > 0 ? o1 : 0);
@@ -368,6 +372,17 @@ __device__ __forceinline__ int next_seq_in_span(const DecodeParams& p, const Seq
   int nb = b + 1;
   while (nb < p.batch && t.prefix[nb + 1] == t.prefix[nb]) ++nb;  // skip empty sequences
   return (nb < p.batch && t.prefix[nb] < sp.end) ? nb : -1;
+}
+
+// The blocks g0..g1 whose spans hold pages of sequence b (b non-empty), given
+// the number of non-empty sequences before it: its real pages sit at weighted
+// positions prefix[b] + kSeqWeight * (nonempty_before + 1) onwards.  The
+// combine kernel derives the same range from seq_lens.
+__device__ __forceinline__ void seq_blocks(const SeqTable& t, int b, int nonempty_before, int& g0, int& g1) {
+  const int w = t.prefix[b] + kSeqWeight * (nonempty_before + 1);
+  const int n = t.prefix[b + 1] - t.prefix[b];
+  g0 = w / t.per;
+  g1 = (w + n - 1) / t.per;
 }
 
 // Lets the dependent (combine) grid launch while this grid runs.

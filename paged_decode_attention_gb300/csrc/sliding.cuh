@@ -14,7 +14,12 @@
 //     of the K/V rows and of the output accumulator (packed fp32x2 FMAs);
 //   * when a sequence's pages in the span end, the four warps' (max, sum,
 //     accumulator) are merged through shared memory and written as o (the
-//     span holds the whole sequence) or as a partial for the combine kernel.
+//     span holds the whole sequence) or as a partial.  A partial is merged by
+//     the combine kernel or, when the host plan bounds the blocks that share
+//     a sequence (p.merge_in_grid), by the last of those blocks to finish:
+//     each writes its partial, counts itself in with an atomic add, and the
+//     one that completes the count reads the others' partials back and
+//     writes o.  No block waits for another.
 // Masking selects, never multiplies: rows outside [lo, L) get logit -inf
 // and their V row is skipped, so NaN in unused slots cannot leak.
 #pragma once
@@ -46,12 +51,91 @@ struct Smem {
   alignas(16) float merge_o[kConsumerWarps][kG][kD];
   float merge_m[kConsumerWarps][kG];
   float merge_l[kConsumerWarps][kG];
+  int32_t merge_last;  // this block completed the arrivals of the sequence it closes
+  int32_t merge_cnt[kConsumerWarps];  // non-empty sequences before it, per consumer warp
   SeqTable table;
   alignas(8) uint64_t full[kStages];
   alignas(8) uint64_t empty[kStages];
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 128;  // + alignment slack
+static_assert(kBlocksPerSm * (kSmemBytes + 1024) <= 228 * 1024, "shared memory of the resident blocks");
+
+// The merge of a cut sequence by the last of its blocks, run by the 128
+// consumer threads right after each has written its share (head h, dims
+// d0..d0+3) of this block's partial (M, Lsum, O) to the workspace.
+//
+// Every contributor fences its partial, then one thread adds 1 to the
+// sequence's counter; the contributor that raises it to the number of
+// contributors (blocks g0..g1 of this column) holds the last partial.  It
+// fences again, reads every partial of the sequence (its own from
+// registers) in block order g0..g1, so the result does not depend on which
+// block came last, merges them as the combine kernel would
+//     o = sum_g 2^{m_g - M} O_g / sum_g 2^{m_g - M} l_g,
+// writes o and puts the counter back to 0 for the next call (no other block
+// of this call touches it again).  Partials read back bypass L1.
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, const SeqTable& t, Smem& s, int b, int g,
+                                               int c, int h, int d0, float M, float Lsum, float4 O) {
+  const int tt = threadIdx.x;
+  int cnt = 0;  // non-empty sequences before b among b' = tt, tt + 128
+  for (int j = tt; j < b; j += kConsumerWarps * 32) cnt += t.prefix[j + 1] > t.prefix[j];
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  if ((tt & 31) == 0) s.merge_cnt[tt >> 5] = cnt;
+  int32_t* counter = p.counters + b * kHkv + c;
+  __threadfence();
+  named_barrier_sync(1, kConsumerWarps * 32);
+  int g0, g1;
+  seq_blocks(t, b, s.merge_cnt[0] + s.merge_cnt[1] + s.merge_cnt[2] + s.merge_cnt[3], g0, g1);
+  if (tt == 0) s.merge_last = atomicAdd(counter, 1) == g1 - g0;
+  named_barrier_sync(1, kConsumerWarps * 32);
+  if (!s.merge_last) return;
+  if (tt == 0) *counter = 0;  // every contributor of this call has arrived
+  __threadfence();
+  if ((static_cast<int64_t>(g1) + b + 1) * kHq > p.part_rows || g < g0 || g > g1) {
+    if (tt == 0) report(p.status, ATTN_DEV_INTERNAL);  // cannot happen: partials beyond the workspace
+    return;
+  }
+  const int hq = c * kG + h;
+  float rm = -INFINITY, rl = 0.f;
+  float4 ro = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kBatch = 4;  // partials whose loads are in flight together
+  for (int gb = g0; gb <= g1; gb += kBatch) {
+    float2 e[kBatch];
+    float4 a[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int gg = gb + j;
+      if (gg > g1) {
+        e[j] = make_float2(-INFINITY, 0.f);
+        a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else if (gg == g) {
+        e[j] = make_float2(M, Lsum);
+        a[j] = O;
+      } else {
+        const size_t sl = (static_cast<size_t>(gg) + b) * kHq + hq;
+        e[j] = __ldcg(p.part_ml + sl);
+        a[j] = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * kD + d0));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (e[j].y > 0.f) {  // a partial without a visible position adds nothing
+        const float mn = fmaxf(rm, e[j].x);
+        const float fr = rm == -INFINITY ? 0.f : exp2f(rm - mn);
+        const float fe = exp2f(e[j].x - mn);
+        rl = rl * fr + e[j].y * fe;
+        ro.x = ro.x * fr + a[j].x * fe;
+        ro.y = ro.y * fr + a[j].y * fe;
+        ro.z = ro.z * fr + a[j].z * fe;
+        ro.w = ro.w * fr + a[j].w * fe;
+        rm = mn;
+      }
+    }
+  }
+  const float inv = rl > 0.f ? 1.f / rl : 0.f;
+  const size_t row = static_cast<size_t>(b) * kHq + hq;
+  store_out4(p, row * kD + d0, make_float4(ro.x * inv, ro.y * inv, ro.z * inv, ro.w * inv));
+}
 
 __global__ void __launch_bounds__(kThreads)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -98,6 +182,15 @@ __global__ void __launch_bounds__(kThreads)
   const SeqTable& t = s.table;
   const Span sp = t.span;
   const int n_pages = sp.end - sp.begin;
+  if (p.merge_in_grid && g == 0 && warp < kConsumerWarps) {
+    // No combine kernel runs: block 0 of each column writes the empty sum of
+    // the sequences with no visible position (L = 0).
+    for (int b = 0; b < p.batch; ++b) {
+      if (t.prefix[b + 1] != t.prefix[b]) continue;
+      const size_t row = static_cast<size_t>(b) * kHq + c * kG + (threadIdx.x >> 6);
+      store_out4(p, row * kD + (threadIdx.x & 63) * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+  }
   if (n_pages <= 0) return;
 
   if (warp == kConsumerWarps) {
@@ -321,6 +414,7 @@ __global__ void __launch_bounds__(kThreads)
         const size_t slot = (static_cast<size_t>(g) + cur.b) * kHq + hq0 + h;
         *reinterpret_cast<float4*>(p.part_o + slot * kD + d0) = O;
         if (d0 == 0) p.part_ml[slot] = make_float2(M, Lsum);
+        if (p.merge_in_grid) merge_partials(p, t, s, cur.b, g, c, h, d0, M, Lsum, O);
       }
       named_barrier_sync(1, kConsumerWarps * 32);  // merge buffers free again
       reset();

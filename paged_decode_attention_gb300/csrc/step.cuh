@@ -25,15 +25,18 @@ struct attn_step {
 
 namespace {
 
-// Validates `call` (its launches suppressed) and, if it passes, appends it.
-int32_t record(attn_step* step, int32_t kernels, std::function<int32_t(void*)> call, const char* name) {
+// Validates `call` (its launches suppressed) and, if it passes, appends it
+// with the number of kernels it launches.
+int32_t record(attn_step* step, std::function<int32_t(void*)> call, const char* name) {
   g_err[0] = '\0';
   if (!step) return fail(ATTN_ERR_INVALID_ARG, "%s: null step", name);
   if (step->finalized) return fail(ATTN_ERR_INVALID_ARG, "%s: the step is already finalized", name);
   g_validate_only = true;
+  g_last_launches = 0;
   const int32_t st = call(nullptr);
   g_validate_only = false;
   if (st != ATTN_OK) return st;
+  const int32_t kernels = g_last_launches;
   try {
     step->calls.push_back(std::move(call));
   } catch (...) {  // no exception may leave the C ABI
@@ -67,7 +70,7 @@ int32_t attn_step_add_decode_sliding(attn_step* step, const void* q, const void*
                                      int32_t max_blocks, int64_t num_pages, int32_t max_seq_len, int32_t window,
                                      int32_t out_dtype, int32_t num_splits, void* workspace, size_t workspace_bytes,
                                      int32_t* status) {
-  return record(step, 2, [=](void* s) {
+  return record(step, [=](void* s) {
     return attn_decode_sliding(q, k_pool, v_pool, block_table, seq_lens, o, batch, max_blocks, num_pages,
                                max_seq_len, window, out_dtype, num_splits, workspace, workspace_bytes, status, s);
   }, "attn_step_add_decode_sliding");
@@ -78,7 +81,7 @@ int32_t attn_step_add_decode_global(attn_step* step, const void* q, const void* 
                                     int32_t max_blocks, int64_t num_pages, int32_t max_seq_len, int32_t window,
                                     int32_t out_dtype, int32_t num_splits, void* workspace, size_t workspace_bytes,
                                     int32_t* status) {
-  return record(step, 2, [=](void* s) {
+  return record(step, [=](void* s) {
     return attn_decode_global(q, k_pool, v_pool, block_table, seq_lens, o, batch, max_blocks, num_pages,
                               max_seq_len, window, out_dtype, num_splits, workspace, workspace_bytes, status, s);
   }, "attn_step_add_decode_global");
@@ -90,7 +93,7 @@ int32_t attn_step_add_decode_global_shared(attn_step* step, const void* q, const
                                            int32_t max_seq_len, int32_t window, int32_t out_dtype,
                                            int32_t num_splits, void* workspace, size_t workspace_bytes,
                                            int32_t* status) {
-  return record(step, 2, [=](void* s) {
+  return record(step, [=](void* s) {
     return attn_decode_global_shared(q, kv_pool, w_k, block_table, seq_lens, o, batch, max_blocks, num_pages,
                                      max_seq_len, window, out_dtype, num_splits, workspace, workspace_bytes,
                                      status, s);
@@ -101,7 +104,7 @@ int32_t attn_step_add_kv_append_sliding(attn_step* step, const void* qkv, const 
                                         const int32_t* block_table, const int32_t* positions, void* q_out,
                                         void* k_pool, void* v_pool, int32_t batch, int32_t max_blocks,
                                         int64_t num_pages, int32_t* status) {
-  return record(step, 1, [=](void* s) {
+  return record(step, [=](void* s) {
     return attn_kv_append_sliding(qkv, w_q, w_k, block_table, positions, q_out, k_pool, v_pool, batch, max_blocks,
                                   num_pages, status, s);
   }, "attn_step_add_kv_append_sliding");
@@ -111,7 +114,7 @@ int32_t attn_step_add_kv_append_global(attn_step* step, const void* qkv, const v
                                        const int32_t* block_table, const int32_t* positions, void* q_out,
                                        void* k_pool, void* v_pool, int32_t batch, int32_t max_blocks,
                                        int64_t num_pages, int32_t* status) {
-  return record(step, 1, [=](void* s) {
+  return record(step, [=](void* s) {
     return attn_kv_append_global(qkv, w_q, w_k, block_table, positions, q_out, k_pool, v_pool, batch, max_blocks,
                                  num_pages, status, s);
   }, "attn_step_add_kv_append_global");

@@ -66,7 +66,7 @@ def _workspace(gx, batch, D):
     def a256(x):
         return (x + 255) // 256 * 256
     rows = (gx + batch) * 16
-    return a256(rows * D * 4) + a256(rows * 8)
+    return pda.WORKSPACE_ZERO_BYTES + a256(rows * D * 4) + a256(rows * 8)
 
 
 def test_plan_fills_one_wave(lib):
@@ -88,6 +88,22 @@ def test_plan_small_problems_launch_fewer_blocks(lib):
     assert gx == 17  # ceil(65 / 4)
     gx, ws = pda.attn_decode_plan(pda.KIND_SLIDING, 2, 0, 1024)
     assert gx == 1 and ws == _workspace(1, 2, 256)
+
+
+def test_split_sequences_merge_in_the_grid_when_few_blocks_share_one(lib):
+    # sliding, window 1024: at most 65 visible pages, spans of at least 4 pages -> at most 18 blocks
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, 256, 32768, 1024) == 1
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, 4, 1100, 1024, num_splits=1000) == 1
+    # a window of 1456 spans at most 92 pages, (92 - 1) // 4 + 2 = 24 blocks: the bound; 1457 does not fit
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 262144, 1456) == 1
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 262144, 1457) == 2
+    # max_seq_len caps the pages too: 1472 positions are 92 pages
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 1472, 100000) == 1
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 1473, 100000) == 2
+    # global layers keep the combine kernel
+    assert pda.attn_decode_launches(pda.KIND_GLOBAL, 8, 8192, 0) == 2
+    with pytest.raises(pda.AttnDecodeError):
+        pda.attn_decode_launches(pda.KIND_SLIDING, 0, 100, 1024)
 
 
 def test_plan_respects_forced_block_counts(lib):

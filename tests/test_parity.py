@@ -105,6 +105,33 @@ def test_split_count_does_not_change_the_result(cuda_lib, kind):
         assert_within_tolerance(o.double().cpu().numpy(), want, "%s %d splits" % (kind, ns))
 
 
+def test_in_grid_merge_matches_the_oracle_and_leaves_its_counters_zero(cuda_lib):
+    """Sliding calls merge their split sequences inside the decode kernel (the
+    last block of each sequence reads the others' partials): every split count,
+    empty sequences among them, matches the oracle, the counters at the head of
+    the workspace are zero again after each call, and a workspace whose partial
+    rows hold a previous layout's data gives the same output."""
+    case = make_case("sliding", [0, 1, 17, 300, 1100, 5000, 0, 2047, 1024, 16], seed=95).to(DEV)
+    want = oracle_full(case)
+    for ns in (0, 3, 40, 300, 1000):
+        assert pda.attn_decode_launches(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns) == 1
+        need = pda.attn_decode_workspace_size(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns)
+        ws = pda.new_workspace(need, DEV)
+        outs = []
+        for _ in range(2):  # the second call finds the first one's partial rows in place
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            o = pda.attn_decode_sliding(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                        window=case.window, max_seq_len=case.max_seq_len, out_dtype=torch.float32,
+                                        workspace=ws, num_splits=ns, status=status)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            assert int(torch.count_nonzero(ws[:pda.WORKSPACE_ZERO_BYTES])) == 0, "counters left nonzero"
+            outs.append(o)
+        assert torch.equal(outs[0], outs[1])
+        assert_within_tolerance(outs[0].double().cpu().numpy(), want, "in-grid merge, %d splits" % ns)
+        assert torch.all(outs[0][0] == 0) and torch.all(outs[0][6] == 0)
+
+
 @pytest.mark.parametrize("kind", ["sliding", "global"])
 def test_deterministic_and_bf16_is_rounded_fp32(cuda_lib, kind):
     case = make_case(kind, [5, 300, 1100], seed=82).to(DEV)
@@ -178,7 +205,7 @@ def test_non_default_stream_and_preallocated_workspace(cuda_lib):
     case = make_case("global", [4000, 10], seed=87).to(DEV)
     need = pda.attn_decode_workspace_size(pda.KIND_GLOBAL, case.B, case.max_seq_len, 0)
     assert need > 0
-    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    ws = pda.new_workspace(need, DEV)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         o = pda.attn_decode_global(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,

@@ -8,8 +8,8 @@ compared both with the fp64 oracle and with attn_decode_sliding given a
 workspace, within the parity tolerance of the other tests.  A call with many
 forced splits followed by one with the automatic plan checks that a call
 never reads partial rows left by an earlier call's layout; the same kernels
-given a NaN-filled workspace check that nothing in the scratch needs to start
-at zero.  This file is named to be collected last.
+given a workspace whose partial rows are NaN check that only the counters at
+its head need to start at zero.  This file is named to be collected last.
 """
 
 import ctypes
@@ -82,13 +82,14 @@ def test_noalloc_after_a_call_with_another_split_layout(cuda_lib):
 
 
 def test_the_kernels_read_only_rows_their_call_wrote(cuda_lib):
-    """The workspace entry point given a NaN-filled workspace (the kernels the
-    no-alloc entry point runs): a read of any row this call did not write
-    would turn the output into NaN."""
+    """The workspace entry point given a workspace whose partial rows are NaN
+    (the kernels the no-alloc entry point runs): a read of any row this call
+    did not write would turn the output into NaN."""
     case = make_case("sliding", [1, 17, 300, 1100, 5000, 0, 2047], seed=906).to(DEV)
     for ns in (0, 64):
         ws_bytes = pda.attn_decode_workspace_size(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns)
         ws = torch.full(((ws_bytes + 3) // 4,), float("nan"), dtype=torch.float32, device=DEV).view(torch.uint8)
+        ws[:pda.WORKSPACE_ZERO_BYTES].zero_()  # the arrival counters; the partial rows stay NaN
         o = pda.attn_decode_sliding(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
                                     window=case.window, max_seq_len=case.max_seq_len, out_dtype=torch.float32,
                                     workspace=ws, num_splits=ns)
