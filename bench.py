@@ -71,11 +71,14 @@ NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 # only while the sources still hash to that value (profiles/ has the
 # captures and their commands).
 NCU_TRAFFIC = {
-    ("global", "2"): (65_291_776, "8cb53a1d861c2d40"),
-    ("global", "4b"): (2_152_939_008, "8cb53a1d861c2d40"),
-    ("global_shared", "2"): (32_074_752, "8cb53a1d861c2d40"),
-    ("global_shared", "4b"): (1_077_190_400, "8cb53a1d861c2d40"),
-    ("sliding", "3"): (2_186_832_384, "6f83cfc0ff1d0610"),
+    ("global", "2"): (63_961_705, "6886be9625dd5e2a"),
+    ("global", "4b"): (2_150_904_388, "6886be9625dd5e2a"),
+    ("global", "5"): (4_315_537_481, "6886be9625dd5e2a"),
+    ("global_shared", "2"): (32_073_892, "6886be9625dd5e2a"),
+    ("global_shared", "4b"): (1_074_527_616, "6886be9625dd5e2a"),
+    ("sliding", "3"): (2_186_851_328, "593ea8eabd59f318"),
+    # a whole 48-layer step: 40 sliding decodes, 8 global decodes and their combines
+    ("step", "5"): (50_371_017_035, "c3c83d37e902bbcc"),
 }
 KERNEL_SOURCES = {
     "global": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],
