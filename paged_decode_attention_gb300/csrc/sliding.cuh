@@ -174,7 +174,11 @@ __global__ void __launch_bounds__(kThreads)
     warm_q(p, s.table, kHq * kD, c * kG * kD, kG * kD * 2, kConsumerWarps * 32);
   }
   wait_for_primary_grid();
-  allow_dependent_launch();
+  // The dependent kernel is let launch only once this block's streaming is
+  // done (below).  With no combine kernel after this one, the dependent is
+  // the next call's kernel; a cache append launched at once would sit on
+  // the SMs waiting for this grid (a step of appends and decodes measured
+  // 12 % slower that way, back-to-back decodes 0.5 % faster).
   // The producer reads its first block-table entries while warp 0 confirms
   // the table; it reads them again if the table had to be rebuilt.
   int first = warp == kConsumerWarps ? page_entry(p, s.table, s.table.span, lane, false) : 0;
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(kThreads)
       tma_load_2d_hint(s.k[stage], &tm_k, x, y, &s.full[stage], policy);
       tma_load_2d_hint(s.v[stage], &tm_v, x, y, &s.full[stage], policy);
     });
+    allow_dependent_launch();
     return;
   }
 
@@ -420,6 +425,7 @@ __global__ void __launch_bounds__(kThreads)
       reset();
     }
   }
+  allow_dependent_launch();
 }
 
 }  // namespace sliding
