@@ -440,7 +440,7 @@ def measure_sub(cfg, dev, stream, status, args, peak, peak_src, sampler=None):
     kind = calls0[0].kind
     c0 = calls0[0]
     nk = pda.attn_decode_launches(pda.KIND_SLIDING if kind == "sliding" else pda.KIND_GLOBAL, c0.B, c0.max_seq_len,
-                                  c0.window, NUM_SPLITS)
+                                  c0.window, NUM_SPLITS, torch.cuda.get_device_properties(dev).multi_processor_count)
     kernels = ("%s decode + combine (2 launches per call, timed together)" % kind if nk == 2 else
                "%s decode, split sequences merged in the grid (1 launch per call)" % kind)
     out = {"workload": workload_name(cfg), "calls_per_step": len(calls0), "ms_per_call": round(ms, 6),
@@ -487,8 +487,9 @@ def run_ours(args, rank, world, local_rank):
         launch_calls(pl, status, stream)
 
     # the decode kernel, and a combine kernel unless the call merges in the grid
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     kernels_per_call = [pda.attn_decode_launches(pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL,
-                                                 c.B, c.max_seq_len, c.window, NUM_SPLITS) for c in calls0]
+                                                 c.B, c.max_seq_len, c.window, NUM_SPLITS, sms) for c in calls0]
 
     # Warm-up with direct calls; then the W warm-up steps and the K timed steps
     # are each captured as one CUDA graph (step i reads input set i % n_sets),

@@ -135,8 +135,10 @@ extern "C" {
  *              bounds the blocks that can share a sequence to at most 24
  *              (sliding calls whose window, or max_seq_len, caps a sequence
  *              at 92 visible pages or fewer; the node's window of 1024 caps
- *              it at 65 pages, 18 blocks), the last of them to finish
- *              merges the partials inside the decode kernel;
+ *              it at 65 pages, 18 blocks) and expects at most 8 (spans
+ *              sized as if every sequence had its cap of visible pages),
+ *              the last of them to finish merges the partials inside the
+ *              decode kernel;
  *              otherwise a second kernel merges them.  attn_decode_launches
  *              tells which.  The result does not depend on this value beyond
  *              floating-point regrouping.
@@ -220,12 +222,13 @@ int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32
 
 /*
  * attn_decode_launches -- kernels one decode call with these arguments
- * launches (host arithmetic only): 1 when the split sequences are merged
- * inside the decode kernel, 2 when a combine kernel follows it; -1 (and
- * attn_last_error) on bad arguments.
+ * launches on a device of num_sms multiprocessors (host arithmetic only, like
+ * attn_decode_plan): 1 when the split sequences are merged inside the decode
+ * kernel, 2 when a combine kernel follows it; -1 (and attn_last_error) on bad
+ * arguments.
  */
 int32_t attn_decode_launches(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
-                             int32_t num_splits);
+                             int32_t num_splits, int32_t num_sms);
 
 /*
  * attn_decode_workspace_size -- attn_decode_plan's workspace size for the

@@ -88,7 +88,7 @@ def load(path=None):
     lib.attn_decode_workspace_size.restype = c_sz
     lib.attn_decode_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32]
     lib.attn_decode_launches.restype = c_i32
-    lib.attn_decode_launches.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32]
+    lib.attn_decode_launches.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]
     app = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,  # qkv w_q w_k block_table positions q_out k_pool v_pool
            c_i32, c_i32, c_i64, c_vp, c_vp]                 # batch max_blocks num_pages status stream
     for name in ("attn_kv_append_sliding", "attn_kv_append_global"):
@@ -162,9 +162,9 @@ def attn_decode_workspace_size(kind, batch, max_seq_len, window, num_splits=0):
     return n
 
 
-def attn_decode_launches(kind, batch, max_seq_len, window, num_splits=0):
+def attn_decode_launches(kind, batch, max_seq_len, window, num_splits=0, num_sms=152):
     """Kernels one decode call launches: 1 (split sequences merged in the decode kernel) or 2 (and a combine)."""
-    n = load().attn_decode_launches(kind, batch, max_seq_len, window, num_splits)
+    n = load().attn_decode_launches(kind, batch, max_seq_len, window, num_splits, num_sms)
     if n < 0:
         raise AttnDecodeError(1, attn_last_error())
     return n

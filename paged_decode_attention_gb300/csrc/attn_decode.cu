@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -70,6 +71,10 @@ struct Plan {
 // many blocks can share one sequence: the last of them reads the others'
 // partial rows (2 KB each per KV head) in groups of four.
 constexpr int kMergeInGridMax = 24;
+// ... and when the blocks that typically share one sequence are few: with
+// many, the last block's reads of their partials take longer than the
+// combine kernel, whose blocks read every partial of a row at once.
+constexpr int kMergeInGridTypical = 8;
 
 // Workspace layout: [counters, ATTN_WORKSPACE_ZERO_BYTES][partial rows][(max, sum) pairs].
 static_assert(ATTN_WORKSPACE_ZERO_BYTES >= ATTN_MAX_BATCH * ATTN_SLIDING_HKV * 4, "a counter per (sequence, KV head)");
@@ -112,7 +117,11 @@ int32_t make_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t wind
   // every span holds at least min_pages weighted pages, so a run of n pages
   // meets at most (n - 1) / min_pages + 2 spans.
   const int64_t sharing = max_pages > 0 ? (max_pages - 1) / min_pages + 2 : 1;
-  out->merge_in_grid = sliding && sharing <= kMergeInGridMax;
+  // Typical sharing: spans sized as if every sequence had max_pages visible
+  // pages (shorter sequences give shorter spans; the bound above still holds).
+  const int64_t per_typ = std::max<int64_t>(min_pages, (total_max + gx - 1) / gx);
+  const int64_t sharing_typ = max_pages > 0 ? (max_pages - 1) / per_typ + 2 : 1;
+  out->merge_in_grid = sliding && sharing <= kMergeInGridMax && sharing_typ <= kMergeInGridTypical;
   const size_t rows = (static_cast<size_t>(gx) + batch) * Hq;
   out->part_o_bytes = align256(rows * D * sizeof(float));
   out->workspace_bytes = ATTN_WORKSPACE_ZERO_BYTES + out->part_o_bytes + align256(rows * sizeof(float2));
@@ -473,11 +482,10 @@ int32_t attn_decode_plan(int32_t kind, int32_t batch, int32_t max_seq_len, int32
 }
 
 int32_t attn_decode_launches(int32_t kind, int32_t batch, int32_t max_seq_len, int32_t window,
-                             int32_t num_splits) {
+                             int32_t num_splits, int32_t num_sms) {
   g_err[0] = '\0';
   Plan plan;
-  // the SM count changes the grid, not whether the merge runs in the grid
-  if (make_plan(kind, batch, max_seq_len, window, num_splits, 1, &plan) != ATTN_OK) return -1;
+  if (make_plan(kind, batch, max_seq_len, window, num_splits, num_sms, &plan) != ATTN_OK) return -1;
   return plan.merge_in_grid ? 1 : 2;
 }
 

@@ -91,19 +91,28 @@ def test_plan_small_problems_launch_fewer_blocks(lib):
 
 
 def test_split_sequences_merge_in_the_grid_when_few_blocks_share_one(lib):
-    # sliding, window 1024: at most 65 visible pages, spans of at least 4 pages -> at most 18 blocks
-    assert pda.attn_decode_launches(pda.KIND_SLIDING, 256, 32768, 1024) == 1
-    assert pda.attn_decode_launches(pda.KIND_SLIDING, 4, 1100, 1024, num_splits=1000) == 1
+    K = pda.KIND_SLIDING
+    # sliding, window 1024: at most 65 visible pages, spans of at least 4 pages -> at most 18 blocks;
+    # with 256 sequences the spans are long, so 2 or 3 blocks share one
+    assert pda.attn_decode_launches(K, 256, 32768, 1024) == 1
+    assert pda.attn_decode_launches(K, 64, 262144, 1024) == 1
     # a window of 1456 spans at most 92 pages, (92 - 1) // 4 + 2 = 24 blocks: the bound; 1457 does not fit
-    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 262144, 1456) == 1
-    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 262144, 1457) == 2
+    assert pda.attn_decode_launches(K, 256, 262144, 1456) == 1
+    assert pda.attn_decode_launches(K, 256, 262144, 1457) == 2
     # max_seq_len caps the pages too: 1472 positions are 92 pages
-    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 1472, 100000) == 1
-    assert pda.attn_decode_launches(pda.KIND_SLIDING, 1, 1473, 100000) == 2
+    assert pda.attn_decode_launches(K, 256, 1472, 100000) == 1
+    assert pda.attn_decode_launches(K, 256, 1473, 100000) == 2
+    # few short-spanned blocks: 4 sequences of up to 65 pages over 57 blocks would put about 15 blocks on
+    # one sequence, whose last block would read 14 partials: the combine kernel is faster there
+    assert pda.attn_decode_launches(K, 4, 1100, 1024) == 2
+    assert pda.attn_decode_launches(K, 10, 5000, 1024, num_splits=40) == 1
+    assert pda.attn_decode_launches(K, 10, 5000, 1024, num_splits=300) == 2
+    # the SM count sizes the grid: one SM holds 3 blocks over 8 columns, so spans are long
+    assert pda.attn_decode_launches(K, 4, 1100, 1024, num_sms=1) == 1
     # global layers keep the combine kernel
     assert pda.attn_decode_launches(pda.KIND_GLOBAL, 8, 8192, 0) == 2
     with pytest.raises(pda.AttnDecodeError):
-        pda.attn_decode_launches(pda.KIND_SLIDING, 0, 100, 1024)
+        pda.attn_decode_launches(K, 0, 100, 1024)
 
 
 def test_plan_respects_forced_block_counts(lib):

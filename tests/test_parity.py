@@ -106,15 +106,22 @@ def test_split_count_does_not_change_the_result(cuda_lib, kind):
 
 
 def test_in_grid_merge_matches_the_oracle_and_leaves_its_counters_zero(cuda_lib):
-    """Sliding calls merge their split sequences inside the decode kernel (the
-    last block of each sequence reads the others' partials): every split count,
-    empty sequences among them, matches the oracle, the counters at the head of
-    the workspace are zero again after each call, and a workspace whose partial
-    rows hold a previous layout's data gives the same output."""
+    """Sliding calls whose plan expects few blocks per sequence merge their split
+    sequences inside the decode kernel (the last block of each sequence reads
+    the others' partials); the others keep the combine kernel.  Either way
+    every split count, empty sequences among them, matches the oracle, the
+    counters at the head of the workspace are zero again after each call, and a
+    workspace whose partial rows hold a previous layout's data gives the same
+    output."""
     case = make_case("sliding", [0, 1, 17, 300, 1100, 5000, 0, 2047, 1024, 16], seed=95).to(DEV)
-    want = oracle_full(case)
-    for ns in (0, 3, 40, 300, 1000):
-        assert pda.attn_decode_launches(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns) == 1
+    # one long sequence among empty ones: the plan expects short spans to be rare, and its
+    # 65 pages fall on about 17 blocks, whose last one merges them all
+    lone = make_case("sliding", [1100] + [0] * 15, seed=96).to(DEV)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    for case, ns in ((case, 0), (case, 3), (case, 40), (case, 300), (case, 1000), (lone, 0)):
+        want = oracle_full(case)
+        in_grid = pda.attn_decode_launches(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns, sms) == 1
+        assert in_grid == (ns <= 40)
         need = pda.attn_decode_workspace_size(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, ns)
         ws = pda.new_workspace(need, DEV)
         outs = []
@@ -128,8 +135,9 @@ def test_in_grid_merge_matches_the_oracle_and_leaves_its_counters_zero(cuda_lib)
             assert int(torch.count_nonzero(ws[:pda.WORKSPACE_ZERO_BYTES])) == 0, "counters left nonzero"
             outs.append(o)
         assert torch.equal(outs[0], outs[1])
-        assert_within_tolerance(outs[0].double().cpu().numpy(), want, "in-grid merge, %d splits" % ns)
-        assert torch.all(outs[0][0] == 0) and torch.all(outs[0][6] == 0)
+        assert_within_tolerance(outs[0].double().cpu().numpy(), want, "B=%d, %d splits" % (case.B, ns))
+        empty = [b for b, L in enumerate(case.seq_lens_host) if L == 0]
+        assert all(torch.all(outs[0][b] == 0) for b in empty)
 
 
 @pytest.mark.parametrize("kind", ["sliding", "global"])

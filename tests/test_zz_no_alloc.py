@@ -68,11 +68,19 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cuda_lib):
 
 def test_noalloc_after_a_call_with_another_split_layout(cuda_lib):
     """Many forced splits leave partial rows all over the scratch; the next
-    call (automatic plan, other lengths) must not read any of them."""
+    calls (automatic plan, other lengths; split sequences merged inside the
+    decode kernel, with its arrival counters in the scratch, then by the
+    combine kernel) must not read any of them."""
     fn = _noalloc(pda.load())
     first = make_case("sliding", [1100, 3000, 17, 2500], seed=904).to(DEV)
-    second = make_case("sliding", [5, 1024, 1500, 40, 777, 2049], seed=905).to(DEV)
-    for case, ns in ((first, 200), (second, 0)):
+    lens = torch.randint(1, 3000, (48,), generator=torch.Generator().manual_seed(907)).tolist()
+    second = make_case("sliding", lens, seed=905).to(DEV)
+    third = make_case("sliding", [5, 1024, 1500, 40, 777, 2049], seed=908).to(DEV)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    launches = [pda.attn_decode_launches(pda.KIND_SLIDING, c.B, c.max_seq_len, c.window, ns, sms)
+                for c, ns in ((first, 200), (second, 0), (third, 0))]
+    assert launches == [2, 1, 2]
+    for case, ns in ((first, 200), (second, 0), (third, 0)):
         o = torch.full((case.B, 16, 256), float("nan"), dtype=torch.float32, device=DEV)
         status = torch.zeros(1, dtype=torch.int32, device=DEV)
         assert _call_noalloc(fn, case, o, status, num_splits=ns) == 0, pda.attn_last_error()
