@@ -107,7 +107,9 @@ extern "C" {
 /* The first ATTN_WORKSPACE_ZERO_BYTES of every decode workspace hold the
  * arrival counters of the in-grid merge (see num_splits below).  They must be
  * zero before a workspace is first used; every call leaves them zero.  The
- * rest of the workspace needs no initialisation. */
+ * rest of the workspace needs no initialisation.  A call that finds a counter
+ * above its number of arrivals raises ATTN_DEV_INTERNAL (its sequence may then
+ * be left unwritten); a counter left below it cannot be told apart. */
 #define ATTN_WORKSPACE_ZERO_BYTES 8192
 
 /*

@@ -86,7 +86,13 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, const SeqT
   named_barrier_sync(1, kConsumerWarps * 32);
   int g0, g1;
   seq_blocks(t, b, s.merge_cnt[0] + s.merge_cnt[1] + s.merge_cnt[2] + s.merge_cnt[3], g0, g1);
-  if (tt == 0) s.merge_last = atomicAdd(counter, 1) == g1 - g0;
+  if (tt == 0) {
+    const int before_me = atomicAdd(counter, 1);
+    s.merge_last = before_me == g1 - g0;
+    // more arrivals than contributors: the counter did not start at zero (a
+    // workspace whose head was not zeroed before its first use)
+    if (before_me > g1 - g0 || before_me < 0) report(p.status, ATTN_DEV_INTERNAL);
+  }
   named_barrier_sync(1, kConsumerWarps * 32);
   if (!s.merge_last) return;
   if (tt == 0) *counter = 0;  // every contributor of this call has arrived

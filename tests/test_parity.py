@@ -140,6 +140,22 @@ def test_in_grid_merge_matches_the_oracle_and_leaves_its_counters_zero(cuda_lib)
         assert all(torch.all(outs[0][b] == 0) for b in empty)
 
 
+def test_a_workspace_whose_counters_were_not_zeroed_is_reported(cuda_lib):
+    """Counters that start far above zero (a workspace head never zeroed) raise
+    ATTN_DEV_INTERNAL instead of going unnoticed; nothing waits on them."""
+    lens = torch.randint(1, 3000, (48,), generator=torch.Generator().manual_seed(97)).tolist()
+    case = make_case("sliding", lens, seed=98).to(DEV)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert pda.attn_decode_launches(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window, 0, sms) == 1
+    need = pda.attn_decode_workspace_size(pda.KIND_SLIDING, case.B, case.max_seq_len, case.window)
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.attn_decode_sliding(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, window=case.window,
+                            max_seq_len=case.max_seq_len, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pda.DEV_INTERNAL
+
+
 @pytest.mark.parametrize("kind", ["sliding", "global"])
 def test_deterministic_and_bf16_is_rounded_fp32(cuda_lib, kind):
     case = make_case(kind, [5, 300, 1100], seed=82).to(DEV)
