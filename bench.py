@@ -73,12 +73,12 @@ NUM_SPLITS = 0  # --num-splits: thread blocks per KV head, 0 = automatic
 NCU_TRAFFIC = {
     ("global", "2"): (63_961_705, "6886be9625dd5e2a"),
     ("global", "4b"): (2_150_904_388, "6886be9625dd5e2a"),
-    ("global", "5"): (4_315_537_481, "6886be9625dd5e2a"),
+    ("global", "5"): (4_315_656_713, "6886be9625dd5e2a"),
     ("global_shared", "2"): (32_073_892, "6886be9625dd5e2a"),
     ("global_shared", "4b"): (1_074_527_616, "6886be9625dd5e2a"),
-    ("sliding", "3"): (2_186_851_328, "593ea8eabd59f318"),
+    ("sliding", "3"): (2_184_783_705, "fa5274c6beb31627"),
     # a whole 48-layer step: 40 sliding decodes, 8 global decodes and their combines
-    ("step", "5"): (50_371_017_035, "c3c83d37e902bbcc"),
+    ("step", "5"): (50_372_611_502, "20ccbb5b18bae52d"),
 }
 KERNEL_SOURCES = {
     "global": ["global.cuh", "common.cuh", "ptx.cuh", "rope.cuh"],

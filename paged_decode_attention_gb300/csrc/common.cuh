@@ -54,7 +54,8 @@ struct DecodeParams {
 // the same amount of work whatever the mix of lengths.  A sequence that lies
 // inside one span is finished by that block; one that straddles spans leaves
 // a partial result in slot (block + b), an injective numbering because spans
-// and sequences are both in order, and the combine kernel merges them.
+// and sequences are both in order; the combine kernel, or the last of the
+// sequence's blocks (sliding kernel, merge in the grid), merges them.
 // ---------------------------------------------------------------------------
 constexpr int kSeqWeight = 1;  // virtual pages charged per sequence start
 
