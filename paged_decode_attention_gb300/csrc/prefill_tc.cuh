@@ -65,7 +65,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_>
+template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
@@ -88,15 +88,22 @@ struct Config {
   static constexpr int kKTile = kKChunks * kChunkRows;
   static constexpr int kVTile = kPPS * kVPage;
   static constexpr int kPBytes = kRows * kKeys * 2;
-  static constexpr int kThreads = 6 * 32;
+  // Threads issuing the S products: one MMA instruction costs its issuing
+  // thread about 70 cycles whatever its size, so with two issuers the D
+  // k-steps of a step are split in halves, each accumulated into its own S
+  // buffer (the softmax adds the two).  Warp 5 issues the first half and
+  // every P V product; warp 6 the second half.
+  static constexpr int kIssuers = kIssuers_;
+  static constexpr int kThreads = (6 + (kIssuers - 1)) * 32;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSCol = kDS;  // S buffers at columns kDS and kDS + kKeys
-  static constexpr uint32_t kPCol = kSCol + 2 * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
+  static constexpr uint32_t kSCol = kDS;  // S buffers: column kSCol + kKeys (kIssuers buffer + half)
+  static constexpr uint32_t kPCol = kSCol + 2 * kIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
   static_assert(kPCol + (kPInTmem ? kKeys : 0) <= kTmemCols, "O, two S buffers and P fit in tensor memory");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
+  static_assert(kIssuers == 1 || (kIssuers == 2 && (kD / 16) % 2 == 0), "S k-steps split in halves");
 
   struct Smem {
     alignas(1024) uint8_t q[kKChunks][kQChunkBytes];
@@ -147,16 +154,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
-      mbar_init(&s.empty[st], 1);
+      mbar_init(&s.empty[st], C::kIssuers);  // every issuer's products of the stage done
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_full[i], C::kIssuers);
       mbar_init(&s.s_free[i], 4);
       mbar_init(&s.p_full[i], 4);
       mbar_init(&s.p_empty[i], 1);
     }
     mbar_init(&s.q_ready, 4);
-    mbar_init(&s.mma_done, 1);
+    mbar_init(&s.mma_done, C::kIssuers);
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
@@ -293,10 +300,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_after_sync();
           const uint32_t k_base = smem_addr(s.k[st]);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < kD / 16 / C::kIssuers; ++kk) {
             const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
             const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-            umma_bf16(tmem + C::kSCol + C::kKeys * bs, a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s.s_full[bs]);
           if (j >= 1) pv(j - 1);
@@ -304,6 +311,34 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         pv(n_steps - 1);
         umma_commit(&s.mma_done);
         if (!mbar_wait(&s.mma_done, 0)) ok = false;  // every product done before the memory is freed
+        if (!ok) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      }
+      __syncwarp();
+    } else if (C::kIssuers == 2 && warp == 6) {
+      // ---------------- second S issuer (one thread): k-steps [kD/32, kD/16) ----------------
+      if (lane == 0) {
+        bool ok = mbar_wait(&s.q_ready, 0);
+        const uint32_t q_base = smem_addr(s.q[0]);
+        constexpr int kHalfK = kD / 16 / 2;
+        for (int j = 0; j < n_steps; ++j) {
+          const int st = j % kStages;
+          const int bs = j & 1;
+          if (ok) ok = mbar_wait(&s.full[st], (j / kStages) & 1);
+          if (ok && j >= 2) ok = mbar_wait(&s.s_free[bs], ((j - 2) >> 1) & 1);
+          tc_fence_after_sync();
+          const uint32_t k_base = smem_addr(s.k[st]);
+#pragma unroll
+          for (int k2 = 0; k2 < kHalfK; ++k2) {
+            const int kk = kHalfK + k2;
+            const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
+            const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
+            umma_bf16(tmem + C::kSCol + C::kKeys * (2 * bs + 1), a_desc, b_desc, C::kIdescS, k2 > 0 ? 1u : 0u);
+          }
+          umma_commit(&s.s_full[bs]);
+          umma_commit(&s.empty[st]);  // this issuer's reads of the stage's K tile done
+        }
+        umma_commit(&s.mma_done);
+        if (!mbar_wait(&s.mma_done, 0)) ok = false;
         if (!ok) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       }
       __syncwarp();
@@ -343,7 +378,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         float sv[C::kKeys];
 #pragma unroll
         for (int blk = 0; blk < C::kKeys / 16; ++blk)
-          tmem_ld16(t_row + C::kSCol + C::kKeys * bs + 16 * blk, *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+          tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs) + 16 * blk,
+                    *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+        if constexpr (C::kIssuers == 2) {
+          float sb[C::kKeys];
+#pragma unroll
+          for (int blk = 0; blk < C::kKeys / 16; ++blk)
+            tmem_ld16(t_row + C::kSCol + C::kKeys * (2 * bs + 1) + 16 * blk,
+                      *reinterpret_cast<float(*)[16]>(&sb[16 * blk]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < C::kKeys; ++k) sv[k] += sb[k];
+        }
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
@@ -472,8 +518,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per block, D = 256,
 // 6 stages of 16 KB.  Global: 8 queries x 16 heads per block, D = 512 split
 // into two blocks of 256 output dims (both compute S), 3 stages of 24 KB.
-using SlidingConfig = Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 5, 2, true>;
-using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true>;
+using SlidingConfig =
+    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 5, 2, true, 2>;
+using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2>;
 
 }  // namespace prefill_tc
 }  // namespace pda
