@@ -14,13 +14,16 @@
 //                  128-byte swizzle), B = the page's K tile as TMA wrote it;
 //                  accumulator in tensor memory, two buffers (a step is
 //                  kPPS pages: N = 16 kPPS keys);
-//   P   = softmax  warps 0-3, one thread per row (TMEM lane = row): masks,
+//   P   = softmax  warps 0-3 (and a second warpgroup for the second half of
+//                  the keys), one thread per row (TMEM lane = row): masks,
 //                  running max, P rounded to bf16 into shared memory as
 //                  K-major core matrices;
 //   O  += P V      tcgen05.mma M=128, N=kDS, K=16, B = the V tile, MN-major
 //                  with the 128-byte swizzle; accumulator O in tensor memory.
 // Warp 4 streams the pages by TMA, warp 5 allocates tensor memory and one of
-// its threads issues the MMAs.  S of page j+1 is computed while the softmax
+// its threads issues the MMAs (with kIssuers > 1, warps 6 .. 4 + kIssuers
+// issue parts of S; with two softmax warpgroups the last four warps handle
+// the second half of every row).  S of page j+1 is computed while the softmax
 // of page j runs, and P V of page j while the softmax of page j+1 runs.
 //
 // Running max.  A row's reference max m moves only when a score exceeds it by
@@ -65,7 +68,8 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1>
+template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
+          int kSoftmaxGroups_ = 1>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
@@ -89,12 +93,17 @@ struct Config {
   static constexpr int kVTile = kPPS * kVPage;
   static constexpr int kPBytes = kRows * kKeys * 2;
   // Threads issuing the S products: one MMA instruction costs its issuing
-  // thread about 70 cycles whatever its size, so with two issuers the D
-  // k-steps of a step are split in halves, each accumulated into its own S
-  // buffer (the softmax adds the two).  Warp 5 issues the first half and
-  // every P V product; warp 6 the second half.
+  // thread about 70 cycles whatever its size, so the D k-steps of a step are
+  // split into kIssuers parts, each accumulated into its own S buffer (the
+  // softmax adds them).  Warp 5 issues part 0 and every P V product; warps
+  // 6 .. 4 + kIssuers the other parts.
   static constexpr int kIssuers = kIssuers_;
-  static constexpr int kThreads = (6 + (kIssuers - 1)) * 32;
+  // Softmax warpgroups: with two, each row's keys of a step are split in
+  // halves (warps 0-3 the first, warps 5 + kIssuers .. 8 + kIssuers the
+  // second), and so are its output dims.
+  static constexpr int kSoftmaxGroups = kSoftmaxGroups_;
+  static constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
+  static constexpr int kThreads = (4 * kSoftmaxGroups + 1 + kIssuers) * 32;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = kDS;  // S buffers: column kSCol + kKeys (kIssuers buffer + half)
   static constexpr uint32_t kPCol = kSCol + 2 * kIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
@@ -103,7 +112,9 @@ struct Config {
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
   static_assert(kPCol + (kPInTmem ? kKeys : 0) <= kTmemCols, "O, two S buffers and P fit in tensor memory");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
-  static_assert(kIssuers == 1 || (kIssuers == 2 && (kD / 16) % 2 == 0), "S k-steps split in halves");
+  static_assert(kIssuers >= 1 && kIssuers <= kD / 16, "S k-steps split among the issuers");
+  static_assert(kSoftmaxGroups == 1 || (kSoftmaxGroups == 2 && kPInTmem && (kKeys / 2) % 16 == 0 && kDS % 32 == 0),
+                "two softmax warpgroups: halves of whole 16-key blocks, P in tensor memory");
 
   struct Smem {
     alignas(1024) uint8_t q[kKChunks][kQChunkBytes];
@@ -119,6 +130,8 @@ struct Config {
     alignas(8) uint64_t q_ready;         // Q tile written (4 warps)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
     uint32_t tmem_base;
+    float half_max[2][kSoftmaxGroups][kRows];  // two warpgroups: each half-row's max, by step parity
+    float half_sum[kSoftmaxGroups][kRows];     // and its share of the row sum, at the end
   };
   static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 };
@@ -158,11 +171,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], C::kIssuers);
-      mbar_init(&s.s_free[i], 4);
-      mbar_init(&s.p_full[i], 4);
+      mbar_init(&s.s_free[i], 4 * C::kSoftmaxGroups);
+      mbar_init(&s.p_full[i], 4 * C::kSoftmaxGroups);
       mbar_init(&s.p_empty[i], 1);
     }
-    mbar_init(&s.q_ready, 4);
+    mbar_init(&s.q_ready, 4 * C::kSoftmaxGroups);
     mbar_init(&s.mma_done, C::kIssuers);
     fence_mbar_init();
   }
@@ -300,7 +313,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_after_sync();
           const uint32_t k_base = smem_addr(s.k[st]);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16 / C::kIssuers; ++kk) {
+          for (int kk = 0; kk < (kD / 16) / C::kIssuers; ++kk) {
             const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
             const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
             umma_bf16(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
@@ -314,12 +327,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!ok) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       }
       __syncwarp();
-    } else if (C::kIssuers == 2 && warp == 6) {
-      // ---------------- second S issuer (one thread): k-steps [kD/32, kD/16) ----------------
+    } else if (warp >= 6 && warp < 5 + C::kIssuers) {
+      // ---------------- the other S issuers (one thread each): part i of the k-steps ----------------
       if (lane == 0) {
+        const int part = warp - 5;
+        const int kk0 = part * (kD / 16) / C::kIssuers, kk1 = (part + 1) * (kD / 16) / C::kIssuers;
         bool ok = mbar_wait(&s.q_ready, 0);
         const uint32_t q_base = smem_addr(s.q[0]);
-        constexpr int kHalfK = kD / 16 / 2;
         for (int j = 0; j < n_steps; ++j) {
           const int st = j % kStages;
           const int bs = j & 1;
@@ -327,12 +341,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (ok && j >= 2) ok = mbar_wait(&s.s_free[bs], ((j - 2) >> 1) & 1);
           tc_fence_after_sync();
           const uint32_t k_base = smem_addr(s.k[st]);
-#pragma unroll
-          for (int k2 = 0; k2 < kHalfK; ++k2) {
-            const int kk = kHalfK + k2;
+          for (int kk = kk0; kk < kk1; ++kk) {
             const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
             const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-            umma_bf16(tmem + C::kSCol + C::kKeys * (2 * bs + 1), a_desc, b_desc, C::kIdescS, k2 > 0 ? 1u : 0u);
+            umma_bf16(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs + part), a_desc, b_desc, C::kIdescS,
+                      kk > kk0 ? 1u : 0u);
           }
           umma_commit(&s.s_full[bs]);
           umma_commit(&s.empty[st]);  // this issuer's reads of the stage's K tile done
@@ -343,24 +356,36 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       __syncwarp();
     } else {
-      // ---------------- softmax and epilogue: one thread per row ----------------
-      const int r = threadIdx.x;  // 0..127: TMEM lane r
+      // ---------------- softmax and epilogue: one thread per row (and half) ----------------
+      // With two warpgroups, thread r of group h handles keys [h kHalf, (h + 1) kHalf)
+      // of each step of row r, and columns [h kDS/2, (h + 1) kDS/2) of O; the
+      // two halves of a row share the row max through shared memory.
+      constexpr int kGroups = C::kSoftmaxGroups;
+      constexpr int kHalf = C::kKeys / kGroups;  // keys of a step per thread
+      constexpr int kOCols = kDS / kGroups;      // output dims per thread
+      const int h = warp >= 4 ? 1 : 0;            // softmax warpgroup (warps 0-3, then the last four)
+      const int r = 32 * (warp & 3) + lane;       // row = TMEM lane
+      const int st = h * 128 + r;                 // index among the softmax threads
+      const int kc0 = h * kHalf;                  // this thread's first key column of a step
+      const int oc0 = h * kOCols;                 // and first output column
       const int g = r / kQ;
       const int qi = r % kQ;
       const bool valid = qi < nq;
       const int head = c * kG + g;
       const int pos = P0 + qi;
       const int lo_r = p.window > 0 ? pos - p.window + 1 : 0;
-      const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
       // Q row into shared memory: K-major, 128-byte swizzle, chunks of 64 dims
+      // (each group copies its share of the row's 16-byte units)
       {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+        const uint8_t* src_row = reinterpret_cast<const uint8_t*>(
             p.q + (static_cast<size_t>(valid ? q0 + i0 + qi : 0) * kHq + head) * kD);
         const uint32_t q_base = smem_addr(s.q[0]);
+        constexpr int kUnits = kD / 8 / kGroups;
 #pragma unroll 8
-        for (int u = 0; u < kD / 8; ++u)
-          cp_async_16(q_base + (u >> 3) * C::kQChunkBytes + r * 128 + (((u & 7) ^ (r & 7)) << 4), src + 16 * u,
+        for (int u = h * kUnits; u < (h + 1) * kUnits; ++u)
+          cp_async_16(q_base + (u >> 3) * C::kQChunkBytes + r * 128 + (((u & 7) ^ (r & 7)) << 4), src_row + 16 * u,
                       valid ? 16u : 0u);
         cp_async_wait_all();
         fence_proxy_async_smem();
@@ -368,43 +393,50 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) mbar_arrive(&s.q_ready);
       }
 
-      float m = -INFINITY, l = 0.f;  // reference max (log2 units) and row sum
+      float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this thread's share of the row sum
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
         const int bs = j & 1;
-        const int pos0 = (page0 + j * kPPS) * kPage;  // key of column 0
+        const int step0 = (page0 + j * kPPS) * kPage;  // key of the step's column 0
+        const int pos0 = step0 + kc0;                   // key of this thread's first column
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[bs], (j >> 1) & 1));
         tc_fence_after_sync();
-        float sv[C::kKeys];
+        float sv[kHalf];
 #pragma unroll
-        for (int blk = 0; blk < C::kKeys / 16; ++blk)
-          tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs) + 16 * blk,
+        for (int blk = 0; blk < kHalf / 16; ++blk)
+          tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs) + kc0 + 16 * blk,
                     *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
-        if constexpr (C::kIssuers == 2) {
-          float sb[C::kKeys];
 #pragma unroll
-          for (int blk = 0; blk < C::kKeys / 16; ++blk)
-            tmem_ld16(t_row + C::kSCol + C::kKeys * (2 * bs + 1) + 16 * blk,
+        for (int part = 1; part < C::kIssuers; ++part) {
+          float sb[kHalf];
+#pragma unroll
+          for (int blk = 0; blk < kHalf / 16; ++blk)
+            tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs + part) + kc0 + 16 * blk,
                       *reinterpret_cast<float(*)[16]>(&sb[16 * blk]));
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < C::kKeys; ++k) sv[k] += sb[k];
+          for (int k = 0; k < kHalf; ++k) sv[k] += sb[k];
         }
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.s_free[bs]);
 
-        if (!valid || pos0 < lo_r || pos0 + C::kKeys - 1 > pos) {
+        if (!valid || pos0 < lo_r || pos0 + kHalf - 1 > pos) {
 #pragma unroll
-          for (int k = 0; k < C::kKeys; ++k) {
+          for (int k = 0; k < kHalf; ++k) {
             const int key = pos0 + k;
             if (!valid || key < lo_r || key > pos) sv[k] = -INFINITY;
           }
         }
         float mx = sv[0];
 #pragma unroll
-        for (int k = 1; k < C::kKeys; ++k) mx = fmaxf(mx, sv[k]);
+        for (int k = 1; k < kHalf; ++k) mx = fmaxf(mx, sv[k]);
+        if constexpr (kGroups == 2) {
+          s.half_max[bs][h][r] = mx;
+          named_barrier_sync(1, C::kSoftmaxThreads);
+          mx = fmaxf(mx, s.half_max[bs][1 - h][r]);
+        }
         const float m_new = mx * kLog2e;
         const bool move = m_new > m + kSlack;  // false while the row has no visible key
         const bool rescale = move && m != -INFINITY;
@@ -414,7 +446,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_after_sync();
           const float f = rescale ? ex2_approx(m - m_new) : 1.f;
 #pragma unroll 1
-          for (int col = 0; col < kDS; col += 16) {
+          for (int col = oc0; col < oc0 + kOCols; col += 16) {
             float ov[16];
             tmem_ld16(t_row + col, ov);
             tmem_wait_ld();
@@ -429,7 +461,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const float m_use = m == -INFINITY ? 0.f : m;
         float ls = 0.f;
 #pragma unroll
-        for (int k = 0; k < C::kKeys; ++k) {
+        for (int k = 0; k < kHalf; ++k) {
           sv[k] = ex2_approx(fmaf(sv[k], kLog2e, -m_use));
           ls += sv[k];
         }
@@ -439,13 +471,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // P V of step j-2 has read it
         if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[bs], ((j - 2) >> 1) & 1));
         if constexpr (C::kPInTmem) {
-          // this row of P into its lane: columns kPCol + (kKeys / 2) bs + j hold keys 2j, 2j + 1
+          // this row's keys into its lane: column kPCol + (kKeys / 2) bs + k / 2 holds keys k, k + 1
 #pragma unroll
-          for (int kc = 0; kc < C::kKeys / 16; ++kc) {
+          for (int kc = 0; kc < kHalf / 16; ++kc) {
             uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
-            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * bs + 8 * kc, w);
+            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * bs + kc0 / 2 + 8 * kc, w);
           }
           tmem_wait_st();
         } else {
@@ -458,12 +490,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                     pack_bf16x2(sv[8 * kc + 6], sv[8 * kc + 7])));
         }
         // zero this step's V rows outside [k_lo, k_hi] (the first and last steps)
-        if (pos0 < k_lo || pos0 + C::kKeys - 1 > k_hi) {
+        if (step0 < k_lo || step0 + C::kKeys - 1 > k_hi) {
           const uint32_t v_base = smem_addr(s.v[j % kStages]);
 #pragma unroll 1
-          for (int it = r; it < C::kKeys * 8; it += 128) {
+          for (int it = st; it < C::kKeys * 8; it += C::kSoftmaxThreads) {
             const int kr = it >> 3;  // key row of the step
-            const int key = pos0 + kr;
+            const int key = step0 + kr;
             if (key < k_lo || key > k_hi) {
 #pragma unroll
               for (int ch = 0; ch < C::kVChunks; ++ch)
@@ -478,14 +510,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) mbar_arrive(&s.p_full[bs]);
       }
 
-      // ---- epilogue: wait for the last P V, normalise, write this row's kDS dims ----
+      // ---- epilogue: wait for the last P V, normalise, write this row's output dims ----
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       tc_fence_after_sync();
+      if constexpr (kGroups == 2) {
+        s.half_sum[h][r] = l;
+        named_barrier_sync(1, C::kSoftmaxThreads);
+        l += s.half_sum[1 - h][r];
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t o_off = (static_cast<size_t>(q0 + i0 + qi) * kHq + head) * kD + slice * kDS;
 #pragma unroll 1
-      for (int col = 0; col < kDS; col += 16) {
+      for (int col = oc0; col < oc0 + kOCols; col += 16) {
         float ov[16];
         tmem_ld16(t_row + col, ov);
         tmem_wait_ld();
@@ -516,10 +553,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 }
 
 // Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per block, D = 256,
-// 6 stages of 16 KB.  Global: 8 queries x 16 heads per block, D = 512 split
-// into two blocks of 256 output dims (both compute S), 3 stages of 24 KB.
+// 2-page steps in 4 stages of 32 KB, two S issuers, two softmax warpgroups.
+// Global: 8 queries x 16 heads per block, D = 512 split into two blocks of
+// 256 output dims (both compute S), 2-page steps in 2 stages of 48 KB, two S
+// issuers, one softmax warpgroup.
 using SlidingConfig =
-    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 5, 2, true, 2>;
+    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 4, 2, true, 2, 2>;
 using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2>;
 
 }  // namespace prefill_tc
