@@ -20,17 +20,23 @@
 //                  K-major core matrices;
 //   O  += P V      tcgen05.mma M=128, N=kDS, K=16, B = the V tile, MN-major
 //                  with the 128-byte swizzle; accumulator O in tensor memory.
-// Warp 4 streams the pages by TMA, warp 5 allocates tensor memory and one of
-// its threads issues the MMAs (with kIssuers > 1, warps 6 .. 4 + kIssuers
-// issue parts of S; with two softmax warpgroups the last four warps handle
-// the second half of every row).  S of page j+1 is computed while the softmax
+// Warp 4 streams the pages by TMA, warp 5 allocates tensor memory and issues
+// the MMAs (the whole warp runs the loop, one elected lane issues; with
+// kIssuers > 1, warps 6 .. 4 + kIssuers issue parts of S; with two softmax
+// warpgroups the last four warps handle the second half of every row).  S of page j+1 is computed while the softmax
 // of page j runs, and P V of page j while the softmax of page j+1 runs.
 //
 // Running max.  A row's reference max m moves only when a score exceeds it by
-// more than 2^8 (kSlack log2 units): exp2(s - m) <= 256 stays well inside fp32
-// and bf16, numerator and denominator share m, so the result is the same
-// softmax; O is rescaled in tensor memory only then (rarely after a row's
-// first pages).  Key rows outside [k_lo, k_hi] of the first and last page are
+// more than kSlack = 16 log2 units, and then to kHeadroom = 48 above that
+// score.  So every weight exp2(s - m) is at most 2^16, the row's largest is
+// at least 2^-48, and only keys more than 78 log2 units below the row max
+// (relative weight < 2^-78) flush to zero: all well inside fp32 and bf16.
+// Numerator and denominator share m, so the result is the same softmax.  O
+// is rescaled in tensor memory only when m moves.  A warp rescales if any of
+// its 32 rows moves, and a row's first keys (the window edge) estimate its
+// max poorly, so a narrow band (2^8, no headroom) made about half of the
+// steps rescale; with these bounds it is a few per cent.  The rescale loads
+// 64 columns per tensor-memory round trip.  Key rows outside [k_lo, k_hi] of the first and last page are
 // zeroed in shared memory before P V (0 * NaN would be NaN); masked scores
 // become -inf.
 #pragma once
@@ -69,7 +75,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 }
 
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
-          int kSoftmaxGroups_ = 1>
+          int kSoftmaxGroups_ = 1, int kRotate_ = 0>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
@@ -103,6 +109,11 @@ struct Config {
   // second), and so are its output dims.
   static constexpr int kSoftmaxGroups = kSoftmaxGroups_;
   static constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
+  // Step order: with kRotate > 0 the block of query tile t starts at step
+  // (kRotate t) mod n_steps and wraps around, so that the blocks resident at
+  // one time read different pages (the softmax does not depend on the order
+  // of the keys).
+  static constexpr int kRotate = kRotate_;
   static constexpr int kThreads = (4 * kSoftmaxGroups + 1 + kIssuers) * 32;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = kDS;  // S buffers: column kSCol + kKeys (kIssuers buffer + half)
@@ -136,7 +147,9 @@ struct Config {
   static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 };
 
-constexpr float kSlack = 8.f;  // log2 units
+constexpr float kSlack = 16.f;     // log2 units
+constexpr float kHeadroom = 48.f;  // a moved reference max sits this far above the row's max
+constexpr int kRoundTrip = 4;     // 16-column TMEM loads per wait when O is rescaled or written
 
 // 16 bytes global -> shared without a register round trip; src_bytes 0
 // writes zeros (src is then not read).
@@ -223,6 +236,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int page0 = k_lo / kPage;
     const int n_pages = k_hi / kPage - page0 + 1;
     const int n_steps = (n_pages + kPPS - 1) / kPPS;
+    const int rot = C::kRotate > 0 ? static_cast<int>((static_cast<int64_t>(tile) * C::kRotate) % n_steps) : 0;
+    // step j of the copy order covers logical step (j + rot) mod n_steps;
+    // page gp of the copy order is logical page logical_page(gp)
+    const auto logical_step = [&](int j) { return j + rot < n_steps ? j + rot : j + rot - n_steps; };
+    const auto logical_page = [&](int gp) { return logical_step(gp / kPPS) * kPPS + gp % kPPS; };
 
     if (warp == 4) {
       // ---------------- producer: step i = pages page0 + i*kPPS ... ----------------
@@ -234,19 +252,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
       bool ok = true;
       int issued = 0;
-      // block-table entries of pages 32k + lane, one batch ahead
-      int cur = lane < n_pages ? bt[page0 + lane] : -1;
-      int nxt = 32 + lane < n_pages ? bt[page0 + 32 + lane] : -1;
+      // block-table entry of the page copied at position gp of the order
+      const auto entry = [&](int gp) {
+        const int lp = logical_page(gp);
+        return gp < n_steps * kPPS && lp < n_pages ? bt[page0 + lp] : -1;
+      };
+      // block-table entries of pages 32k + lane (in copy order), one batch ahead
+      int cur = entry(lane);
+      int nxt = entry(32 + lane);
       for (int i = 0; i < n_steps; ++i) {
         const int gp0 = i * kPPS;
         if (gp0 > 0 && (gp0 & 31) == 0) {
           cur = nxt;
-          nxt = gp0 + 32 + lane < n_pages ? bt[page0 + gp0 + 32 + lane] : -1;
+          nxt = entry(gp0 + 32 + lane);
         }
         const int phys = __shfl_sync(0xffffffffu, cur, (gp0 + (lane < kPPS ? lane : 0)) & 31);
         const int stage = i % kStages;
         if (i >= kStages) {
-          const int w = lane == 0 ? static_cast<int>(mbar_wait(&s.empty[stage], ((i / kStages) - 1) & 1)) : 0;
+          const int w = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.empty[stage], ((i / kStages) - 1) & 1)) : 0;
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         }
         if (!ok) {
@@ -256,7 +279,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], C::kKTile + C::kVTile);
         __syncwarp();
         if (lane < kPPS) {
-          const int gp = gp0 + lane;
+          const int gp = logical_page(gp0 + lane);
           int32_t y = -kPage;
           if (gp < n_pages) {
             if (phys < 0 || static_cast<int64_t>(phys) >= p.num_pages)
@@ -281,80 +304,76 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       }
     } else if (warp == 5) {
-      // ---------------- MMA issuer (one thread) ----------------
-      if (lane == 0) {
-        bool ok = mbar_wait(&s.q_ready, 0);
-        const uint32_t q_base = smem_addr(s.q[0]);
-        auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
-          const int bp = j & 1;
-          const int st = j % kStages;
-          if (ok) ok = mbar_wait(&s.p_full[bp], (j >> 1) & 1);
-          tc_fence_after_sync();
-          const uint32_t v_base = smem_addr(s.v[st]);
+      // ---------------- MMA issuer (the whole warp; an elected lane issues) ----------------
+      bool ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, 0));
+      const uint32_t q_base = smem_addr(s.q[0]);
+      auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
+        const int bp = j & 1;
+        const int st = j % kStages;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[bp], (j >> 1) & 1));
+        tc_fence_after_sync();
+        const uint32_t v_base = smem_addr(s.v[st]);
 #pragma unroll
-          for (int kk = 0; kk < kPPS; ++kk) {
-            const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
-            if constexpr (C::kPInTmem) {
-              umma_bf16_ts(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-            } else {
-              const uint64_t a_desc = umma_desc(smem_addr(s.p[bp]) + kk * 256, 128, C::kKeys * 16, 0);
-              umma_bf16(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-            }
+        for (int kk = 0; kk < kPPS; ++kk) {
+          const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
+          if constexpr (C::kPInTmem) {
+            umma_bf16_ts_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            const uint64_t a_desc = umma_desc(smem_addr(s.p[bp]) + kk * 256, 128, C::kKeys * 16, 0);
+            umma_bf16_warp(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&s.empty[st]);
-          umma_commit(&s.p_empty[bp]);
-        };
-        for (int j = 0; j < n_steps; ++j) {
-          const int st = j % kStages;
-          const int bs = j & 1;
-          if (ok) ok = mbar_wait(&s.full[st], (j / kStages) & 1);
-          if (ok && j >= 2) ok = mbar_wait(&s.s_free[bs], ((j - 2) >> 1) & 1);
-          tc_fence_after_sync();
-          const uint32_t k_base = smem_addr(s.k[st]);
-#pragma unroll
-          for (int kk = 0; kk < (kD / 16) / C::kIssuers; ++kk) {
-            const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
-            const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-            umma_bf16(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&s.s_full[bs]);
-          if (j >= 1) pv(j - 1);
         }
-        pv(n_steps - 1);
-        umma_commit(&s.mma_done);
-        if (!mbar_wait(&s.mma_done, 0)) ok = false;  // every product done before the memory is freed
-        if (!ok) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        umma_commit_warp(&s.empty[st]);
+        umma_commit_warp(&s.p_empty[bp]);
+      };
+      for (int j = 0; j < n_steps; ++j) {
+        const int st = j % kStages;
+        const int bs = j & 1;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
+        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j - 2) >> 1) & 1));
+        tc_fence_after_sync();
+        const uint32_t k_base = smem_addr(s.k[st]);
+#pragma unroll
+        for (int kk = 0; kk < (kD / 16) / C::kIssuers; ++kk) {
+          const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
+          const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
+          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit_warp(&s.s_full[bs]);
+        if (j >= 1) pv(j - 1);
       }
-      __syncwarp();
+      pv(n_steps - 1);
+      umma_commit_warp(&s.mma_done);
+      if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // every product done before the memory is freed
+      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     } else if (warp >= 6 && warp < 5 + C::kIssuers) {
-      // ---------------- the other S issuers (one thread each): part i of the k-steps ----------------
-      if (lane == 0) {
-        const int part = warp - 5;
-        const int kk0 = part * (kD / 16) / C::kIssuers, kk1 = (part + 1) * (kD / 16) / C::kIssuers;
-        bool ok = mbar_wait(&s.q_ready, 0);
-        const uint32_t q_base = smem_addr(s.q[0]);
-        for (int j = 0; j < n_steps; ++j) {
-          const int st = j % kStages;
-          const int bs = j & 1;
-          if (ok) ok = mbar_wait(&s.full[st], (j / kStages) & 1);
-          if (ok && j >= 2) ok = mbar_wait(&s.s_free[bs], ((j - 2) >> 1) & 1);
-          tc_fence_after_sync();
-          const uint32_t k_base = smem_addr(s.k[st]);
-          for (int kk = kk0; kk < kk1; ++kk) {
-            const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
-            const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-            umma_bf16(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs + part), a_desc, b_desc, C::kIdescS,
-                      kk > kk0 ? 1u : 0u);
-          }
-          umma_commit(&s.s_full[bs]);
-          umma_commit(&s.empty[st]);  // this issuer's reads of the stage's K tile done
+      // ---------------- the other S issuers (whole warps): part i of the k-steps ----------------
+      constexpr int kPart = (kD / 16) / C::kIssuers;  // k-steps per issuer, whole 64-dim chunks
+      static_assert(kPart % 4 == 0, "each issuer takes whole chunks of Q and K");
+      const int part = warp - 5;
+      bool ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, 0));
+      const uint32_t q_base = smem_addr(s.q[0]) + (part * kPart / 4) * C::kQChunkBytes;
+      for (int j = 0; j < n_steps; ++j) {
+        const int st = j % kStages;
+        const int bs = j & 1;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
+        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j - 2) >> 1) & 1));
+        tc_fence_after_sync();
+        const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kChunkRows;
+#pragma unroll
+        for (int kk = 0; kk < kPart; ++kk) {
+          const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
+          const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
+          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs + part), a_desc, b_desc, C::kIdescS,
+                         kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s.mma_done);
-        if (!mbar_wait(&s.mma_done, 0)) ok = false;
-        if (!ok) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        umma_commit_warp(&s.s_full[bs]);
+        umma_commit_warp(&s.empty[st]);  // this issuer's reads of the stage's K tile done
       }
-      __syncwarp();
+      umma_commit_warp(&s.mma_done);
+      if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
+      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     } else {
       // ---------------- softmax and epilogue: one thread per row (and half) ----------------
       // With two warpgroups, thread r of group h handles keys [h kHalf, (h + 1) kHalf)
@@ -363,6 +382,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       constexpr int kGroups = C::kSoftmaxGroups;
       constexpr int kHalf = C::kKeys / kGroups;  // keys of a step per thread
       constexpr int kOCols = kDS / kGroups;      // output dims per thread
+      static_assert(kOCols % (16 * kRoundTrip) == 0, "whole TMEM round trips");
       const int h = warp >= 4 ? 1 : 0;            // softmax warpgroup (warps 0-3, then the last four)
       const int r = 32 * (warp & 3) + lane;       // row = TMEM lane
       const int st = h * 128 + r;                 // index among the softmax threads
@@ -397,9 +417,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
         const int bs = j & 1;
-        const int step0 = (page0 + j * kPPS) * kPage;  // key of the step's column 0
+        const int step0 = (page0 + logical_step(j) * kPPS) * kPage;  // key of the step's column 0
         const int pos0 = step0 + kc0;                   // key of this thread's first column
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[bs], (j >> 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (j >> 1) & 1));
         tc_fence_after_sync();
         float sv[kHalf];
 #pragma unroll
@@ -442,22 +462,26 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const bool rescale = move && m != -INFINITY;
         if (__any_sync(0xffffffffu, rescale)) {
           // O's row holds P V up to step j-1: wait for that product, then scale in place
-          if (ok && j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          if (ok && j >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1));
           tc_fence_after_sync();
-          const float f = rescale ? ex2_approx(m - m_new) : 1.f;
+          const float f = rescale ? ex2_approx(m - (m_new + kHeadroom)) : 1.f;
 #pragma unroll 1
-          for (int col = oc0; col < oc0 + kOCols; col += 16) {
-            float ov[16];
-            tmem_ld16(t_row + col, ov);
+          for (int col = oc0; col < oc0 + kOCols; col += 16 * kRoundTrip) {
+            float ov[kRoundTrip][16];
+#pragma unroll
+            for (int u = 0; u < kRoundTrip; ++u) tmem_ld16(t_row + col + 16 * u, ov[u]);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) ov[k] *= f;
-            tmem_st16(t_row + col, ov);
+            for (int u = 0; u < kRoundTrip; ++u) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) ov[u][k] *= f;
+              tmem_st16(t_row + col + 16 * u, ov[u]);
+            }
           }
           tmem_wait_st();
           l *= f;
         }
-        if (move) m = m_new;
+        if (move) m = m_new + kHeadroom;
         const float m_use = m == -INFINITY ? 0.f : m;
         float ls = 0.f;
 #pragma unroll
@@ -469,7 +493,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
         // P row into buffer bs (K-major core matrices of 8 rows x 8 keys) once
         // P V of step j-2 has read it
-        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[bs], ((j - 2) >> 1) & 1));
+        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[bs], ((j - 2) >> 1) & 1));
         if constexpr (C::kPInTmem) {
           // this row's keys into its lane: column kPCol + (kKeys / 2) bs + k / 2 holds keys k, k + 1
 #pragma unroll
@@ -511,7 +535,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
 
       // ---- epilogue: wait for the last P V, normalise, write this row's output dims ----
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s.p_empty[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       tc_fence_after_sync();
       if constexpr (kGroups == 2) {
@@ -522,22 +546,28 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t o_off = (static_cast<size_t>(q0 + i0 + qi) * kHq + head) * kD + slice * kDS;
 #pragma unroll 1
-      for (int col = oc0; col < oc0 + kOCols; col += 16) {
-        float ov[16];
-        tmem_ld16(t_row + col, ov);
+      for (int col0 = oc0; col0 < oc0 + kOCols; col0 += 16 * kRoundTrip) {
+        float ovs[kRoundTrip][16];
+#pragma unroll
+        for (int u = 0; u < kRoundTrip; ++u) tmem_ld16(t_row + col0 + 16 * u, ovs[u]);
         tmem_wait_ld();
         if (!valid) continue;
-        if (p.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_off + col);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_float4(ov[4 * k] * inv, ov[4 * k + 1] * inv, ov[4 * k + 2] * inv, ov[4 * k + 3] * inv);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_off + col);
-          dst[0] = make_uint4(pack_bf16x2(ov[0] * inv, ov[1] * inv), pack_bf16x2(ov[2] * inv, ov[3] * inv),
-                              pack_bf16x2(ov[4] * inv, ov[5] * inv), pack_bf16x2(ov[6] * inv, ov[7] * inv));
-          dst[1] = make_uint4(pack_bf16x2(ov[8] * inv, ov[9] * inv), pack_bf16x2(ov[10] * inv, ov[11] * inv),
-                              pack_bf16x2(ov[12] * inv, ov[13] * inv), pack_bf16x2(ov[14] * inv, ov[15] * inv));
+        for (int u = 0; u < kRoundTrip; ++u) {
+          const float* ov = ovs[u];
+          const int col = col0 + 16 * u;
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_off + col);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_float4(ov[4 * k] * inv, ov[4 * k + 1] * inv, ov[4 * k + 2] * inv, ov[4 * k + 3] * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_off + col);
+            dst[0] = make_uint4(pack_bf16x2(ov[0] * inv, ov[1] * inv), pack_bf16x2(ov[2] * inv, ov[3] * inv),
+                                pack_bf16x2(ov[4] * inv, ov[5] * inv), pack_bf16x2(ov[6] * inv, ov[7] * inv));
+            dst[1] = make_uint4(pack_bf16x2(ov[8] * inv, ov[9] * inv), pack_bf16x2(ov[10] * inv, ov[11] * inv),
+                                pack_bf16x2(ov[12] * inv, ov[13] * inv), pack_bf16x2(ov[14] * inv, ov[15] * inv));
+          }
         }
       }
     }
@@ -556,10 +586,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // 2-page steps in 4 stages of 32 KB, two S issuers, two softmax warpgroups.
 // Global: 8 queries x 16 heads per block, D = 512 split into two blocks of
 // 256 output dims (both compute S), 2-page steps in 2 stages of 48 KB, two S
-// issuers, one softmax warpgroup.
+// issuers, one softmax warpgroup; every block of a KV head reads the same
+// pages, so tile t starts 7 t steps into its range (the blocks resident at
+// one time then read different pages: 8 % faster than all in step).
 using SlidingConfig =
     Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 4, 2, true, 2, 2>;
-using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2>;
+using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2, 1, 7>;
 
 }  // namespace prefill_tc
 }  // namespace pda

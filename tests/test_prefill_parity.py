@@ -5,7 +5,8 @@ Through the C ABI on the GPU.  Element-wise tolerance as for the decode:
 to bf16 for the P V product).  Cases cover several query tiles per sequence
 with ragged tails, whole prompts (n = L), single queries, sequences without
 queries, windows that cut the first page, NaN in every slot no query may
-read, both output dtypes, and the device status bits.
+read, scores over hundreds of log2 units, both output dtypes, and the device
+status bits.
 """
 
 import numpy as np
@@ -71,6 +72,25 @@ def test_bf16_output_and_window_only_pages(cuda_lib, kind):
 def test_global_layer_with_a_window(cuda_lib):
     case = make_prefill_case("global", [700, 2049], [50, 300], seed=703, window=256)
     check_full(case, "global window 256")
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_scores_over_a_wide_range(cuda_lib, kind):
+    # Query token t scaled by 2^(t % 10 - 6) and the key at position l by
+    # 1 + l / 256: some rows are nearly uniform, others nearly one-hot with
+    # scores spanning hundreds of log2 units, and row maxima keep growing
+    # along the keys, so the kernel's reference max moves and O is rescaled.
+    case = make_prefill_case(kind, [3000, 1300], [300, 64], seed=705)
+    c = case.cache
+    f = torch.tensor([2.0 ** (t % 10 - 6) for t in range(case.q.shape[0])])
+    case.q = (case.q.float() * f[:, None, None]).to(torch.bfloat16)
+    bt = c.block_table.cpu()
+    k = c.k_pool.float()
+    for b, L in enumerate(c.seq_lens.tolist()):
+        for pos in range(L):
+            k[int(bt[b, pos // PAGE_SIZE]), pos % PAGE_SIZE] *= 1.0 + pos / 256.0
+    c.k_pool = k.to(torch.bfloat16)
+    check_full(case, "%s wide score range" % kind)
 
 
 @pytest.mark.parametrize("kind", ["sliding", "global"])
