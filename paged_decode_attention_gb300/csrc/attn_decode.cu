@@ -18,6 +18,7 @@
 #include "global.cuh"
 #include "kv_append.cuh"
 #include "prefill_tc.cuh"
+#include "prefill_pair.cuh"
 #include "sliding.cuh"
 
 namespace {
@@ -615,9 +616,11 @@ extern "C" int32_t attn_selftest_wait_timeout(int32_t* status, void* stream) {
 
 namespace {
 
-// Multi-query attention over the paged cache (attn_prefill_*).
-template <typename C>
-int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+// Multi-query attention over the paged cache (attn_prefill_*): one CTA per
+// query tile (prefill_tc.cuh) or CTA pairs sharing each product
+// (prefill_pair.cuh, kPair).
+template <typename C, bool kPair, typename Kernel>
+int32_t run_prefill(Kernel kernel, int32_t kind, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
                     const int32_t* seq_lens, const int32_t* cu_q, void* o, int32_t batch, int32_t total_q,
                     int32_t max_q, int32_t max_blocks, int64_t num_pages, int32_t window, int32_t out_dtype,
                     int32_t* status, void* stream) {
@@ -648,11 +651,15 @@ int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void*
   int32_t st = current_device(&dev, &num_sms);
   if (st != ATTN_OK) return st;
   static bool smem_set[2][kMaxDevices] = {{false}};
-  if ((st = ensure_smem(pda::prefill_tc::prefill_tc_kernel<C>, C::kSmemBytes, dev, smem_set[kind]))) return st;
+  if ((st = ensure_smem(kernel, C::kSmemBytes, dev, smem_set[kind]))) return st;
 
-  CUtensorMap tm_k, tm_v;  // K: one page's 16 rows x 64 dims; V: a page's kDS dims of one KV head
-  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, 1))) return st;
-  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, C::kVChunks))) return st;
+  // K: a CTA pair holds one page of all D dims per CTA (one box); a single
+  // CTA one 64-dim chunk of a page per box.  V: a page's output dims of the
+  // CTA (half of kDS in a pair).
+  CUtensorMap tm_k, tm_v;
+  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, kPair ? C::kKChunks : 1))) return st;
+  if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, kPair ? C::kDS / 128 : C::kDS / 64)))
+    return st;
 
   pda::prefill_tc::PrefillParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -668,12 +675,30 @@ int32_t run_prefill(int32_t kind, const void* q, const void* k_pool, const void*
   p.total_q = total_q;
   p.max_q = max_q;
   p.out_f32 = out_dtype == ATTN_OUT_F32;
-  const dim3 grid((max_q + C::kQ - 1) / C::kQ, C::kHkv * C::kSlices, batch);
-  cudaError_t e = launch_pdl(pda::prefill_tc::prefill_tc_kernel<C>, grid, C::kThreads, C::kSmemBytes,
-                             static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
+  int tiles = (max_q + C::kQ - 1) / C::kQ;
+  if (kPair) tiles += tiles & 1;  // whole clusters of two query tiles
+  const dim3 grid(tiles, C::kHkv * C::kSlices, batch);
+  cudaError_t e = launch_pdl(kernel, grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
   return ATTN_OK;
+}
+
+// The prefill kernels in use: global layers on CTA pairs (each SM copies
+// half of every K and V tile: 290 -> 462 TFLOP/s on a 4096-token chunk of a
+// 32768-token context); sliding layers on single CTAs, which measured faster
+// there (609 against 338 TFLOP/s with pairs: their steps are bound by the
+// softmax and issue latency, which the pair's cross-SM handshakes lengthen).
+constexpr bool kSlidingPair = false;
+constexpr bool kGlobalPair = true;
+using kSlidingPrefill = pda::prefill_tc::SlidingConfig;
+using kGlobalPrefill = pda::prefill_pair::GlobalPairConfig;
+template <typename C, bool kPair>
+auto prefill_kernel() {
+  if constexpr (kPair)
+    return pda::prefill_pair::prefill_pair_kernel<C>;
+  else
+    return pda::prefill_tc::prefill_tc_kernel<C>;
 }
 
 }  // namespace
@@ -683,7 +708,7 @@ extern "C" int32_t attn_prefill_sliding(const void* q, const void* k_pool, const
                                         void* o, int32_t batch, int32_t total_q, int32_t max_q, int32_t max_blocks,
                                         int64_t num_pages, int32_t window, int32_t out_dtype, int32_t* status,
                                         void* stream) {
-  return run_prefill<pda::prefill_tc::SlidingConfig>(ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, cu_q,
+  return run_prefill<kSlidingPrefill, kSlidingPair>(prefill_kernel<kSlidingPrefill, kSlidingPair>(), ATTN_KIND_SLIDING, q, k_pool, v_pool, block_table, seq_lens, cu_q,
                                                   o, batch, total_q, max_q, max_blocks, num_pages, window, out_dtype,
                                                   status, stream);
 }
@@ -693,7 +718,7 @@ extern "C" int32_t attn_prefill_global(const void* q, const void* k_pool, const 
                                        void* o, int32_t batch, int32_t total_q, int32_t max_q, int32_t max_blocks,
                                        int64_t num_pages, int32_t window, int32_t out_dtype, int32_t* status,
                                        void* stream) {
-  return run_prefill<pda::prefill_tc::GlobalConfig>(ATTN_KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, cu_q, o,
+  return run_prefill<kGlobalPrefill, kGlobalPair>(prefill_kernel<kGlobalPrefill, kGlobalPair>(), ATTN_KIND_GLOBAL, q, k_pool, v_pool, block_table, seq_lens, cu_q, o,
                                                  batch, total_q, max_q, max_blocks, num_pages, window, out_dtype,
                                                  status, stream);
 }
