@@ -61,11 +61,14 @@ struct PairConfig {
   static constexpr int kSoftmaxGroups = kSoftmaxGroups_;
   static constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
   static constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
-  // + producer (warp 4) + issuer (warp 5 of rank 0; of rank 1 it forwards the
-  // stages) + two warps that forward rank 1's softmax arrivals to rank 0
+  // + producer (warp 4) + two more warps in each CTA.  Rank 0: warp 5
+  // issues the S products, warp kFwdSWarp the P V products (separate
+  // threads, so that S runs ahead of the softmax whatever P waits for).
+  // Rank 1: warp 5 forwards its stages, kFwdSWarp its s_free and q_ready
+  // phases, kFwdPWarp its p_full phases to rank 0.
   static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
-  static constexpr int kFwdSWarp = kSoftmaxWarps + 2;  // s_free (and q_ready)
-  static constexpr int kFwdPWarp = kSoftmaxWarps + 3;  // p_full
+  static constexpr int kFwdSWarp = kSoftmaxWarps + 2;
+  static constexpr int kFwdPWarp = kSoftmaxWarps + 3;
   static constexpr int kRotate = kRotate_;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = kDS;                 // two S buffers of kKeys columns
@@ -83,13 +86,13 @@ struct PairConfig {
     alignas(1024) uint8_t v[kStages][kVTile];
     alignas(8) uint64_t full[kStages];       // this CTA's copies of the stage landed (TMA)
     alignas(8) uint64_t peer_full[kStages];  // rank 0: rank 1's copies landed (forwarded)
-    alignas(8) uint64_t empty[kStages];      // the products reading the stage done (commit, both CTAs)
+    alignas(8) uint64_t empty[kStages];      // S and P V of the stage done (two commits, both CTAs)
     alignas(8) uint64_t s_full[2];           // S buffer written (commit, both CTAs)
     alignas(8) uint64_t s_free[2];           // S buffer read by this CTA's softmax warps (rank 0: and rank 1's)
     alignas(8) uint64_t p_full[2];           // P written, O rescaled, V edges zeroed (rank 0: both CTAs)
     alignas(8) uint64_t p_empty[2];          // P V of the buffer's step done (commit, both CTAs)
     alignas(8) uint64_t q_ready;             // Q tile written (rank 0: both CTAs)
-    alignas(8) uint64_t mma_done;            // every product done (commit, both CTAs)
+    alignas(8) uint64_t mma_done;            // every product done (one commit per issuer, both CTAs)
     uint32_t tmem_base;
     float half_max[2][kSoftmaxGroups][kRows];
     float half_sum[kSoftmaxGroups][kRows];
@@ -126,7 +129,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
       mbar_init(&s.peer_full[st], 1);
-      mbar_init(&s.empty[st], 1);
+      mbar_init(&s.empty[st], 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -135,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.p_empty[i], 1);
     }
     mbar_init(&s.q_ready, kArrivals);
-    mbar_init(&s.mma_done, 1);
+    mbar_init(&s.mma_done, 2);
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
@@ -248,24 +251,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         }
       }
     } else if (warp == 5 && rank == 0) {
-      // ---------------- rank 0: the pair's MMAs (whole warp, an elected lane issues) ----------------
+      // ---------------- rank 0: the pair's S products (whole warp, an elected lane issues) ----------------
       bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.q_ready, 0));
       const uint32_t q_base = smem_addr(s.q[0]);
-      auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
-        const int bp = j & 1;
-        const int st = j % kStages;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.p_full[bp], (j >> 1) & 1));
-        tc_fence_after_sync();
-        const uint32_t v_base = smem_addr(s.v[st]);
-#pragma unroll
-        for (int kk = 0; kk < kPPS; ++kk) {
-          const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kPageChunk, 1024, 2);
-          umma_bf16_ts_pair_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit_pair_warp(&s.empty[st]);
-        umma_commit_pair_warp(&s.p_empty[bp]);
-      };
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
         const int bs = j & 1;
@@ -281,12 +269,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
           umma_bf16_pair_warp(tmem + C::kSCol + C::kKeys * bs, a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit_pair_warp(&s.s_full[bs]);
-        if (j >= 1) pv(j - 1);
+        umma_commit_pair_warp(&s.empty[st]);  // K of the stage read
       }
-      pv(n_steps - 1);
       // the softmax warps' last arrivals on s_free (they are not waited for above)
       for (int j = n_steps >= 2 ? n_steps - 2 : 0; j < n_steps; ++j)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[j & 1], (j >> 1) & 1));
+      umma_commit_pair_warp(&s.mma_done);
+      if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
+      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+    } else if (warp == C::kFwdSWarp && rank == 0) {
+      // ---------------- rank 0: the pair's P V products, one of K = 16 per page ----------------
+      // V of step j landed before S(j) was issued, and P(j) exists only after S(j).
+      bool ok = true;
+      for (int j = 0; j < n_steps; ++j) {
+        const int bp = j & 1;
+        const int st = j % kStages;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.p_full[bp], (j >> 1) & 1));
+        tc_fence_after_sync();
+        const uint32_t v_base = smem_addr(s.v[st]);
+#pragma unroll
+        for (int kk = 0; kk < kPPS; ++kk) {
+          const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kPageChunk, 1024, 2);
+          umma_bf16_ts_pair_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit_pair_warp(&s.empty[st]);  // V of the stage read
+        umma_commit_pair_warp(&s.p_empty[bp]);
+      }
       umma_commit_pair_warp(&s.mma_done);
       if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
