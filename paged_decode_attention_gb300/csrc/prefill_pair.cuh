@@ -38,7 +38,7 @@ namespace prefill_pair {
 
 using prefill_tc::PrefillParams;
 
-template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kSoftmaxGroups_, int kRotate_>
+template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kSoftmaxGroups_, int kRotate_, int kSBufs_ = 2>
 struct PairConfig {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per pair (each CTA holds V for half of them)
@@ -71,12 +71,13 @@ struct PairConfig {
   static constexpr int kFwdPWarp = kSoftmaxWarps + 3;
   static constexpr int kRotate = kRotate_;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSCol = kDS;                 // two S buffers of kKeys columns
-  static constexpr uint32_t kPCol = kSCol + 2 * kKeys;   // two P buffers (bf16 pairs), kKeys / 2 columns each
+  static constexpr int kSBufs = kSBufs_;                  // S buffers: S runs up to kSBufs steps ahead
+  static constexpr uint32_t kSCol = kDS;                  // kSBufs S buffers of kKeys columns
+  static constexpr uint32_t kPCol = kSCol + kSBufs * kKeys;  // two P buffers (bf16 pairs), kKeys / 2 columns each
   static constexpr uint32_t kIdescS = umma_idesc_bf16(256, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(256, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 128 == 0 && kDS <= 256, "tile shapes");
-  static_assert(kPCol + kKeys <= kTmemCols, "O, two S buffers and two P buffers fit in tensor memory");
+  static_assert(kPCol + kKeys <= kTmemCols, "O, the S buffers and two P buffers fit in tensor memory");
   static_assert(kSoftmaxGroups == 1 || (kSoftmaxGroups == 2 && (kKeys / 2) % 16 == 0 && kDS % 32 == 0),
                 "two softmax warpgroups: halves of whole 16-key blocks");
 
@@ -87,8 +88,8 @@ struct PairConfig {
     alignas(8) uint64_t full[kStages];       // this CTA's copies of the stage landed (TMA)
     alignas(8) uint64_t peer_full[kStages];  // rank 0: rank 1's copies landed (forwarded)
     alignas(8) uint64_t empty[kStages];      // S and P V of the stage done (two commits, both CTAs)
-    alignas(8) uint64_t s_full[2];           // S buffer written (commit, both CTAs)
-    alignas(8) uint64_t s_free[2];           // S buffer read by this CTA's softmax warps (rank 0: and rank 1's)
+    alignas(8) uint64_t s_full[kSBufs];      // S buffer written (commit, both CTAs)
+    alignas(8) uint64_t s_free[kSBufs];      // S buffer read by this CTA's softmax warps (rank 0: and rank 1's)
     alignas(8) uint64_t p_full[2];           // P written, O rescaled, V edges zeroed (rank 0: both CTAs)
     alignas(8) uint64_t p_empty[2];          // P V of the buffer's step done (commit, both CTAs)
     alignas(8) uint64_t q_ready;             // Q tile written (rank 0: both CTAs)
@@ -131,9 +132,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.peer_full[st], 1);
       mbar_init(&s.empty[st], 2);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], kArrivals);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s.p_full[i], kArrivals);
       mbar_init(&s.p_empty[i], 1);
     }
@@ -256,10 +259,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       const uint32_t q_base = smem_addr(s.q[0]);
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
-        const int bs = j & 1;
+        const int bs = j % C::kSBufs;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.peer_full[st], (j / kStages) & 1));
-        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[bs], ((j - 2) >> 1) & 1));
+        if (ok && j >= C::kSBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
         tc_fence_after_sync();
         const uint32_t k_base = smem_addr(s.k[st]);
 #pragma unroll
@@ -272,8 +276,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         umma_commit_pair_warp(&s.empty[st]);  // K of the stage read
       }
       // the softmax warps' last arrivals on s_free (they are not waited for above)
-      for (int j = n_steps >= 2 ? n_steps - 2 : 0; j < n_steps; ++j)
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[j & 1], (j >> 1) & 1));
+      for (int j = n_steps >= C::kSBufs ? n_steps - C::kSBufs : 0; j < n_steps; ++j)
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[j % C::kSBufs], (j / C::kSBufs) & 1));
       umma_commit_pair_warp(&s.mma_done);
       if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -306,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (lane == 0) mbar_arrive_cluster(peer_full0 + 8 * st);
+        if (lane == 0) mbar_arrive_cluster_relaxed(peer_full0 + 8 * st);
       }
       if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // rank 0's last product
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -320,10 +324,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
           if (lane == 0) mbar_arrive_cluster(at_rank0(&s.q_ready));
         }
         const uint32_t dst0 = at_rank0(fwd_s ? &s.s_free[0] : &s.p_full[0]);
+        const int nbuf = fwd_s ? C::kSBufs : 2;
         for (int j = 0; j < n_steps; ++j) {
-          const int bs = j & 1;
-          if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(fwd_s ? &s.s_free[bs] : &s.p_full[bs], (j >> 1) & 1));
-          if (lane == 0) mbar_arrive_cluster(dst0 + 8 * bs);
+          const int bs = j % nbuf;
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(fwd_s ? &s.s_free[bs] : &s.p_full[bs], (j / nbuf) & 1));
+          if (lane == 0) {
+            // s_free relays finished loads (no data); p_full publishes P and zeroed V rows
+            if (fwd_s)
+              mbar_arrive_cluster_relaxed(dst0 + 8 * bs);
+            else
+              mbar_arrive_cluster(dst0 + 8 * bs);
+          }
         }
         if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       }
@@ -365,19 +376,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
-        const int bs = j & 1;
+        const int bs = j & 1;              // P buffer
+        const int sb = j % C::kSBufs;      // S buffer
         const int step0 = (page0 + logical_step(j) * kPPS) * kPage;  // key of the step's column 0
         const int pos0 = step0 + kc0;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (j >> 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[sb], (j / C::kSBufs) & 1));
         tc_fence_after_sync();
         float sv[kHalf];
 #pragma unroll
         for (int blk = 0; blk < kHalf / 16; ++blk)
-          tmem_ld16(t_row + C::kSCol + C::kKeys * bs + kc0 + 16 * blk, *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+          tmem_ld16(t_row + C::kSCol + C::kKeys * sb + kc0 + 16 * blk, *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.s_free[bs]);
+        if (lane == 0) mbar_arrive(&s.s_free[sb]);
 
         if (!valid || pos0 < lo_r || pos0 + kHalf - 1 > pos) {
 #pragma unroll
@@ -512,10 +524,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
 // stages, two softmax warpgroups.  Global: each CTA 8 queries x 16 heads, D
 // = 512 split into two slices of 256 output dims (both compute S), its stage
 // 16 KB of K and 8 KB of V, 4 stages, one softmax warpgroup, the step order
-// rotated by pair.
+// rotated by pair, three S buffers (655 against 646 TFLOP/s with two).
 using SlidingPairConfig =
     PairConfig<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 8, 2, 0>;
-using GlobalPairConfig = PairConfig<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 4, 1, 7>;
+using GlobalPairConfig = PairConfig<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 4, 1, 7, 3>;
 
 }  // namespace prefill_pair
 }  // namespace pda
