@@ -38,7 +38,8 @@ namespace prefill_pair {
 
 using prefill_tc::PrefillParams;
 
-template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kSoftmaxGroups_, int kRotate_, int kSBufs_ = 2>
+template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kSoftmaxGroups_, int kRotate_, int kSBufs_ = 2,
+          int kPBufs_ = 2>
 struct PairConfig {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per pair (each CTA holds V for half of them)
@@ -73,11 +74,12 @@ struct PairConfig {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSBufs = kSBufs_;                  // S buffers: S runs up to kSBufs steps ahead
   static constexpr uint32_t kSCol = kDS;                  // kSBufs S buffers of kKeys columns
-  static constexpr uint32_t kPCol = kSCol + kSBufs * kKeys;  // two P buffers (bf16 pairs), kKeys / 2 columns each
+  static constexpr int kPBufs = kPBufs_;                  // P buffers: P V may lag the softmax by kPBufs - 1 steps
+  static constexpr uint32_t kPCol = kSCol + kSBufs * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
   static constexpr uint32_t kIdescS = umma_idesc_bf16(256, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(256, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 128 == 0 && kDS <= 256, "tile shapes");
-  static_assert(kPCol + kKeys <= kTmemCols, "O, the S buffers and two P buffers fit in tensor memory");
+  static_assert(kPCol + kPBufs * kKeys / 2 <= kTmemCols, "O, the S buffers and the P buffers fit in tensor memory");
   static_assert(kSoftmaxGroups == 1 || (kSoftmaxGroups == 2 && (kKeys / 2) % 16 == 0 && kDS % 32 == 0),
                 "two softmax warpgroups: halves of whole 16-key blocks");
 
@@ -90,8 +92,8 @@ struct PairConfig {
     alignas(8) uint64_t empty[kStages];      // S and P V of the stage done (two commits, both CTAs)
     alignas(8) uint64_t s_full[kSBufs];      // S buffer written (commit, both CTAs)
     alignas(8) uint64_t s_free[kSBufs];      // S buffer read by this CTA's softmax warps (rank 0: and rank 1's)
-    alignas(8) uint64_t p_full[2];           // P written, O rescaled, V edges zeroed (rank 0: both CTAs)
-    alignas(8) uint64_t p_empty[2];          // P V of the buffer's step done (commit, both CTAs)
+    alignas(8) uint64_t p_full[kPBufs];      // P written, O rescaled, V edges zeroed (rank 0: both CTAs)
+    alignas(8) uint64_t p_empty[kPBufs];     // P V of the buffer's step done (commit, both CTAs)
     alignas(8) uint64_t q_ready;             // Q tile written (rank 0: both CTAs)
     alignas(8) uint64_t mma_done;            // every product done (one commit per issuer, both CTAs)
     uint32_t tmem_base;
@@ -136,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], kArrivals);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kPBufs; ++i) {
       mbar_init(&s.p_full[i], kArrivals);
       mbar_init(&s.p_empty[i], 1);
     }
@@ -286,9 +288,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       // V of step j landed before S(j) was issued, and P(j) exists only after S(j).
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
-        const int bp = j & 1;
+        const int bp = j % C::kPBufs;
         const int st = j % kStages;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.p_full[bp], (j >> 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.p_full[bp], (j / C::kPBufs) & 1));
         tc_fence_after_sync();
         const uint32_t v_base = smem_addr(s.v[st]);
 #pragma unroll
@@ -324,16 +326,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
           if (lane == 0) mbar_arrive_cluster(at_rank0(&s.q_ready));
         }
         const uint32_t dst0 = at_rank0(fwd_s ? &s.s_free[0] : &s.p_full[0]);
-        const int nbuf = fwd_s ? C::kSBufs : 2;
+        const int nbuf = fwd_s ? C::kSBufs : C::kPBufs;
         for (int j = 0; j < n_steps; ++j) {
           const int bs = j % nbuf;
           if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(fwd_s ? &s.s_free[bs] : &s.p_full[bs], (j / nbuf) & 1));
           if (lane == 0) {
-            // s_free relays finished loads (no data); p_full publishes P and zeroed V rows
-            if (fwd_s)
-              mbar_arrive_cluster_relaxed(dst0 + 8 * bs);
-            else
+            // s_free relays finished tensor-memory loads and p_full finished
+            // tensor-memory stores (tcgen05.wait::ld / ::st): no data to
+            // publish, except the V rows that the first and last steps zero
+            // in shared memory
+            const int step0 = (page0 + logical_step(j) * kPPS) * kPage;
+            if (!fwd_s && (step0 < k_lo || step0 + C::kKeys - 1 > k_hi))
               mbar_arrive_cluster(dst0 + 8 * bs);
+            else
+              mbar_arrive_cluster_relaxed(dst0 + 8 * bs);
           }
         }
         if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -376,7 +382,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
-        const int bs = j & 1;              // P buffer
+        const int bs = j & 1;              // exchange buffer of the row maxima
+        const int pb = j % C::kPBufs;      // P buffer
         const int sb = j % C::kSBufs;      // S buffer
         const int step0 = (page0 + logical_step(j) * kPPS) * kPage;  // key of the step's column 0
         const int pos0 = step0 + kc0;
@@ -410,7 +417,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         const bool move = m_new > m + kSlack;
         const bool rescale = move && m != -INFINITY;
         if (__any_sync(0xffffffffu, rescale)) {
-          if (ok && j >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          if (ok && j >= 1)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_fast(&s.p_empty[(j - 1) % C::kPBufs], ((j - 1) / C::kPBufs) & 1));
           tc_fence_after_sync();
           const float f = rescale ? ex2_approx(m - (m_new + kHeadroom)) : 1.f;
 #pragma unroll 1
@@ -439,14 +448,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         }
         l += ls;
 
-        // P row into buffer bs once P V of step j-2 has read it
-        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[bs], ((j - 2) >> 1) & 1));
+        // P row into buffer pb once P V of step j - kPBufs has read it
+        if (ok && j >= C::kPBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[pb], ((j / C::kPBufs) - 1) & 1));
 #pragma unroll
         for (int kc = 0; kc < kHalf / 16; ++kc) {
           uint32_t w[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
-          tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * bs + kc0 / 2 + 8 * kc, w);
+          tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, w);
         }
         tmem_wait_st();
         // zero this CTA's V rows outside [k_lo, k_hi] (the first and last steps)
@@ -467,12 +477,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.p_full[bs]);
+        if (lane == 0) mbar_arrive(&s.p_full[pb]);
       }
 
-      // ---- epilogue: wait for the last two P V products, normalise, write this row's output dims ----
-      for (int j = n_steps >= 2 ? n_steps - 2 : 0; j < n_steps; ++j)
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[j & 1], (j >> 1) & 1));
+      // ---- epilogue: wait for the last P V products, normalise, write this row's output dims ----
+      for (int j = n_steps >= C::kPBufs ? n_steps - C::kPBufs : 0; j < n_steps; ++j)
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[j % C::kPBufs], (j / C::kPBufs) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       tc_fence_after_sync();
       if constexpr (kGroups == 2) {
