@@ -75,7 +75,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 }
 
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
-          int kSoftmaxGroups_ = 1, int kRotate_ = 0>
+          int kSoftmaxGroups_ = 1, int kRotate_ = 0, int kSBufs_ = 2, int kPBufs_ = 2>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
@@ -114,14 +114,19 @@ struct Config {
   // one time read different pages (the softmax does not depend on the order
   // of the keys).
   static constexpr int kRotate = kRotate_;
+  // S and P buffers in tensor memory: S runs up to kSBufs steps ahead of the
+  // softmax, P V may lag it by kPBufs - 1 steps.
+  static constexpr int kSBufs = kSBufs_;
+  static constexpr int kPBufs = kPBufs_;
   static constexpr int kThreads = (4 * kSoftmaxGroups + 1 + kIssuers) * 32;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSCol = kDS;  // S buffers: column kSCol + kKeys (kIssuers buffer + half)
-  static constexpr uint32_t kPCol = kSCol + 2 * kIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
+  static constexpr uint32_t kSCol = kDS;  // S buffers: column kSCol + kKeys (kIssuers buffer + part)
+  static constexpr uint32_t kPCol = kSCol + kSBufs * kIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
-  static_assert(kPCol + (kPInTmem ? kKeys : 0) <= kTmemCols, "O, two S buffers and P fit in tensor memory");
+  static_assert(kPCol + (kPInTmem ? kPBufs * kKeys / 2 : 0) <= kTmemCols, "O, the S buffers and P fit in tensor memory");
+  static_assert(kPInTmem || kPBufs == 2, "P in shared memory: two buffers");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
   static_assert(kIssuers >= 1 && kIssuers <= kD / 16, "S k-steps split among the issuers");
   static_assert(kSoftmaxGroups == 1 || (kSoftmaxGroups == 2 && kPInTmem && (kKeys / 2) % 16 == 0 && kDS % 32 == 0),
@@ -134,10 +139,10 @@ struct Config {
     alignas(128) uint8_t p[kPInTmem ? 1 : 2][kPInTmem ? 16 : kPBytes];
     alignas(8) uint64_t full[kStages];   // K and V of the stage landed (TMA)
     alignas(8) uint64_t empty[kStages];  // both products of the stage's page done (commit)
-    alignas(8) uint64_t s_full[2];       // S buffer written (commit)
-    alignas(8) uint64_t s_free[2];       // S buffer read (4 softmax warps)
-    alignas(8) uint64_t p_full[2];       // P buffer written, O rescaled, V edges zeroed (4 warps)
-    alignas(8) uint64_t p_empty[2];      // P V of the buffer's page done (commit)
+    alignas(8) uint64_t s_full[kSBufs];   // S buffer written (commit)
+    alignas(8) uint64_t s_free[kSBufs];   // S buffer read (the softmax warps)
+    alignas(8) uint64_t p_full[kPBufs];   // P buffer written, O rescaled, V edges zeroed (the softmax warps)
+    alignas(8) uint64_t p_empty[kPBufs];  // P V of the buffer's step done (commit)
     alignas(8) uint64_t q_ready;         // Q tile written (4 warps)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
     uint32_t tmem_base;
@@ -182,9 +187,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.full[st], 1);
       mbar_init(&s.empty[st], C::kIssuers);  // every issuer's products of the stage done
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&s.s_full[i], C::kIssuers);
       mbar_init(&s.s_free[i], 4 * C::kSoftmaxGroups);
+    }
+    for (int i = 0; i < C::kPBufs; ++i) {
       mbar_init(&s.p_full[i], 4 * C::kSoftmaxGroups);
       mbar_init(&s.p_empty[i], 1);
     }
@@ -308,9 +315,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       bool ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, 0));
       const uint32_t q_base = smem_addr(s.q[0]);
       auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
-        const int bp = j & 1;
+        const int bp = j % C::kPBufs;
         const int st = j % kStages;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[bp], (j >> 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[bp], (j / C::kPBufs) & 1));
         tc_fence_after_sync();
         const uint32_t v_base = smem_addr(s.v[st]);
 #pragma unroll
@@ -329,9 +336,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       };
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
-        const int bs = j & 1;
+        const int bs = j % C::kSBufs;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j - 2) >> 1) & 1));
+        if (ok && j >= C::kSBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
         tc_fence_after_sync();
         const uint32_t k_base = smem_addr(s.k[st]);
 #pragma unroll
@@ -356,9 +364,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t q_base = smem_addr(s.q[0]) + (part * kPart / 4) * C::kQChunkBytes;
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
-        const int bs = j & 1;
+        const int bs = j % C::kSBufs;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j - 2) >> 1) & 1));
+        if (ok && j >= C::kSBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
         tc_fence_after_sync();
         const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kChunkRows;
 #pragma unroll
@@ -416,10 +425,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this thread's share of the row sum
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
-        const int bs = j & 1;
+        const int bs = j % C::kSBufs;  // S buffer
+        const int pb = j % C::kPBufs;  // P buffer
+        const int xb = j & 1;          // exchange buffer of the half-row maxima
         const int step0 = (page0 + logical_step(j) * kPPS) * kPage;  // key of the step's column 0
         const int pos0 = step0 + kc0;                   // key of this thread's first column
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (j >> 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (j / C::kSBufs) & 1));
         tc_fence_after_sync();
         float sv[kHalf];
 #pragma unroll
@@ -453,16 +464,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int k = 1; k < kHalf; ++k) mx = fmaxf(mx, sv[k]);
         if constexpr (kGroups == 2) {
-          s.half_max[bs][h][r] = mx;
+          s.half_max[xb][h][r] = mx;
           named_barrier_sync(1, C::kSoftmaxThreads);
-          mx = fmaxf(mx, s.half_max[bs][1 - h][r]);
+          mx = fmaxf(mx, s.half_max[xb][1 - h][r]);
         }
         const float m_new = mx * kLog2e;
         const bool move = m_new > m + kSlack;  // false while the row has no visible key
         const bool rescale = move && m != -INFINITY;
         if (__any_sync(0xffffffffu, rescale)) {
           // O's row holds P V up to step j-1: wait for that product, then scale in place
-          if (ok && j >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          if (ok && j >= 1)
+            ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(j - 1) % C::kPBufs], ((j - 1) / C::kPBufs) & 1));
           tc_fence_after_sync();
           const float f = rescale ? ex2_approx(m - (m_new + kHeadroom)) : 1.f;
 #pragma unroll 1
@@ -491,21 +503,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         l += ls;
 
-        // P row into buffer bs (K-major core matrices of 8 rows x 8 keys) once
-        // P V of step j-2 has read it
-        if (ok && j >= 2) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[bs], ((j - 2) >> 1) & 1));
+        // P row into buffer pb (K-major core matrices of 8 rows x 8 keys) once
+        // P V of step j - kPBufs has read it
+        if (ok && j >= C::kPBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[pb], ((j / C::kPBufs) - 1) & 1));
         if constexpr (C::kPInTmem) {
-          // this row's keys into its lane: column kPCol + (kKeys / 2) bs + k / 2 holds keys k, k + 1
+          // this row's keys into its lane: column kPCol + (kKeys / 2) pb + k / 2 holds keys k, k + 1
 #pragma unroll
           for (int kc = 0; kc < kHalf / 16; ++kc) {
             uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
-            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * bs + kc0 / 2 + 8 * kc, w);
+            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, w);
           }
           tmem_wait_st();
         } else {
-          const uint32_t p_row = smem_addr(s.p[bs]) + (r >> 3) * (C::kKeys * 16) + (r & 7) * 16;
+          const uint32_t p_row = smem_addr(s.p[pb]) + (r >> 3) * (C::kKeys * 16) + (r & 7) * 16;
 #pragma unroll
           for (int kc = 0; kc < C::kKeys / 8; ++kc)
             st_shared_v4(p_row + kc * 128,
@@ -531,11 +544,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.p_full[bs]);
+        if (lane == 0) mbar_arrive(&s.p_full[pb]);
       }
 
       // ---- epilogue: wait for the last P V, normalise, write this row's output dims ----
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1));
+      if (ok)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_fast(&s.p_empty[(n_steps - 1) % C::kPBufs], ((n_steps - 1) / C::kPBufs) & 1));
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       tc_fence_after_sync();
       if constexpr (kGroups == 2) {
