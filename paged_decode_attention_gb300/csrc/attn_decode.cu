@@ -222,6 +222,25 @@ int32_t encode_chunk_map(CUtensorMap* map, const void* pool, int64_t num_pages, 
   return ATTN_OK;
 }
 
+// Q [total_q, Hq, D] as {64 dims, D/64 chunks, total_q queries, Hq heads}:
+// a box {64, 1, kQ, G} copies one 64-dim chunk of kQ consecutive queries for
+// the G heads of a KV head as [head][query][64 dims], 128-byte swizzled (the
+// single-CTA prefill's row order); queries past total_q read as zeros.
+int32_t encode_q_map(CUtensorMap* map, const void* q, int32_t total_q, int hq, int d, int g, int nq) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(d / 64), static_cast<cuuint64_t>(total_q),
+                              static_cast<cuuint64_t>(hq)};
+  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(hq) * d * 2, static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(nq), static_cast<cuuint32_t>(g)};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, elem_strides,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (q map) failed (%d)", static_cast<int>(r));
+  return ATTN_OK;
+}
+
 template <typename Kernel>
 int32_t ensure_smem(Kernel kernel, size_t bytes, int dev, bool* done) {
   if (done[dev]) return ATTN_OK;
@@ -678,7 +697,14 @@ int32_t run_prefill(Kernel kernel, int32_t kind, const void* q, const void* k_po
   int tiles = (max_q + C::kQ - 1) / C::kQ;
   if (kPair) tiles += tiles & 1;  // whole clusters of two query tiles
   const dim3 grid(tiles, C::kHkv * C::kSlices, batch);
-  cudaError_t e = launch_pdl(kernel, grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
+  cudaError_t e = cudaSuccess;
+  if constexpr (kPair) {
+    e = launch_pdl(kernel, grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
+  } else {
+    CUtensorMap tm_q;  // the tile's Q in one box per 64-dim chunk
+    if ((st = encode_q_map(&tm_q, q, total_q, C::kHq, C::kD, C::kG, C::kQ))) return st;
+    e = launch_pdl(kernel, grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_k, tm_v, tm_q, p);
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
   return ATTN_OK;

@@ -74,6 +74,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 4-D tile copy: Q as {64 dims, chunk, query, head}; a box {64, 1, kQ, G}
+// lands as [head][query][128 B], the tile's row order.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+      : "memory");
+}
+
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
           int kSoftmaxGroups_ = 1, int kRotate_ = 0, int kSBufs_ = 2, int kPBufs_ = 2>
 struct Config {
@@ -143,7 +154,7 @@ struct Config {
     alignas(8) uint64_t s_free[kSBufs];   // S buffer read (the softmax warps)
     alignas(8) uint64_t p_full[kPBufs];   // P buffer written, O rescaled, V edges zeroed (the softmax warps)
     alignas(8) uint64_t p_empty[kPBufs];  // P V of the buffer's step done (commit)
-    alignas(8) uint64_t q_ready;         // Q tile written (4 warps)
+    alignas(8) uint64_t q_ready;         // Q tile landed (TMA)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
     uint32_t tmem_base;
     float half_max[2][kSoftmaxGroups][kRows];  // two warpgroups: each half-row's max, by step parity
@@ -168,7 +179,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 template <typename C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ PrefillParams p) {
   constexpr int kD = C::kD, kDS = C::kDS, kG = C::kG, kHq = C::kHq, kQ = C::kQ, kStages = C::kStages;
   constexpr int kPPS = C::kPPS;
   extern __shared__ uint8_t smem_raw[];
@@ -195,13 +206,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.p_full[i], 4 * C::kSoftmaxGroups);
       mbar_init(&s.p_empty[i], 1);
     }
-    mbar_init(&s.q_ready, 4 * C::kSoftmaxGroups);
+    mbar_init(&s.q_ready, 1);
     mbar_init(&s.mma_done, C::kIssuers);
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
+    prefetch_tensor_map(&tm_q);
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, C::kTmemCols);
   tc_fence_before_sync();
@@ -254,8 +266,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // Lane pg < kPPS copies page pg of the step chunk by chunk, so that the
       // step's pages sit contiguously in each [kKeys rows][64 dims] chunk.
       // Pages past the range (the last step) and bad page ids are copied from
-      // a fully out-of-range row: zeros.
+      // a fully out-of-range row: zeros.  First the Q tile: lane ch copies
+      // its 64-dim chunk ch, G heads x kQ queries in one box (queries past
+      // the block's own are copied too and masked by the softmax; queries
+      // past total_q read as zeros).
       static_assert(32 % kPPS == 0, "a step's pages in one batch of 32 table entries");
+      static_assert(C::kKChunks <= 32, "one lane per Q chunk");
+      if (lane == 0) mbar_arrive_expect_tx(&s.q_ready, C::kKChunks * C::kQChunkBytes);
+      __syncwarp();
+      if (lane < C::kKChunks)
+        tma_load_4d(s.q[lane], &tm_q, 0, lane, q0 + i0, c * kG, &s.q_ready);
       const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
       bool ok = true;
       int issued = 0;
@@ -305,6 +325,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         __syncwarp();
       }
       if (lane == 0) {  // no copy may still be landing when the block retires
+        if (!mbar_wait(&s.q_ready, 0)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
         for (int st = 0; st < kStages && st < issued; ++st) {
           const int uses = (issued - 1 - st) / kStages + 1;
           if (!mbar_wait(&s.full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -404,23 +425,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int pos = P0 + qi;
       const int lo_r = p.window > 0 ? pos - p.window + 1 : 0;
       const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-
-      // Q row into shared memory: K-major, 128-byte swizzle, chunks of 64 dims
-      // (each group copies its share of the row's 16-byte units)
-      {
-        const uint8_t* src_row = reinterpret_cast<const uint8_t*>(
-            p.q + (static_cast<size_t>(valid ? q0 + i0 + qi : 0) * kHq + head) * kD);
-        const uint32_t q_base = smem_addr(s.q[0]);
-        constexpr int kUnits = kD / 8 / kGroups;
-#pragma unroll 8
-        for (int u = h * kUnits; u < (h + 1) * kUnits; ++u)
-          cp_async_16(q_base + (u >> 3) * C::kQChunkBytes + r * 128 + (((u & 7) ^ (r & 7)) << 4), src_row + 16 * u,
-                      valid ? 16u : 0u);
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.q_ready);
-      }
 
       float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this thread's share of the row sum
       bool ok = true;
