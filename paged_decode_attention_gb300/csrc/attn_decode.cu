@@ -635,6 +635,9 @@ extern "C" int32_t attn_selftest_wait_timeout(int32_t* status, void* stream) {
 
 namespace {
 
+// Single-CTA prefill grid: one CTA per SM looping over the work items.
+constexpr bool kPersistentPrefill = true;
+
 // Multi-query attention over the paged cache (attn_prefill_*): one CTA per
 // query tile (prefill_tc.cuh) or CTA pairs sharing each product
 // (prefill_pair.cuh, kPair).
@@ -703,7 +706,12 @@ int32_t run_prefill(Kernel kernel, int32_t kind, const void* q, const void* k_po
   } else {
     CUtensorMap tm_q;  // the tile's Q in one box per 64-dim chunk
     if ((st = encode_q_map(&tm_q, q, total_q, C::kHq, C::kD, C::kG, C::kQ))) return st;
-    e = launch_pdl(kernel, grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_k, tm_v, tm_q, p);
+    // one CTA per SM looping over the work items (query tile, KV head and
+    // slice, sequence), or one CTA per item
+    const int64_t work = static_cast<int64_t>(tiles) * C::kHkv * C::kSlices * batch;
+    const int64_t ctas = kPersistentPrefill ? std::min<int64_t>(work, std::max(1, num_sms)) : work;
+    e = launch_pdl(kernel, dim3(static_cast<unsigned>(ctas)), C::kThreads, C::kSmemBytes,
+                   static_cast<cudaStream_t>(stream), tm_k, tm_v, tm_q, p);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));

@@ -154,7 +154,10 @@ struct Config {
     alignas(8) uint64_t s_free[kSBufs];   // S buffer read (the softmax warps)
     alignas(8) uint64_t p_full[kPBufs];   // P buffer written, O rescaled, V edges zeroed (the softmax warps)
     alignas(8) uint64_t p_empty[kPBufs];  // P V of the buffer's step done (commit)
-    alignas(8) uint64_t q_ready;         // Q tile landed (TMA)
+    alignas(8) uint64_t q_ready;         // the item's Q tile landed (TMA)
+    alignas(8) uint64_t q_empty;         // the item's S products done (one commit per issuer)
+    alignas(8) uint64_t o_full;          // the item's last P V done (commit)
+    alignas(8) uint64_t o_free;          // O read by the item's epilogue (the softmax warps)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
     uint32_t tmem_base;
     float half_max[2][kSoftmaxGroups][kRows];  // two warpgroups: each half-row's max, by step parity
@@ -176,6 +179,73 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// One work item (a query tile of one sequence, KV head and output slice) as
+// every role of the CTA sees it.
+struct TileItem {
+  bool run;
+  int c, slice, b, tile;  // KV head, output slice, sequence, query tile
+  int q0, i0, nq, P0;     // first packed query row, the tile's first query, its valid queries, its first position
+  int k_lo, k_hi;         // keys the tile sees (inclusive)
+  int page0, n_pages, n_steps, rot;
+};
+
+template <typename C>
+__device__ __forceinline__ TileItem load_tile(const PrefillParams& p, int w, int tiles, bool reporter) {
+  constexpr int kQ = C::kQ, kPPS = C::kPPS;
+  TileItem it{};
+  it.tile = w % tiles;
+  const int rest = w / tiles;
+  const int y = rest % (C::kHkv * C::kSlices);
+  it.b = rest / (C::kHkv * C::kSlices);
+  it.c = y / C::kSlices;
+  it.slice = y % C::kSlices;
+  it.q0 = p.cu_q[it.b];
+  const int n = p.cu_q[it.b + 1] - it.q0;
+  it.i0 = it.tile * kQ;
+  const int L = p.seq_lens[it.b];
+  const int cap = p.max_blocks < ATTN_MAX_SEQ_LEN / kPage ? p.max_blocks * kPage : ATTN_MAX_SEQ_LEN;
+  it.run = false;
+  if (n < 0 || it.q0 < 0 || static_cast<int64_t>(it.q0) + n > p.total_q) {
+    if (reporter) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
+    return it;
+  }
+  if (n > p.max_q && it.tile == 0 && y == 0 && reporter)
+    report(p.status, ATTN_DEV_BAD_SEQ_LEN);  // more queries than the host's max_q: the rest are not computed
+  const int n_run = n < p.max_q ? n : p.max_q;
+  if (it.i0 >= n_run) return it;
+  if (L < n || L > cap) {
+    if (reporter) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
+    return it;
+  }
+  it.run = true;
+  it.nq = n_run - it.i0 < kQ ? n_run - it.i0 : kQ;
+  it.P0 = L - n + it.i0;
+  it.k_hi = it.P0 + it.nq - 1;
+  it.k_lo = p.window > 0 ? (it.P0 - p.window + 1 > 0 ? it.P0 - p.window + 1 : 0) : 0;
+  it.page0 = it.k_lo / kPage;
+  it.n_pages = it.k_hi / kPage - it.page0 + 1;
+  it.n_steps = (it.n_pages + kPPS - 1) / kPPS;
+  it.rot = C::kRotate > 0 ? static_cast<int>((static_cast<int64_t>(it.tile) * C::kRotate) % it.n_steps) : 0;
+  return it;
+}
+
+// step j of the copy order covers logical step (j + rot) mod n_steps
+__device__ __forceinline__ int tile_step(const TileItem& it, int j) {
+  return j + it.rot < it.n_steps ? j + it.rot : j + it.rot - it.n_steps;
+}
+
+// A value every lane of the warp holds, marked as such for the compiler, so
+// that MMA descriptors derived from it stay in uniform registers.
+__device__ __forceinline__ int warp_uniform_int(int v) { return __shfl_sync(0xffffffffu, v, 0); }
+
+// The grid holds one CTA per work item, or fewer (one per SM) that loop over
+// the items: work item w = tile + tiles * (c * kSlices + slice + Hkv kSlices b),
+// CTA g taking g, g + gridDim.x, ...  Every pipeline (stages, S and P
+// buffers) runs on counters that continue from one item to the next, so the
+// next item's Q and pages stream in, and its first S products run, while the
+// last item's softmax and epilogue finish.  Q is one buffer, refilled once
+// the item's S products are done (q_empty); O passes from an item's epilogue
+// to the next item's first P V product through o_full / o_free.
 template <typename C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -186,12 +256,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   typename C::Smem& s =
       *reinterpret_cast<typename C::Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int tile = blockIdx.x;
-  const int c = blockIdx.y / C::kSlices;
-  const int slice = blockIdx.y % C::kSlices;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int tiles = (p.max_q + kQ - 1) / kQ;
+  const int n_work = tiles * C::kHkv * C::kSlices * p.batch;
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -207,6 +275,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.p_empty[i], 1);
     }
     mbar_init(&s.q_ready, 1);
+    mbar_init(&s.q_empty, C::kIssuers);
+    mbar_init(&s.o_full, 1);
+    mbar_init(&s.o_free, 4 * C::kSoftmaxGroups);
     mbar_init(&s.mma_done, C::kIssuers);
     fence_mbar_init();
   }
@@ -225,90 +296,58 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   wait_for_primary_grid();
   allow_dependent_launch();
 
-  // ---- this block's queries and the keys they can see (uniform) ----
-  const int q0 = p.cu_q[b];
-  const int n = p.cu_q[b + 1] - q0;
-  const int i0 = tile * kQ;
-  const int L = p.seq_lens[b];
-  const int cap = p.max_blocks < ATTN_MAX_SEQ_LEN / kPage ? p.max_blocks * kPage : ATTN_MAX_SEQ_LEN;
-  bool run = true;
-  if (n < 0 || q0 < 0 || static_cast<int64_t>(q0) + n > p.total_q) {
-    if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
-    run = false;
-  } else {
-    if (n > p.max_q && tile == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-      report(p.status, ATTN_DEV_BAD_SEQ_LEN);  // more queries than the host's max_q: the rest are not computed
-    if (i0 >= (n < p.max_q ? n : p.max_q)) {
-      run = false;
-    } else if (L < n || L > cap) {
-      if (threadIdx.x == 0) report(p.status, ATTN_DEV_BAD_SEQ_LEN);
-      run = false;
-    }
-  }
-
-  if (run) {
-    const int P0 = L - n + i0;                   // position of the block's first query
-    const int n_run = n < p.max_q ? n : p.max_q;   // queries computed
-    const int nq = n_run - i0 < kQ ? n_run - i0 : kQ;  // valid queries in the block
-    const int k_hi = P0 + nq - 1;                // last visible key (inclusive)
-    const int k_lo = p.window > 0 ? (P0 - p.window + 1 > 0 ? P0 - p.window + 1 : 0) : 0;
-    const int page0 = k_lo / kPage;
-    const int n_pages = k_hi / kPage - page0 + 1;
-    const int n_steps = (n_pages + kPPS - 1) / kPPS;
-    const int rot = C::kRotate > 0 ? static_cast<int>((static_cast<int64_t>(tile) * C::kRotate) % n_steps) : 0;
-    // step j of the copy order covers logical step (j + rot) mod n_steps;
-    // page gp of the copy order is logical page logical_page(gp)
-    const auto logical_step = [&](int j) { return j + rot < n_steps ? j + rot : j + rot - n_steps; };
-    const auto logical_page = [&](int gp) { return logical_step(gp / kPPS) * kPPS + gp % kPPS; };
-
-    if (warp == 4) {
-      // ---------------- producer: step i = pages page0 + i*kPPS ... ----------------
-      // Lane pg < kPPS copies page pg of the step chunk by chunk, so that the
-      // step's pages sit contiguously in each [kKeys rows][64 dims] chunk.
-      // Pages past the range (the last step) and bad page ids are copied from
-      // a fully out-of-range row: zeros.  First the Q tile: lane ch copies
-      // its 64-dim chunk ch, G heads x kQ queries in one box (queries past
-      // the block's own are copied too and masked by the softmax; queries
-      // past total_q read as zeros).
-      static_assert(32 % kPPS == 0, "a step's pages in one batch of 32 table entries");
-      static_assert(C::kKChunks <= 32, "one lane per Q chunk");
+  if (warp == 4) {
+    // ---------------- producer: each item's Q, then its steps, pages page0 + i*kPPS ... ----------------
+    // Lane ch < D/64 copies chunk ch of Q (G heads x kQ queries in one box;
+    // queries past the tile's own are copied too and masked by the softmax,
+    // queries past total_q read as zeros).  Lane pg < kPPS copies page pg of
+    // a step chunk by chunk, so that the step's pages sit contiguously in
+    // each [kKeys rows][64 dims] chunk.  Pages past the range (the last step)
+    // and bad page ids are copied from a fully out-of-range row: zeros.
+    static_assert(32 % kPPS == 0, "a step's pages in one batch of 32 table entries");
+    static_assert(C::kKChunks <= 32, "one lane per Q chunk");
+    bool ok = true;
+    int gs = 0, gt = 0;  // steps and items issued
+    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      const TileItem it = load_tile<C>(p, w, tiles, lane == 0);
+      if (!it.run) continue;
+      if (gt >= 1) {  // the previous item's S products have read Q
+        const int wq = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.q_empty, (gt - 1) & 1)) : 0;
+        ok = __shfl_sync(0xffffffffu, wq, 0) != 0;
+        if (!ok) break;
+      }
       if (lane == 0) mbar_arrive_expect_tx(&s.q_ready, C::kKChunks * C::kQChunkBytes);
       __syncwarp();
-      if (lane < C::kKChunks)
-        tma_load_4d(s.q[lane], &tm_q, 0, lane, q0 + i0, c * kG, &s.q_ready);
-      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-      bool ok = true;
-      int issued = 0;
+      if (lane < C::kKChunks) tma_load_4d(s.q[lane], &tm_q, 0, lane, it.q0 + it.i0, it.c * kG, &s.q_ready);
+      ++gt;
+      const int32_t* bt = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
       // block-table entry of the page copied at position gp of the order
       const auto entry = [&](int gp) {
-        const int lp = logical_page(gp);
-        return gp < n_steps * kPPS && lp < n_pages ? bt[page0 + lp] : -1;
+        const int lp = tile_step(it, gp / kPPS) * kPPS + gp % kPPS;
+        return gp < it.n_steps * kPPS && lp < it.n_pages ? bt[it.page0 + lp] : -1;
       };
       // block-table entries of pages 32k + lane (in copy order), one batch ahead
       int cur = entry(lane);
       int nxt = entry(32 + lane);
-      for (int i = 0; i < n_steps; ++i) {
+      for (int i = 0; i < it.n_steps; ++i) {
         const int gp0 = i * kPPS;
         if (gp0 > 0 && (gp0 & 31) == 0) {
           cur = nxt;
           nxt = entry(gp0 + 32 + lane);
         }
         const int phys = __shfl_sync(0xffffffffu, cur, (gp0 + (lane < kPPS ? lane : 0)) & 31);
-        const int stage = i % kStages;
-        if (i >= kStages) {
-          const int w = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.empty[stage], ((i / kStages) - 1) & 1)) : 0;
-          ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        const int stage = gs % kStages;
+        if (gs >= kStages) {
+          const int wv = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.empty[stage], ((gs / kStages) - 1) & 1)) : 0;
+          ok = __shfl_sync(0xffffffffu, wv, 0) != 0;
         }
-        if (!ok) {
-          if (lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-          break;
-        }
+        if (!ok) break;
         if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], C::kKTile + C::kVTile);
         __syncwarp();
         if (lane < kPPS) {
-          const int gp = logical_page(gp0 + lane);
+          const int gp = tile_step(it, i) * kPPS + lane;
           int32_t y = -kPage;
-          if (gp < n_pages) {
+          if (gp < it.n_pages) {
             if (phys < 0 || static_cast<int64_t>(phys) >= p.num_pages)
               report(p.status, ATTN_DEV_BAD_PAGE);
             else
@@ -316,125 +355,170 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
 #pragma unroll
           for (int ch = 0; ch < C::kKChunks; ++ch)
-            tma_load_3d(s.k[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_k, 0, y,
-                                 c * C::kKChunks + ch, &s.full[stage]);
-          tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, c * C::kKChunks + slice * C::kVChunks,
+            tma_load_3d(s.k[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_k, 0, y, it.c * C::kKChunks + ch,
+                        &s.full[stage]);
+          tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, it.c * C::kKChunks + it.slice * C::kVChunks,
                       &s.full[stage]);
         }
-        ++issued;
+        ++gs;
         __syncwarp();
       }
-      if (lane == 0) {  // no copy may still be landing when the block retires
-        if (!mbar_wait(&s.q_ready, 0)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-        for (int st = 0; st < kStages && st < issued; ++st) {
-          const int uses = (issued - 1 - st) / kStages + 1;
-          if (!mbar_wait(&s.full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+    }
+    if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+    if (lane == 0) {  // no copy may still be landing, nor a commit arriving, when the CTA retires
+      if (gt >= 1) {
+        if (!mbar_wait(&s.q_ready, (gt - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        if (ok && !mbar_wait(&s.q_empty, (gt - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      }
+      for (int st = 0; st < kStages && st < gs; ++st) {
+        const int uses = (gs - 1 - st) / kStages + 1;
+        if (!mbar_wait(&s.full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        if (ok && !mbar_wait(&s.empty[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer (the whole warp; an elected lane issues) ----------------
+    // Stage, S buffer and P buffer indices advance by one per step, with
+    // their phase parities, and the loop bounds are broadcast from lane 0:
+    // the descriptors then stay in uniform registers.
+    bool ok = true;
+    int gt = 0, g = 0;                      // items done, steps done
+    int st = 0, st_ph = 0, sb = 0, sb_ph = 0;
+    int pst = 0, pb = 0, pb_ph = 0;         // P V: stage and P buffer of its next step
+    const uint32_t q_base = smem_addr(s.q[0]);
+    auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[pb], pb_ph));
+      tc_fence_after_sync();
+      const uint32_t v_base = smem_addr(s.v[pst]);
+#pragma unroll
+      for (int kk = 0; kk < kPPS; ++kk) {
+        const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
+        if constexpr (C::kPInTmem) {
+          umma_bf16_ts_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * pb + 8 * kk, b_desc, C::kIdescPV,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          const uint64_t a_desc = umma_desc(smem_addr(s.p[pb]) + kk * 256, 128, C::kKeys * 16, 0);
+          umma_bf16_warp(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
       }
-    } else if (warp == 5) {
-      // ---------------- MMA issuer (the whole warp; an elected lane issues) ----------------
-      bool ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, 0));
-      const uint32_t q_base = smem_addr(s.q[0]);
-      auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
-        const int bp = j % C::kPBufs;
-        const int st = j % kStages;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[bp], (j / C::kPBufs) & 1));
-        tc_fence_after_sync();
-        const uint32_t v_base = smem_addr(s.v[st]);
-#pragma unroll
-        for (int kk = 0; kk < kPPS; ++kk) {
-          const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
-          if constexpr (C::kPInTmem) {
-            umma_bf16_ts_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-          } else {
-            const uint64_t a_desc = umma_desc(smem_addr(s.p[bp]) + kk * 256, 128, C::kKeys * 16, 0);
-            umma_bf16_warp(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        umma_commit_warp(&s.empty[st]);
-        umma_commit_warp(&s.p_empty[bp]);
-      };
+      umma_commit_warp(&s.empty[pst]);
+      umma_commit_warp(&s.p_empty[pb]);
+      if (++pst == kStages) pst = 0;
+      if (++pb == C::kPBufs) pb = 0, pb_ph ^= 1;
+    };
+    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+      const TileItem it = load_tile<C>(p, w, tiles, false);
+      if (!warp_uniform_int(it.run)) continue;
+      const int n_steps = warp_uniform_int(it.n_steps);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, gt & 1));
       for (int j = 0; j < n_steps; ++j) {
-        const int st = j % kStages;
-        const int bs = j % C::kSBufs;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (ok && j >= C::kSBufs)
-          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], st_ph));
+        if (ok && g >= C::kSBufs) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[sb], sb_ph ^ 1));
         tc_fence_after_sync();
         const uint32_t k_base = smem_addr(s.k[st]);
 #pragma unroll
         for (int kk = 0; kk < (kD / 16) / C::kIssuers; ++kk) {
           const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
           const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * sb), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit_warp(&s.s_full[bs]);
-        if (j >= 1) pv(j - 1);
+        umma_commit_warp(&s.s_full[sb]);
+        if (j == n_steps - 1) umma_commit_warp(&s.q_empty);  // this issuer's reads of the item's Q done
+        if (++st == kStages) st = 0, st_ph ^= 1;
+        if (++sb == C::kSBufs) sb = 0, sb_ph ^= 1;
+        ++g;
+        if (j >= 1) {
+          pv(j - 1);
+        } else if (ok && gt >= 1) {
+          // the item's first P V overwrites O: the previous item's epilogue must have read it
+          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_free, (gt - 1) & 1));
+        }
       }
       pv(n_steps - 1);
-      umma_commit_warp(&s.mma_done);
-      if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // every product done before the memory is freed
-      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-    } else if (warp >= 6 && warp < 5 + C::kIssuers) {
-      // ---------------- the other S issuers (whole warps): part i of the k-steps ----------------
-      constexpr int kPart = (kD / 16) / C::kIssuers;  // k-steps per issuer, whole 64-dim chunks
-      static_assert(kPart % 4 == 0, "each issuer takes whole chunks of Q and K");
-      const int part = warp - 5;
-      bool ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, 0));
-      const uint32_t q_base = smem_addr(s.q[0]) + (part * kPart / 4) * C::kQChunkBytes;
+      umma_commit_warp(&s.o_full);  // the item's products done
+      ++gt;
+    }
+    // the softmax warps' last arrivals on s_free and o_free (not waited for above)
+    for (int k = g >= C::kSBufs ? g - C::kSBufs : 0; k < g; ++k)
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[k % C::kSBufs], (k / C::kSBufs) & 1));
+    if (ok && gt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_free, (gt - 1) & 1));
+    umma_commit_warp(&s.mma_done);
+    if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // every product done before the memory is freed
+    if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+  } else if (warp >= 6 && warp < 5 + C::kIssuers) {
+    // ---------------- the other S issuers (whole warps): part i of the k-steps ----------------
+    constexpr int kPart = (kD / 16) / C::kIssuers;  // k-steps per issuer, whole 64-dim chunks
+    static_assert(kPart % 4 == 0, "each issuer takes whole chunks of Q and K");
+    const int part = warp - 5;
+    bool ok = true;
+    int gt = 0, g = 0;
+    int st = 0, st_ph = 0, sb = 0, sb_ph = 0;
+    const uint32_t q_base = smem_addr(s.q[0]) + (part * kPart / 4) * C::kQChunkBytes;
+    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+      const TileItem it = load_tile<C>(p, w, tiles, false);
+      if (!warp_uniform_int(it.run)) continue;
+      const int n_steps = warp_uniform_int(it.n_steps);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, gt & 1));
       for (int j = 0; j < n_steps; ++j) {
-        const int st = j % kStages;
-        const int bs = j % C::kSBufs;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (ok && j >= C::kSBufs)
-          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], st_ph));
+        if (ok && g >= C::kSBufs) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[sb], sb_ph ^ 1));
         tc_fence_after_sync();
         const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kChunkRows;
 #pragma unroll
         for (int kk = 0; kk < kPart; ++kk) {
           const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
           const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * bs + part), a_desc, b_desc, C::kIdescS,
+          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * sb + part), a_desc, b_desc, C::kIdescS,
                          kk > 0 ? 1u : 0u);
         }
-        umma_commit_warp(&s.s_full[bs]);
+        umma_commit_warp(&s.s_full[sb]);
         umma_commit_warp(&s.empty[st]);  // this issuer's reads of the stage's K tile done
+        if (j == n_steps - 1) umma_commit_warp(&s.q_empty);
+        if (++st == kStages) st = 0, st_ph ^= 1;
+        if (++sb == C::kSBufs) sb = 0, sb_ph ^= 1;
+        ++g;
       }
-      umma_commit_warp(&s.mma_done);
-      if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
-      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-    } else {
-      // ---------------- softmax and epilogue: one thread per row (and half) ----------------
-      // With two warpgroups, thread r of group h handles keys [h kHalf, (h + 1) kHalf)
-      // of each step of row r, and columns [h kDS/2, (h + 1) kDS/2) of O; the
-      // two halves of a row share the row max through shared memory.
-      constexpr int kGroups = C::kSoftmaxGroups;
-      constexpr int kHalf = C::kKeys / kGroups;  // keys of a step per thread
-      constexpr int kOCols = kDS / kGroups;      // output dims per thread
-      static_assert(kOCols % (16 * kRoundTrip) == 0, "whole TMEM round trips");
-      const int h = warp >= 4 ? 1 : 0;            // softmax warpgroup (warps 0-3, then the last four)
-      const int r = 32 * (warp & 3) + lane;       // row = TMEM lane
-      const int st = h * 128 + r;                 // index among the softmax threads
-      const int kc0 = h * kHalf;                  // this thread's first key column of a step
-      const int oc0 = h * kOCols;                 // and first output column
-      const int g = r / kQ;
-      const int qi = r % kQ;
-      const bool valid = qi < nq;
-      const int head = c * kG + g;
-      const int pos = P0 + qi;
+      ++gt;
+    }
+    umma_commit_warp(&s.mma_done);
+    if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
+    if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+  } else {
+    // ---------------- softmax and epilogue: one thread per row (and half) ----------------
+    // With two warpgroups, thread r of group h handles keys [h kHalf, (h + 1) kHalf)
+    // of each step of row r, and columns [h kDS/2, (h + 1) kDS/2) of O; the
+    // two halves of a row share the row max through shared memory.
+    constexpr int kGroups = C::kSoftmaxGroups;
+    constexpr int kHalf = C::kKeys / kGroups;  // keys of a step per thread
+    constexpr int kOCols = kDS / kGroups;      // output dims per thread
+    static_assert(kOCols % (16 * kRoundTrip) == 0, "whole TMEM round trips");
+    const int h = warp >= 4 ? 1 : 0;            // softmax warpgroup (warps 0-3, then the last four)
+    const int r = 32 * (warp & 3) + lane;       // row = TMEM lane
+    const int st = h * 128 + r;                 // index among the softmax threads
+    const int kc0 = h * kHalf;                  // this thread's first key column of a step
+    const int oc0 = h * kOCols;                 // and first output column
+    const int g = r / kQ;
+    const int qi = r % kQ;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    bool ok = true;
+    int gs = 0, gt = 0;  // steps and items done
+    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+      const TileItem it = load_tile<C>(p, w, tiles, false);
+      if (!it.run) continue;
+      const bool valid = qi < it.nq;
+      const int head = it.c * kG + g;
+      const int pos = it.P0 + qi;
       const int lo_r = p.window > 0 ? pos - p.window + 1 : 0;
-      const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
       float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this thread's share of the row sum
-      bool ok = true;
-      for (int j = 0; j < n_steps; ++j) {
-        const int bs = j % C::kSBufs;  // S buffer
-        const int pb = j % C::kPBufs;  // P buffer
-        const int xb = j & 1;          // exchange buffer of the half-row maxima
-        const int step0 = (page0 + logical_step(j) * kPPS) * kPage;  // key of the step's column 0
+      for (int j = 0; j < it.n_steps; ++j) {
+        const int gj = gs + j;
+        const int bs = gj % C::kSBufs;  // S buffer
+        const int pb = gj % C::kPBufs;  // P buffer
+        const int xb = gj & 1;          // exchange buffer of the half-row maxima
+        const int step0 = (it.page0 + tile_step(it, j) * kPPS) * kPage;  // key of the step's column 0
         const int pos0 = step0 + kc0;                   // key of this thread's first column
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (j / C::kSBufs) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (gj / C::kSBufs) & 1));
         tc_fence_after_sync();
         float sv[kHalf];
 #pragma unroll
@@ -478,7 +562,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (__any_sync(0xffffffffu, rescale)) {
           // O's row holds P V up to step j-1: wait for that product, then scale in place
           if (ok && j >= 1)
-            ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(j - 1) % C::kPBufs], ((j - 1) / C::kPBufs) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(gj - 1) % C::kPBufs], ((gj - 1) / C::kPBufs) & 1));
           tc_fence_after_sync();
           const float f = rescale ? ex2_approx(m - (m_new + kHeadroom)) : 1.f;
 #pragma unroll 1
@@ -508,17 +592,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l += ls;
 
         // P row into buffer pb (K-major core matrices of 8 rows x 8 keys) once
-        // P V of step j - kPBufs has read it
-        if (ok && j >= C::kPBufs)
-          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[pb], ((j / C::kPBufs) - 1) & 1));
+        // P V of step gj - kPBufs has read it
+        if (ok && gj >= C::kPBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[pb], ((gj / C::kPBufs) - 1) & 1));
         if constexpr (C::kPInTmem) {
           // this row's keys into its lane: column kPCol + (kKeys / 2) pb + k / 2 holds keys k, k + 1
 #pragma unroll
           for (int kc = 0; kc < kHalf / 16; ++kc) {
-            uint32_t w[8];
+            uint32_t wv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
-            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, w);
+            for (int e = 0; e < 8; ++e) wv[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
+            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, wv);
           }
           tmem_wait_st();
         } else {
@@ -531,16 +615,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                     pack_bf16x2(sv[8 * kc + 6], sv[8 * kc + 7])));
         }
         // zero this step's V rows outside [k_lo, k_hi] (the first and last steps)
-        if (step0 < k_lo || step0 + C::kKeys - 1 > k_hi) {
-          const uint32_t v_base = smem_addr(s.v[j % kStages]);
+        if (step0 < it.k_lo || step0 + C::kKeys - 1 > it.k_hi) {
+          const uint32_t v_base = smem_addr(s.v[gj % kStages]);
 #pragma unroll 1
-          for (int it = st; it < C::kKeys * 8; it += C::kSoftmaxThreads) {
-            const int kr = it >> 3;  // key row of the step
+          for (int e = st; e < C::kKeys * 8; e += C::kSoftmaxThreads) {
+            const int kr = e >> 3;  // key row of the step
             const int key = step0 + kr;
-            if (key < k_lo || key > k_hi) {
+            if (key < it.k_lo || key > it.k_hi) {
 #pragma unroll
               for (int ch = 0; ch < C::kVChunks; ++ch)
-                st_shared_v4(v_base + (kr >> 4) * C::kVPage + ch * C::kChunkBytes + (kr & 15) * 128 + (it & 7) * 16,
+                st_shared_v4(v_base + (kr >> 4) * C::kVPage + ch * C::kChunkBytes + (kr & 15) * 128 + (e & 7) * 16,
                              make_uint4(0, 0, 0, 0));
             }
           }
@@ -551,11 +635,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) mbar_arrive(&s.p_full[pb]);
       }
 
-      // ---- epilogue: wait for the last P V, normalise, write this row's output dims ----
-      if (ok)
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_fast(&s.p_empty[(n_steps - 1) % C::kPBufs], ((n_steps - 1) / C::kPBufs) & 1));
-      if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      // ---- epilogue: wait for the item's last P V, normalise, write this row's output dims ----
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_full, gt & 1));
       tc_fence_after_sync();
       if constexpr (kGroups == 2) {
         s.half_sum[h][r] = l;
@@ -563,7 +644,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l += s.half_sum[1 - h][r];
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const size_t o_off = (static_cast<size_t>(q0 + i0 + qi) * kHq + head) * kD + slice * kDS;
+      const size_t o_off = (static_cast<size_t>(it.q0 + it.i0 + qi) * kHq + head) * kD + it.slice * kDS;
 #pragma unroll 1
       for (int col0 = oc0; col0 < oc0 + kOCols; col0 += 16 * kRoundTrip) {
         float ovs[kRoundTrip][16];
@@ -589,7 +670,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
       }
+      if constexpr (kGroups == 2) named_barrier_sync(1, C::kSoftmaxThreads);  // half_sum read before its next write
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.o_free);  // the next item's first P V may overwrite O
+      gs += it.n_steps;
+      ++gt;
     }
+    // the last P V products' commits (not all waited for above)
+    for (int gj = gs >= C::kPBufs ? gs - C::kPBufs : 0; gj < gs; ++gj)
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[gj % C::kPBufs], (gj / C::kPBufs) & 1));
+    if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
   }
 
   // ---------------- teardown: free the tensor memory ----------------
