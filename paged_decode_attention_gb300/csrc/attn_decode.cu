@@ -222,7 +222,7 @@ int32_t encode_chunk_map(CUtensorMap* map, const void* pool, int64_t num_pages, 
   return ATTN_OK;
 }
 
-// Q [total_q, Hq, D] as {64 dims, D/64 chunks, total_q queries, Hq heads}:
+// Q or O [total_q, Hq, D] (bf16) as {64 dims, D/64 chunks, total_q queries, Hq heads}:
 // a box {64, 1, kQ, G} copies one 64-dim chunk of kQ consecutive queries for
 // the G heads of a KV head as [head][query][64 dims], 128-byte swizzled (the
 // single-CTA prefill's row order); queries past total_q read as zeros.
@@ -704,14 +704,19 @@ int32_t run_prefill(Kernel kernel, int32_t kind, const void* q, const void* k_po
   if constexpr (kPair) {
     e = launch_pdl(kernel, grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_k, tm_v, p);
   } else {
-    CUtensorMap tm_q;  // the tile's Q in one box per 64-dim chunk
+    CUtensorMap tm_q, tm_o;  // the tile's Q, and (bf16 output) its O, in one box per 64-dim chunk
     if ((st = encode_q_map(&tm_q, q, total_q, C::kHq, C::kD, C::kG, C::kQ))) return st;
+    if (out_dtype == ATTN_OUT_BF16) {
+      if ((st = encode_q_map(&tm_o, o, total_q, C::kHq, C::kD, C::kG, C::kQ))) return st;
+    } else {
+      tm_o = tm_q;  // not used: fp32 output is written by the threads
+    }
     // one CTA per SM looping over the work items (query tile, KV head and
     // slice, sequence), or one CTA per item
     const int64_t work = static_cast<int64_t>(tiles) * C::kHkv * C::kSlices * batch;
     const int64_t ctas = kPersistentPrefill ? std::min<int64_t>(work, std::max(1, num_sms)) : work;
     e = launch_pdl(kernel, dim3(static_cast<unsigned>(ctas)), C::kThreads, C::kSmemBytes,
-                   static_cast<cudaStream_t>(stream), tm_k, tm_v, tm_q, p);
+                   static_cast<cudaStream_t>(stream), tm_k, tm_v, tm_q, tm_o, p);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));

@@ -85,6 +85,24 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 4-D tile store from shared memory (the same box shape as tma_load_4d), in
+// the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int32_t x, int32_t y, int32_t z,
+                                             int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until this thread's bulk stores have read their shared memory ...
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... or have completed.
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
           int kSoftmaxGroups_ = 1, int kRotate_ = 0, int kSBufs_ = 2, int kPBufs_ = 2>
 struct Config {
@@ -148,6 +166,7 @@ struct Config {
     alignas(1024) uint8_t k[kStages][kKTile];
     alignas(1024) uint8_t v[kStages][kVTile];
     alignas(128) uint8_t p[kPInTmem ? 1 : 2][kPInTmem ? 16 : kPBytes];
+    alignas(1024) uint8_t ost[kRows * 128];  // one 64-dim chunk of O in bf16, staged for a TMA store
     alignas(8) uint64_t full[kStages];   // K and V of the stage landed (TMA)
     alignas(8) uint64_t empty[kStages];  // both products of the stage's page done (commit)
     alignas(8) uint64_t s_full[kSBufs];   // S buffer written (commit)
@@ -164,6 +183,7 @@ struct Config {
     float half_sum[kSoftmaxGroups][kRows];     // and its share of the row sum, at the end
   };
   static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM within the 227 KB a CTA may have");
 };
 
 constexpr float kSlack = 16.f;     // log2 units
@@ -249,7 +269,8 @@ __device__ __forceinline__ int warp_uniform_int(int v) { return __shfl_sync(0xff
 template <typename C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                      const __grid_constant__ PrefillParams p) {
   constexpr int kD = C::kD, kDS = C::kDS, kG = C::kG, kHq = C::kHq, kQ = C::kQ, kStages = C::kStages;
   constexpr int kPPS = C::kPPS;
   extern __shared__ uint8_t smem_raw[];
@@ -644,6 +665,40 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l += s.half_sum[1 - h][r];
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (!p.out_f32 && it.nq == kQ) {
+        // A full tile in bf16: O goes out one 64-dim chunk at a time, staged in
+        // shared memory (swizzled like Q) and written by one TMA store per
+        // chunk, G heads x kQ queries in one box.  A thread's own row is 8 KB
+        // from its neighbours' in global memory, so per-thread stores made 32
+        // transactions of every warp instruction.  (A partial tile takes the
+        // per-thread stores below: a box would reach the next sequence's rows.)
+        constexpr int kOutChunks = kDS / 64;
+        constexpr int kOwnChunks = kOutChunks / kGroups;
+#pragma unroll 1
+        for (int cc = 0; cc < kOutChunks; ++cc) {
+          if (cc / kOwnChunks == h) {
+            float ov[4][16];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tmem_ld16(t_row + 64 * cc + 16 * u, ov[u]);
+            tmem_wait_ld();
+            const uint32_t row = smem_addr(s.ost) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float* v = &ov[u >> 1][8 * (u & 1)];
+              st_shared_v4(row + ((u ^ (r & 7)) << 4),
+                           make_uint4(pack_bf16x2(v[0] * inv, v[1] * inv), pack_bf16x2(v[2] * inv, v[3] * inv),
+                                      pack_bf16x2(v[4] * inv, v[5] * inv), pack_bf16x2(v[6] * inv, v[7] * inv)));
+            }
+            fence_proxy_async_smem();
+          }
+          named_barrier_sync(1, C::kSoftmaxThreads);
+          if (st == 0) {
+            tma_store_4d(&tm_o, s.ost, 0, it.slice * kOutChunks + cc, it.q0 + it.i0, it.c * kG);
+            tma_store_wait_read();
+          }
+          named_barrier_sync(1, C::kSoftmaxThreads);  // the staging buffer read: the next chunk may overwrite it
+        }
+      } else {
       const size_t o_off = (static_cast<size_t>(it.q0 + it.i0 + qi) * kHq + head) * kD + it.slice * kDS;
 #pragma unroll 1
       for (int col0 = oc0; col0 < oc0 + kOCols; col0 += 16 * kRoundTrip) {
@@ -670,6 +725,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
       }
+      }
       if constexpr (kGroups == 2) named_barrier_sync(1, C::kSoftmaxThreads);  // half_sum read before its next write
       tc_fence_before_sync();
       __syncwarp();
@@ -681,6 +737,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (int gj = gs >= C::kPBufs ? gs - C::kPBufs : 0; gj < gs; ++gj)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[gj % C::kPBufs], (gj / C::kPBufs) & 1));
     if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+    if (st == 0) tma_store_wait_all();  // the output stores complete before the CTA retires
   }
 
   // ---------------- teardown: free the tensor memory ----------------
