@@ -93,6 +93,22 @@ def test_scores_over_a_wide_range(cuda_lib, kind):
     check_full(case, "%s wide score range" % kind)
 
 
+@pytest.mark.parametrize("kind,out_dtype", [("sliding", torch.bfloat16), ("sliding", torch.float32),
+                                             ("global", torch.bfloat16)])
+def test_many_ragged_sequences(cuda_lib, kind, out_dtype):
+    # More work items (query tiles x KV heads x sequences) than SMs, so the
+    # persistent CTAs loop, most of them skipping the tiles that short
+    # sequences lack; full and partial tiles, with bf16 output through the
+    # staged tensor store and the per-thread path.
+    seq_lens = [700, 1, 1500, 130, 2200, 64, 65, 900, 40, 1800]
+    q_lens = [700, 1, 600, 0, 1300, 64, 65, 129, 40, 5]
+    case = make_prefill_case(kind, seq_lens, q_lens, seed=706)
+    o, st = gpu_prefill(case, out_dtype)
+    assert st == 0
+    want = oracle_prefill(case)
+    assert_within_tolerance(o.float().double().cpu().numpy(), want, "%s ragged %s" % (kind, out_dtype))
+
+
 @pytest.mark.parametrize("kind", ["sliding", "global"])
 def test_long_context_sampled_rows(cuda_lib, kind):
     # a chunk of 512 new tokens on a 32768-token context: rows sampled for the oracle
