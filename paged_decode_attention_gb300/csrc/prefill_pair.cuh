@@ -39,7 +39,7 @@ namespace prefill_pair {
 using prefill_tc::PrefillParams;
 
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kSoftmaxGroups_, int kRotate_, int kSBufs_ = 2,
-          int kPBufs_ = 2>
+          int kPBufs_ = 2, int kSIssuers_ = 1>
 struct PairConfig {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per pair (each CTA holds V for half of them)
@@ -73,9 +73,15 @@ struct PairConfig {
   static constexpr int kRotate = kRotate_;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSBufs = kSBufs_;                  // S buffers: S runs up to kSBufs steps ahead
-  static constexpr uint32_t kSCol = kDS;                  // kSBufs S buffers of kKeys columns
+  // Warps of rank 0 issuing S (1 or 2): with two, warp kFwdPWarp (idle on
+  // rank 0 otherwise) issues the second half of the D k-steps into its own
+  // part of each S buffer, and the softmax adds the two parts.
+  static constexpr int kSIssuers = kSIssuers_;
+  static constexpr uint32_t kSCol = kDS;                  // kSBufs S buffers of kSIssuers x kKeys columns
   static constexpr int kPBufs = kPBufs_;                  // P buffers: P V may lag the softmax by kPBufs - 1 steps
-  static constexpr uint32_t kPCol = kSCol + kSBufs * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
+  static constexpr uint32_t kPCol = kSCol + kSBufs * kSIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
+  static_assert((kSIssuers == 1 || kSIssuers == 2) && ((kD / 16) / kSIssuers) % 4 == 0,
+                "each S issuer takes whole 64-dim chunks of Q and K");
   static constexpr uint32_t kIdescS = umma_idesc_bf16(256, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(256, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 128 == 0 && kDS <= 256, "tile shapes");
@@ -132,10 +138,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
       mbar_init(&s.peer_full[st], 1);
-      mbar_init(&s.empty[st], 2);
+      mbar_init(&s.empty[st], C::kSIssuers + 1);  // the S issuers and the P V issuer
     }
     for (int i = 0; i < C::kSBufs; ++i) {
-      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_full[i], C::kSIssuers);
       mbar_init(&s.s_free[i], kArrivals);
     }
     for (int i = 0; i < C::kPBufs; ++i) {
@@ -143,7 +149,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       mbar_init(&s.p_empty[i], 1);
     }
     mbar_init(&s.q_ready, kArrivals);
-    mbar_init(&s.mma_done, 2);
+    mbar_init(&s.mma_done, C::kSIssuers + 1);
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
@@ -255,10 +261,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
           if (ok && !mbar_wait(&s.empty[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
         }
       }
-    } else if (warp == 5 && rank == 0) {
+    } else if ((warp == 5 || (C::kSIssuers == 2 && warp == C::kFwdPWarp)) && rank == 0) {
       // ---------------- rank 0: the pair's S products (whole warp, an elected lane issues) ----------------
+      constexpr int kPart = (kD / 16) / C::kSIssuers;  // k-steps per S issuer
+      const int part = warp == 5 ? 0 : 1;
       bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.q_ready, 0));
-      const uint32_t q_base = smem_addr(s.q[0]);
+      const uint32_t q_base = smem_addr(s.q[0]) + (part * kPart / 4) * C::kQChunkBytes;
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
         const int bs = j % C::kSBufs;
@@ -267,12 +275,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         if (ok && j >= C::kSBufs)
           ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
         tc_fence_after_sync();
-        const uint32_t k_base = smem_addr(s.k[st]);
+        const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kPageChunk;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < kPart; ++kk) {
           const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
           const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kPageChunk + (kk & 3) * 32, 16, 1024, 2);
-          umma_bf16_pair_warp(tmem + C::kSCol + C::kKeys * bs, a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+          umma_bf16_pair_warp(tmem + C::kSCol + C::kKeys * (C::kSIssuers * bs + part), a_desc, b_desc, C::kIdescS,
+                              kk > 0 ? 1u : 0u);
         }
         umma_commit_pair_warp(&s.s_full[bs]);
         umma_commit_pair_warp(&s.empty[st]);  // K of the stage read
@@ -392,7 +401,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         float sv[kHalf];
 #pragma unroll
         for (int blk = 0; blk < kHalf / 16; ++blk)
-          tmem_ld16(t_row + C::kSCol + C::kKeys * sb + kc0 + 16 * blk, *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+          tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kSIssuers * sb) + kc0 + 16 * blk,
+                    *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+        if constexpr (C::kSIssuers == 2) {
+          float sb2[kHalf];
+#pragma unroll
+          for (int blk = 0; blk < kHalf / 16; ++blk)
+            tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kSIssuers * sb + 1) + kc0 + 16 * blk,
+                      *reinterpret_cast<float(*)[16]>(&sb2[16 * blk]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < kHalf; ++k) sv[k] += sb2[k];
+        }
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
@@ -534,10 +554,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
 // stages, two softmax warpgroups.  Global: each CTA 8 queries x 16 heads, D
 // = 512 split into two slices of 256 output dims (both compute S), its stage
 // 16 KB of K and 8 KB of V, 4 stages, one softmax warpgroup, the step order
-// rotated by pair, three S buffers (655 against 646 TFLOP/s with two).
+// rotated by pair, two S issuers each with two S buffers (768 against 756
+// TFLOP/s with one issuer and three buffers, on one box).
 using SlidingPairConfig =
     PairConfig<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 8, 2, 0>;
-using GlobalPairConfig = PairConfig<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 4, 1, 7, 3>;
+using GlobalPairConfig =
+    PairConfig<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 4, 1, 7, 2, 2, 2>;
 
 }  // namespace prefill_pair
 }  // namespace pda
