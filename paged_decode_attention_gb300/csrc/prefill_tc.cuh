@@ -158,7 +158,9 @@ struct Config {
   static_assert(kPInTmem || kPBufs == 2, "P in shared memory: two buffers");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
   static_assert(kIssuers >= 1 && kIssuers <= kD / 16, "S k-steps split among the issuers");
-  static_assert(kSoftmaxGroups == 1 || (kSoftmaxGroups == 2 && kPInTmem && (kKeys / 2) % 16 == 0 && kDS % 32 == 0),
+  static_assert(kSoftmaxGroups == 1 ||
+                    ((kSoftmaxGroups == 2 || kSoftmaxGroups == 4) && kPInTmem && (kKeys / kSoftmaxGroups) % 8 == 0 &&
+                     (kDS / kSoftmaxGroups) % 64 == 0),
                 "two softmax warpgroups: halves of whole 16-key blocks, P in tensor memory");
 
   struct Smem {
@@ -179,7 +181,7 @@ struct Config {
     alignas(8) uint64_t o_free;          // O read by the item's epilogue (the softmax warps)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
     uint32_t tmem_base;
-    float half_max[2][kSoftmaxGroups][kRows];  // two warpgroups: each half-row's max, by step parity
+    float half_max[2][kSoftmaxGroups][kRows];  // several warpgroups: each part-row's max, by step parity
     float half_sum[kSoftmaxGroups][kRows];     // and its share of the row sum, at the end
   };
   static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -197,6 +199,20 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// kN consecutive 32-bit columns of this thread's lane (kN a multiple of 8);
+// complete after tmem_wait_ld.
+template <int kN>
+__device__ __forceinline__ void load_row(uint32_t taddr, float (&v)[kN]) {
+  static_assert(kN % 8 == 0, "whole 8-column loads");
+  if constexpr (kN % 16 == 0) {
+#pragma unroll
+    for (int b = 0; b < kN / 16; ++b) tmem_ld16(taddr + 16 * b, *reinterpret_cast<float(*)[16]>(&v[16 * b]));
+  } else {
+#pragma unroll
+    for (int b = 0; b < kN / 8; ++b) tmem_ld8(taddr + 8 * b, *reinterpret_cast<float(*)[8]>(&v[8 * b]));
+  }
 }
 
 // One work item (a query tile of one sequence, KV head and output slice) as
@@ -513,7 +529,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int kHalf = C::kKeys / kGroups;  // keys of a step per thread
     constexpr int kOCols = kDS / kGroups;      // output dims per thread
     static_assert(kOCols % (16 * kRoundTrip) == 0, "whole TMEM round trips");
-    const int h = warp >= 4 ? 1 : 0;            // softmax warpgroup (warps 0-3, then the last four)
+    const int h = warp < 4 ? 0 : (warp - 5 - C::kIssuers) / 4 + 1;  // softmax warpgroup (warps 0-3, then the last ones)
     const int r = 32 * (warp & 3) + lane;       // row = TMEM lane
     const int st = h * 128 + r;                 // index among the softmax threads
     const int kc0 = h * kHalf;                  // this thread's first key column of a step
@@ -542,17 +558,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_full[bs], (gj / C::kSBufs) & 1));
         tc_fence_after_sync();
         float sv[kHalf];
-#pragma unroll
-        for (int blk = 0; blk < kHalf / 16; ++blk)
-          tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs) + kc0 + 16 * blk,
-                    *reinterpret_cast<float(*)[16]>(&sv[16 * blk]));
+        load_row<kHalf>(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs) + kc0, sv);
 #pragma unroll
         for (int part = 1; part < C::kIssuers; ++part) {
           float sb[kHalf];
-#pragma unroll
-          for (int blk = 0; blk < kHalf / 16; ++blk)
-            tmem_ld16(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs + part) + kc0 + 16 * blk,
-                      *reinterpret_cast<float(*)[16]>(&sb[16 * blk]));
+          load_row<kHalf>(t_row + C::kSCol + C::kKeys * (C::kIssuers * bs + part) + kc0, sb);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < kHalf; ++k) sv[k] += sb[k];
@@ -572,10 +582,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         float mx = sv[0];
 #pragma unroll
         for (int k = 1; k < kHalf; ++k) mx = fmaxf(mx, sv[k]);
-        if constexpr (kGroups == 2) {
+        if constexpr (kGroups > 1) {
           s.half_max[xb][h][r] = mx;
           named_barrier_sync(1, C::kSoftmaxThreads);
-          mx = fmaxf(mx, s.half_max[xb][1 - h][r]);
+#pragma unroll
+          for (int o = 1; o < kGroups; ++o) mx = fmaxf(mx, s.half_max[xb][(h + o) % kGroups][r]);
         }
         const float m_new = mx * kLog2e;
         const bool move = m_new > m + kSlack;  // false while the row has no visible key
@@ -618,12 +629,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[pb], ((gj / C::kPBufs) - 1) & 1));
         if constexpr (C::kPInTmem) {
           // this row's keys into its lane: column kPCol + (kKeys / 2) pb + k / 2 holds keys k, k + 1
+          if constexpr (kHalf % 16 == 0) {
 #pragma unroll
-          for (int kc = 0; kc < kHalf / 16; ++kc) {
-            uint32_t wv[8];
+            for (int kc = 0; kc < kHalf / 16; ++kc) {
+              uint32_t wv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
-            tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, wv);
+              for (int e = 0; e < 8; ++e) wv[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
+              tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, wv);
+            }
+          } else {  // 8 keys: 4 columns
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wv[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
+            tmem_st4(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2, wv);
           }
           tmem_wait_st();
         } else {
@@ -659,10 +677,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // ---- epilogue: wait for the item's last P V, normalise, write this row's output dims ----
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_full, gt & 1));
       tc_fence_after_sync();
-      if constexpr (kGroups == 2) {
+      if constexpr (kGroups > 1) {
         s.half_sum[h][r] = l;
         named_barrier_sync(1, C::kSoftmaxThreads);
-        l += s.half_sum[1 - h][r];
+        float lt = 0.f;  // the row sum in group order, the same in every group
+#pragma unroll
+        for (int o = 0; o < kGroups; ++o) lt += s.half_sum[o][r];
+        l = lt;
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (!p.out_f32 && it.nq == kQ) {
@@ -726,7 +747,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       }
       }
-      if constexpr (kGroups == 2) named_barrier_sync(1, C::kSoftmaxThreads);  // half_sum read before its next write
+      if constexpr (kGroups > 1) named_barrier_sync(1, C::kSoftmaxThreads);  // half_sum read before its next write
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.o_free);  // the next item's first P V may overwrite O
