@@ -5,26 +5,29 @@
 // position p = L - n + i and sees key l iff l <= p (and p - window < l with
 // a window); scale 1; query head c*G + g reads KV head c.
 //
-// Block (tile, c * kSlices + slice, b): 128 rows = kQ = 128 / G queries of
-// sequence b times the G query heads of KV head c, row r being head r / kQ of
-// query r % kQ; `slice` selects which kDS of the D output dims it writes
-// (D = 512 is split in two so that O fits in tensor memory).  Per page of 16
-// keys:
-//   S   = Q K^T    tcgen05.mma M=128, N=16, K=D, A = Q (shared memory, K-major,
-//                  128-byte swizzle), B = the page's K tile as TMA wrote it;
-//                  accumulator in tensor memory, two buffers (a step is
-//                  kPPS pages: N = 16 kPPS keys);
+// Work item (tile, c * kSlices + slice, b): 128 rows = kQ = 128 / G queries
+// of sequence b times the G query heads of KV head c, row r being head r / kQ
+// of query r % kQ; `slice` selects which kDS of the D output dims it writes
+// (D = 512 is split in two so that O fits in tensor memory).  Per step of
+// kPPS pages (N = 16 kPPS keys):
+//   S   = Q K^T    tcgen05.mma M=128, N=16 kPPS, K=D, A = Q (K-major: in
+//                  tensor memory, copied there from its 128-byte-swizzled
+//                  shared-memory tile, or read from that tile), B = the
+//                  step's K tile as TMA wrote it; accumulator in tensor
+//                  memory, two buffers;
 //   P   = softmax  warps 0-3 (and a second warpgroup for the second half of
 //                  the keys), one thread per row (TMEM lane = row): masks,
-//                  running max, P rounded to bf16 into shared memory as
-//                  K-major core matrices;
+//                  running max, P rounded to bf16 into tensor memory (or
+//                  shared memory as K-major core matrices);
 //   O  += P V      tcgen05.mma M=128, N=kDS, K=16, B = the V tile, MN-major
 //                  with the 128-byte swizzle; accumulator O in tensor memory.
-// Warp 4 streams the pages by TMA, warp 5 allocates tensor memory and issues
-// the MMAs (the whole warp runs the loop, one elected lane issues; with
-// kIssuers > 1, warps 6 .. 4 + kIssuers issue parts of S; with two softmax
-// warpgroups the last four warps handle the second half of every row).  S of page j+1 is computed while the softmax
-// of page j runs, and P V of page j while the softmax of page j+1 runs.
+// Warp 4 copies Q and the K tiles by TMA; warps 5 .. 4 + kIssuers issue the
+// S products, each a part of the k-steps (the whole warp runs the loop, one
+// elected lane issues), and warp 5 allocates tensor memory; the next warp
+// issues every P V product and the one after it copies the V tiles; with two
+// softmax warpgroups the last four warps handle the second half of every
+// row.  S of step j+1 is computed while the softmax of step j runs, and P V
+// of step j while the softmax of step j+1 runs.
 //
 // Running max.  A row's reference max m moves only when a score exceeds it by
 // more than kSlack = 16 log2 units, and then to kHeadroom = 48 above that
@@ -104,14 +107,19 @@ __device__ __forceinline__ void tma_store_wait_read() {
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
-          int kSoftmaxGroups_ = 1, int kRotate_ = 0, int kSBufs_ = 2, int kPBufs_ = 2>
+          int kSoftmaxGroups_ = 1, int kRotate_ = 0, int kSBufs_ = 2, int kPBufs_ = 2, bool kQInTmem_ = false,
+          int kVStages_ = kStages_>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
   static constexpr int kG = kG_;
   static constexpr int kHkv = kHkv_;
   static constexpr int kHq = kG * kHkv;
-  static constexpr int kStages = kStages_;
+  // K and V tiles in two rings, each filled by its own producer warp: a K
+  // tile is released when its S products are done, a V tile only when its
+  // P V product is, so K runs further ahead than it could in a shared ring.
+  static constexpr int kStages = kStages_;    // K tiles
+  static constexpr int kVStages = kVStages_;  // V tiles
   static constexpr int kPPS = kPPS_;                 // pages per step
   static constexpr bool kPInTmem = kPInTmem_;        // P in tensor memory (else shared memory)
   static constexpr int kKeys = kPPS * kPage;         // keys per step: N of S, K of P V
@@ -130,11 +138,11 @@ struct Config {
   // Threads issuing the S products: one MMA instruction costs its issuing
   // thread about 70 cycles whatever its size, so the D k-steps of a step are
   // split into kIssuers parts, each accumulated into its own S buffer (the
-  // softmax adds them).  Warp 5 issues part 0 and every P V product; warps
-  // 6 .. 4 + kIssuers the other parts.
+  // softmax adds them).  Warps 5 .. 4 + kIssuers issue the parts, and warp
+  // 5 + kIssuers every P V product, so no S product waits behind a P.
   static constexpr int kIssuers = kIssuers_;
   // Softmax warpgroups: with two, each row's keys of a step are split in
-  // halves (warps 0-3 the first, warps 5 + kIssuers .. 8 + kIssuers the
+  // halves (warps 0-3 the first, warps 7 + kIssuers .. 10 + kIssuers the
   // second), and so are its output dims.
   static constexpr int kSoftmaxGroups = kSoftmaxGroups_;
   static constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
@@ -147,14 +155,22 @@ struct Config {
   // softmax, P V may lag it by kPBufs - 1 steps.
   static constexpr int kSBufs = kSBufs_;
   static constexpr int kPBufs = kPBufs_;
-  static constexpr int kThreads = (4 * kSoftmaxGroups + 1 + kIssuers) * 32;
+  static constexpr int kThreads = (4 * kSoftmaxGroups + 3 + kIssuers) * 32;
+  static constexpr int kPVWarp = 5 + kIssuers;     // the P V issuer
+  static constexpr int kVProdWarp = 6 + kIssuers;  // the V producer; softmax warpgroups 1.. follow it
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSCol = kDS;  // S buffers: column kSCol + kKeys (kIssuers buffer + part)
+  // Q as the A operand of S in tensor memory (copied from its shared-memory
+  // tile once per item) instead of shared memory: an S product with N = 32
+  // then reads 1 KB of shared memory instead of 5 KB.
+  static constexpr bool kQInTmem = kQInTmem_;
+  static constexpr uint32_t kQCol = kDS;  // Q (bf16 pairs): kD / 2 columns
+  static constexpr uint32_t kSCol = kDS + (kQInTmem ? kD / 2 : 0);  // S buffers: column kSCol + kKeys (kIssuers buffer + part)
   static constexpr uint32_t kPCol = kSCol + kSBufs * kIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
-  static_assert(kPCol + (kPInTmem ? kPBufs * kKeys / 2 : 0) <= kTmemCols, "O, the S buffers and P fit in tensor memory");
+  static_assert(kPCol + (kPInTmem ? kPBufs * kKeys / 2 : 0) <= kTmemCols,
+                "O, Q, the S buffers and P fit in tensor memory");
   static_assert(kPInTmem || kPBufs == 2, "P in shared memory: two buffers");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
   static_assert(kIssuers >= 1 && kIssuers <= kD / 16, "S k-steps split among the issuers");
@@ -166,17 +182,20 @@ struct Config {
   struct Smem {
     alignas(1024) uint8_t q[kKChunks][kQChunkBytes];
     alignas(1024) uint8_t k[kStages][kKTile];
-    alignas(1024) uint8_t v[kStages][kVTile];
+    alignas(1024) uint8_t v[kVStages][kVTile];
     alignas(128) uint8_t p[kPInTmem ? 1 : 2][kPInTmem ? 16 : kPBytes];
     alignas(1024) uint8_t ost[kRows * 128];  // one 64-dim chunk of O in bf16, staged for a TMA store
-    alignas(8) uint64_t full[kStages];   // K and V of the stage landed (TMA)
-    alignas(8) uint64_t empty[kStages];  // both products of the stage's page done (commit)
+    alignas(8) uint64_t full[kStages];     // K tile landed (TMA)
+    alignas(8) uint64_t empty[kStages];    // its S products done (one commit per issuer)
+    alignas(8) uint64_t v_full[kVStages];   // V tile landed (TMA)
+    alignas(8) uint64_t v_empty[kVStages];  // its P V product done (commit)
     alignas(8) uint64_t s_full[kSBufs];   // S buffer written (commit)
     alignas(8) uint64_t s_free[kSBufs];   // S buffer read (the softmax warps)
     alignas(8) uint64_t p_full[kPBufs];   // P buffer written, O rescaled, V edges zeroed (the softmax warps)
     alignas(8) uint64_t p_empty[kPBufs];  // P V of the buffer's step done (commit)
     alignas(8) uint64_t q_ready;         // the item's Q tile landed (TMA)
-    alignas(8) uint64_t q_empty;         // the item's S products done (one commit per issuer)
+    alignas(8) uint64_t q_empty;         // the item's Q tile read: its S products done, or copied to tensor memory
+    alignas(8) uint64_t q_tfree[kIssuers];  // Q in tensor memory: issuer i's S products of the item done
     alignas(8) uint64_t o_full;          // the item's last P V done (commit)
     alignas(8) uint64_t o_free;          // O read by the item's epilogue (the softmax warps)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
@@ -301,7 +320,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
-      mbar_init(&s.empty[st], C::kIssuers);  // every issuer's products of the stage done
+      mbar_init(&s.empty[st], C::kIssuers);
+    }
+    for (int st = 0; st < C::kVStages; ++st) {
+      mbar_init(&s.v_full[st], 1);
+      mbar_init(&s.v_empty[st], 1);
     }
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&s.s_full[i], C::kIssuers);
@@ -313,9 +336,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     mbar_init(&s.q_ready, 1);
     mbar_init(&s.q_empty, C::kIssuers);
+    for (int i = 0; i < C::kIssuers; ++i) mbar_init(&s.q_tfree[i], 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.o_free, 4 * C::kSoftmaxGroups);
-    mbar_init(&s.mma_done, C::kIssuers);
+    mbar_init(&s.mma_done, C::kIssuers + 1);
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
@@ -333,29 +357,35 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   wait_for_primary_grid();
   allow_dependent_launch();
 
-  if (warp == 4) {
-    // ---------------- producer: each item's Q, then its steps, pages page0 + i*kPPS ... ----------------
+  if (warp == 4 || warp == C::kVProdWarp) {
+    // ---------------- producers: warp 4 each item's Q and its K tiles, the V producer its V tiles ----------------
     // Lane ch < D/64 copies chunk ch of Q (G heads x kQ queries in one box;
     // queries past the tile's own are copied too and masked by the softmax,
     // queries past total_q read as zeros).  Lane pg < kPPS copies page pg of
-    // a step chunk by chunk, so that the step's pages sit contiguously in
-    // each [kKeys rows][64 dims] chunk.  Pages past the range (the last step)
-    // and bad page ids are copied from a fully out-of-range row: zeros.
+    // a step (K chunk by chunk, so that the step's pages sit contiguously in
+    // each [kKeys rows][64 dims] chunk).  Pages past the range (the last
+    // step) and bad page ids are copied from a fully out-of-range row: zeros.
     static_assert(32 % kPPS == 0, "a step's pages in one batch of 32 table entries");
     static_assert(C::kKChunks <= 32, "one lane per Q chunk");
+    const bool kw = warp == 4;  // the K producer
+    const int n_slots = kw ? kStages : C::kVStages;
+    uint64_t* const fullb = kw ? s.full : s.v_full;
+    uint64_t* const emptyb = kw ? s.empty : s.v_empty;
     bool ok = true;
     int gs = 0, gt = 0;  // steps and items issued
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-      const TileItem it = load_tile<C>(p, w, tiles, lane == 0);
+      const TileItem it = load_tile<C>(p, w, tiles, lane == 0 && kw);
       if (!it.run) continue;
-      if (gt >= 1) {  // the previous item's S products have read Q
-        const int wq = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.q_empty, (gt - 1) & 1)) : 0;
-        ok = __shfl_sync(0xffffffffu, wq, 0) != 0;
-        if (!ok) break;
+      if (kw) {
+        if (gt >= 1) {  // the previous item's Q tile read
+          const int wq = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.q_empty, (gt - 1) & 1)) : 0;
+          ok = __shfl_sync(0xffffffffu, wq, 0) != 0;
+          if (!ok) break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&s.q_ready, C::kKChunks * C::kQChunkBytes);
+        __syncwarp();
+        if (lane < C::kKChunks) tma_load_4d(s.q[lane], &tm_q, 0, lane, it.q0 + it.i0, it.c * kG, &s.q_ready);
       }
-      if (lane == 0) mbar_arrive_expect_tx(&s.q_ready, C::kKChunks * C::kQChunkBytes);
-      __syncwarp();
-      if (lane < C::kKChunks) tma_load_4d(s.q[lane], &tm_q, 0, lane, it.q0 + it.i0, it.c * kG, &s.q_ready);
       ++gt;
       const int32_t* bt = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
       // block-table entry of the page copied at position gp of the order
@@ -373,13 +403,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           nxt = entry(gp0 + 32 + lane);
         }
         const int phys = __shfl_sync(0xffffffffu, cur, (gp0 + (lane < kPPS ? lane : 0)) & 31);
-        const int stage = gs % kStages;
-        if (gs >= kStages) {
-          const int wv = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.empty[stage], ((gs / kStages) - 1) & 1)) : 0;
+        const int stage = gs % n_slots;
+        if (gs >= n_slots) {
+          const int wv = lane == 0 ? static_cast<int>(mbar_wait_fast(&emptyb[stage], ((gs / n_slots) - 1) & 1)) : 0;
           ok = __shfl_sync(0xffffffffu, wv, 0) != 0;
         }
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], C::kKTile + C::kVTile);
+        if (lane == 0) mbar_arrive_expect_tx(&fullb[stage], kw ? C::kKTile : C::kVTile);
         __syncwarp();
         if (lane < kPPS) {
           const int gp = tile_step(it, i) * kPPS + lane;
@@ -390,12 +420,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             else
               y = phys * kPage;
           }
+          if (kw) {
 #pragma unroll
-          for (int ch = 0; ch < C::kKChunks; ++ch)
-            tma_load_3d(s.k[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_k, 0, y, it.c * C::kKChunks + ch,
-                        &s.full[stage]);
-          tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, it.c * C::kKChunks + it.slice * C::kVChunks,
-                      &s.full[stage]);
+            for (int ch = 0; ch < C::kKChunks; ++ch)
+              tma_load_3d(s.k[stage] + ch * C::kChunkRows + lane * (kPage * 128), &tm_k, 0, y,
+                          it.c * C::kKChunks + ch, &fullb[stage]);
+          } else {
+            tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, it.c * C::kKChunks + it.slice * C::kVChunks,
+                        &fullb[stage]);
+          }
         }
         ++gs;
         __syncwarp();
@@ -403,92 +436,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     if (lane == 0) {  // no copy may still be landing, nor a commit arriving, when the CTA retires
-      if (gt >= 1) {
+      if (kw && gt >= 1) {
         if (!mbar_wait(&s.q_ready, (gt - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
         if (ok && !mbar_wait(&s.q_empty, (gt - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       }
-      for (int st = 0; st < kStages && st < gs; ++st) {
-        const int uses = (gs - 1 - st) / kStages + 1;
-        if (!mbar_wait(&s.full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-        if (ok && !mbar_wait(&s.empty[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+      for (int st = 0; st < n_slots && st < gs; ++st) {
+        const int uses = (gs - 1 - st) / n_slots + 1;
+        if (!mbar_wait(&fullb[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        if (ok && !mbar_wait(&emptyb[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
       }
     }
-  } else if (warp == 5) {
-    // ---------------- MMA issuer (the whole warp; an elected lane issues) ----------------
-    // Stage, S buffer and P buffer indices advance by one per step, with
-    // their phase parities, and the loop bounds are broadcast from lane 0:
-    // the descriptors then stay in uniform registers.
-    bool ok = true;
-    int gt = 0, g = 0;                      // items done, steps done
-    int st = 0, st_ph = 0, sb = 0, sb_ph = 0;
-    int pst = 0, pb = 0, pb_ph = 0;         // P V: stage and P buffer of its next step
-    const uint32_t q_base = smem_addr(s.q[0]);
-    auto pv = [&](int j) {  // O += P_j V_j, one product of K = 16 per page
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[pb], pb_ph));
-      tc_fence_after_sync();
-      const uint32_t v_base = smem_addr(s.v[pst]);
-#pragma unroll
-      for (int kk = 0; kk < kPPS; ++kk) {
-        const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
-        if constexpr (C::kPInTmem) {
-          umma_bf16_ts_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * pb + 8 * kk, b_desc, C::kIdescPV,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-        } else {
-          const uint64_t a_desc = umma_desc(smem_addr(s.p[pb]) + kk * 256, 128, C::kKeys * 16, 0);
-          umma_bf16_warp(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-      }
-      umma_commit_warp(&s.empty[pst]);
-      umma_commit_warp(&s.p_empty[pb]);
-      if (++pst == kStages) pst = 0;
-      if (++pb == C::kPBufs) pb = 0, pb_ph ^= 1;
-    };
-    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
-      const TileItem it = load_tile<C>(p, w, tiles, false);
-      if (!warp_uniform_int(it.run)) continue;
-      const int n_steps = warp_uniform_int(it.n_steps);
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, gt & 1));
-      for (int j = 0; j < n_steps; ++j) {
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], st_ph));
-        if (ok && g >= C::kSBufs) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[sb], sb_ph ^ 1));
-        tc_fence_after_sync();
-        const uint32_t k_base = smem_addr(s.k[st]);
-#pragma unroll
-        for (int kk = 0; kk < (kD / 16) / C::kIssuers; ++kk) {
-          const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * sb), a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit_warp(&s.s_full[sb]);
-        if (j == n_steps - 1) umma_commit_warp(&s.q_empty);  // this issuer's reads of the item's Q done
-        if (++st == kStages) st = 0, st_ph ^= 1;
-        if (++sb == C::kSBufs) sb = 0, sb_ph ^= 1;
-        ++g;
-        if (j >= 1) {
-          pv(j - 1);
-        } else if (ok && gt >= 1) {
-          // the item's first P V overwrites O: the previous item's epilogue must have read it
-          ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_free, (gt - 1) & 1));
-        }
-      }
-      pv(n_steps - 1);
-      umma_commit_warp(&s.o_full);  // the item's products done
-      ++gt;
-    }
-    // the softmax warps' last arrivals on s_free and o_free (not waited for above)
-    for (int k = g >= C::kSBufs ? g - C::kSBufs : 0; k < g; ++k)
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[k % C::kSBufs], (k / C::kSBufs) & 1));
-    if (ok && gt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_free, (gt - 1) & 1));
-    umma_commit_warp(&s.mma_done);
-    if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // every product done before the memory is freed
-    if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-  } else if (warp >= 6 && warp < 5 + C::kIssuers) {
-    // ---------------- the other S issuers (whole warps): part i of the k-steps ----------------
+  } else if (warp >= 5 && warp < 5 + C::kIssuers) {
+    // ---------------- S issuers (whole warps; an elected lane issues): part i of the k-steps ----------------
+    // Stage and S buffer indices advance by one per step, with their phase
+    // parities, and the loop bounds are broadcast from lane 0: the
+    // descriptors then stay in uniform registers.  S waits only for its
+    // stage and a free S buffer, never for P.
     constexpr int kPart = (kD / 16) / C::kIssuers;  // k-steps per issuer, whole 64-dim chunks
     static_assert(kPart % 4 == 0, "each issuer takes whole chunks of Q and K");
     const int part = warp - 5;
     bool ok = true;
-    int gt = 0, g = 0;
+    int gt = 0, g = 0;  // items done, steps done
     int st = 0, st_ph = 0, sb = 0, sb_ph = 0;
     const uint32_t q_base = smem_addr(s.q[0]) + (part * kPart / 4) * C::kQChunkBytes;
     for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
@@ -496,6 +464,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!warp_uniform_int(it.run)) continue;
       const int n_steps = warp_uniform_int(it.n_steps);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_ready, gt & 1));
+      if constexpr (C::kQInTmem) {
+        // this issuer's k-steps of Q into tensor memory, once its S products
+        // of the previous item have read the columns
+        if (ok && gt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_tfree[part], (gt - 1) & 1));
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kPart; ++kk)
+          tmem_cp_128x256b_warp(tmem + C::kQCol + 8 * (part * kPart + kk),
+                                umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2));
+        umma_commit_warp(&s.q_empty);  // the shared-memory tile may take the next item's Q
+      }
       for (int j = 0; j < n_steps; ++j) {
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], st_ph));
         if (ok && g >= C::kSBufs) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[sb], sb_ph ^ 1));
@@ -503,20 +482,71 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kChunkRows;
 #pragma unroll
         for (int kk = 0; kk < kPart; ++kk) {
-          const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
           const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kChunkRows + (kk & 3) * 32, 16, 1024, 2);
-          umma_bf16_warp(tmem + C::kSCol + C::kKeys * (C::kIssuers * sb + part), a_desc, b_desc, C::kIdescS,
-                         kk > 0 ? 1u : 0u);
+          const uint32_t d_tmem = tmem + C::kSCol + C::kKeys * (C::kIssuers * sb + part);
+          if constexpr (C::kQInTmem) {
+            umma_bf16_ts_warp(d_tmem, tmem + C::kQCol + 8 * (part * kPart + kk), b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+          } else {
+            const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
+            umma_bf16_warp(d_tmem, a_desc, b_desc, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
         }
         umma_commit_warp(&s.s_full[sb]);
-        umma_commit_warp(&s.empty[st]);  // this issuer's reads of the stage's K tile done
-        if (j == n_steps - 1) umma_commit_warp(&s.q_empty);
+        umma_commit_warp(&s.empty[st]);  // this issuer's reads of the K tile done
+        if (j == n_steps - 1) umma_commit_warp(C::kQInTmem ? &s.q_tfree[part] : &s.q_empty);  // and of the item's Q
         if (++st == kStages) st = 0, st_ph ^= 1;
         if (++sb == C::kSBufs) sb = 0, sb_ph ^= 1;
         ++g;
       }
       ++gt;
     }
+    if constexpr (C::kQInTmem) {  // the last item's commit on q_tfree
+      if (ok && gt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_tfree[part], (gt - 1) & 1));
+    }
+    if (part == 0) {  // the softmax warps' last arrivals on s_free (not waited for above)
+      for (int k = g >= C::kSBufs ? g - C::kSBufs : 0; k < g; ++k)
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.s_free[k % C::kSBufs], (k / C::kSBufs) & 1));
+    }
+    umma_commit_warp(&s.mma_done);
+    if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // every product done before the memory is freed
+    if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+  } else if (warp == C::kPVWarp) {
+    // ---------------- P V issuer (whole warp): O += P_j V_j, one product of K = 16 per page ----------------
+    bool ok = true;
+    int gt = 0;                      // items done
+    int pst = 0, pst_ph = 0, pb = 0, pb_ph = 0;  // V tile and P buffer of the next step
+    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+      const TileItem it = load_tile<C>(p, w, tiles, false);
+      if (!warp_uniform_int(it.run)) continue;
+      const int n_steps = warp_uniform_int(it.n_steps);
+      // the item's first P V overwrites O: the previous item's epilogue must have read it
+      if (ok && gt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_free, (gt - 1) & 1));
+      for (int j = 0; j < n_steps; ++j) {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.v_full[pst], pst_ph));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_full[pb], pb_ph));
+        tc_fence_after_sync();
+        const uint32_t v_base = smem_addr(s.v[pst]);
+#pragma unroll
+        for (int kk = 0; kk < kPPS; ++kk) {
+          const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
+          if constexpr (C::kPInTmem) {
+            umma_bf16_ts_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * pb + 8 * kk, b_desc, C::kIdescPV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            const uint64_t a_desc = umma_desc(smem_addr(s.p[pb]) + kk * 256, 128, C::kKeys * 16, 0);
+            umma_bf16_warp(tmem, a_desc, b_desc, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit_warp(&s.v_empty[pst]);  // the V tile read
+        umma_commit_warp(&s.p_empty[pb]);
+        if (++pst == C::kVStages) pst = 0, pst_ph ^= 1;
+        if (++pb == C::kPBufs) pb = 0, pb_ph ^= 1;
+      }
+      umma_commit_warp(&s.o_full);  // the item's products done
+      ++gt;
+    }
+    // the last epilogue's arrival on o_free (not waited for above)
+    if (ok && gt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.o_free, (gt - 1) & 1));
     umma_commit_warp(&s.mma_done);
     if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
     if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -529,7 +559,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int kHalf = C::kKeys / kGroups;  // keys of a step per thread
     constexpr int kOCols = kDS / kGroups;      // output dims per thread
     static_assert(kOCols % (16 * kRoundTrip) == 0, "whole TMEM round trips");
-    const int h = warp < 4 ? 0 : (warp - 5 - C::kIssuers) / 4 + 1;  // softmax warpgroup (warps 0-3, then the last ones)
+    const int h = warp < 4 ? 0 : (warp - C::kVProdWarp - 1) / 4 + 1;  // softmax warpgroup (warps 0-3, then the last ones)
     const int r = 32 * (warp & 3) + lane;       // row = TMEM lane
     const int st = h * 128 + r;                 // index among the softmax threads
     const int kc0 = h * kHalf;                  // this thread's first key column of a step
@@ -654,8 +684,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                     pack_bf16x2(sv[8 * kc + 6], sv[8 * kc + 7])));
         }
         // zero this step's V rows outside [k_lo, k_hi] (the first and last steps)
-        if (step0 < it.k_lo || step0 + C::kKeys - 1 > it.k_hi) {
-          const uint32_t v_base = smem_addr(s.v[gj % kStages]);
+        const bool edge = step0 < it.k_lo || step0 + C::kKeys - 1 > it.k_hi;
+        if (edge) {
+          const int vs = gj % C::kVStages;  // the V tile must have landed before its rows are zeroed
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.v_full[vs], (gj / C::kVStages) & 1));
+          const uint32_t v_base = smem_addr(s.v[vs]);
 #pragma unroll 1
           for (int e = st; e < C::kKeys * 8; e += C::kSoftmaxThreads) {
             const int kr = e >> 3;  // key row of the step
@@ -668,7 +701,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
           }
         }
-        fence_proxy_async_smem();
+        // shared-memory writes (P, zeroed V rows) made visible to the MMA's reads
+        if (!C::kPInTmem || edge) fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.p_full[pb]);
@@ -778,7 +812,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // pages, so tile t starts 7 t steps into its range (the blocks resident at
 // one time then read different pages: 8 % faster than all in step).
 using SlidingConfig =
-    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 4, 2, true, 2, 2>;
+    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 4, 2, true, 1, 2, 0,
+           2, 2, true>;
 using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2, 1, 7>;
 
 }  // namespace prefill_tc

@@ -104,6 +104,18 @@ __device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tm
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Copies a 128-row x 256-bit matrix (16 bf16 elements per row) from shared
+// memory, described like an MMA operand, into tensor memory: row i to lane i,
+// 8 consecutive columns from taddr, two elements per column.  A later MMA of
+// the same thread sees the copy.
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t s_desc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(s_desc)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
