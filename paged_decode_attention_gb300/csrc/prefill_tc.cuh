@@ -30,16 +30,20 @@
 // of step j while the softmax of step j+1 runs.
 //
 // Running max.  A row's reference max m moves only when a score exceeds it by
-// more than kSlack = 16 log2 units, and then to kHeadroom = 48 above that
-// score.  So every weight exp2(s - m) is at most 2^16, the row's largest is
+// more than kSlack = 64 log2 units, and then to kHeadroom = 48 above that
+// score.  So every weight exp2(s - m) is at most 2^64, the row's largest is
 // at least 2^-48, and only keys more than 78 log2 units below the row max
-// (relative weight < 2^-78) flush to zero: all well inside fp32 and bf16.
-// Numerator and denominator share m, so the result is the same softmax.  O
-// is rescaled in tensor memory only when m moves.  A warp rescales if any of
-// its 32 rows moves, and a row's first keys (the window edge) estimate its
-// max poorly, so a narrow band (2^8, no headroom) made about half of the
-// steps rescale; with these bounds it is a few per cent.  The rescale loads
-// 64 columns per tensor-memory round trip.  Key rows outside [k_lo, k_hi] of the first and last page are
+// (relative weight < 2^-78) flush to zero.  A row sum over at most 2^17 keys
+// stays below 2^81 and O below 2^81 max|v|: inside fp32 (and P inside bf16)
+// for any |v| < 2^46.  Numerator and denominator share m, so the result is
+// the same softmax.  O is rescaled in tensor memory only when m moves, and a
+// warp rescales if any of its 32 rows moves: it waits for the previous P V
+// and round-trips its rows of O, so each rescale stalls the softmax.  A
+// row's first keys (the window edge) estimate its max poorly; with scores of
+// standard deviation 16 (unit-variance q and k, D = 256, scale 1) a band of
+// 2^8 and no headroom made about half of the steps rescale, 2^16 with the
+// headroom 9 %, and 2^64 almost none.  The rescale loads 64 columns per
+// tensor-memory round trip.  Key rows outside [k_lo, k_hi] of the first and last page are
 // zeroed in shared memory before P V (0 * NaN would be NaN); masked scores
 // become -inf.
 #pragma once
@@ -184,7 +188,9 @@ struct Config {
     alignas(1024) uint8_t k[kStages][kKTile];
     alignas(1024) uint8_t v[kVStages][kVTile];
     alignas(128) uint8_t p[kPInTmem ? 1 : 2][kPInTmem ? 16 : kPBytes];
-    alignas(1024) uint8_t ost[kRows * 128];  // one 64-dim chunk of O in bf16, staged for a TMA store
+    // one 64-dim chunk of O in bf16, staged for a TMA store (with Q in tensor
+    // memory, the Q tile's buffer stages all of O instead)
+    alignas(1024) uint8_t ost[kQInTmem ? 16 : kRows * 128];
     alignas(8) uint64_t full[kStages];     // K tile landed (TMA)
     alignas(8) uint64_t empty[kStages];    // its S products done (one commit per issuer)
     alignas(8) uint64_t v_full[kVStages];   // V tile landed (TMA)
@@ -196,6 +202,7 @@ struct Config {
     alignas(8) uint64_t q_ready;         // the item's Q tile landed (TMA)
     alignas(8) uint64_t q_empty;         // the item's Q tile read: its S products done, or copied to tensor memory
     alignas(8) uint64_t q_tfree[kIssuers];  // Q in tensor memory: issuer i's S products of the item done
+    alignas(8) uint64_t ost_free;           // Q in tensor memory: the item's output stores have read the Q buffer
     alignas(8) uint64_t o_full;          // the item's last P V done (commit)
     alignas(8) uint64_t o_free;          // O read by the item's epilogue (the softmax warps)
     alignas(8) uint64_t mma_done;        // every MMA done (commit)
@@ -207,7 +214,7 @@ struct Config {
   static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM within the 227 KB a CTA may have");
 };
 
-constexpr float kSlack = 16.f;     // log2 units
+constexpr float kSlack = 64.f;     // log2 units
 constexpr float kHeadroom = 48.f;  // a moved reference max sits this far above the row's max
 constexpr int kRoundTrip = 4;     // 16-column TMEM loads per wait when O is rescaled or written
 
@@ -337,6 +344,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     mbar_init(&s.q_ready, 1);
     mbar_init(&s.q_empty, C::kIssuers);
     for (int i = 0; i < C::kIssuers; ++i) mbar_init(&s.q_tfree[i], 1);
+    mbar_init(&s.ost_free, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.o_free, 4 * C::kSoftmaxGroups);
     mbar_init(&s.mma_done, C::kIssuers + 1);
@@ -378,7 +386,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!it.run) continue;
       if (kw) {
         if (gt >= 1) {  // the previous item's Q tile read
-          const int wq = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.q_empty, (gt - 1) & 1)) : 0;
+          int wq = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.q_empty, (gt - 1) & 1)) : 0;
+          // with Q in tensor memory the buffer also stages the output of the
+          // item before the previous one
+          if (C::kQInTmem && gt >= 2 && wq) wq = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.ost_free, (gt - 2) & 1)) : 0;
           ok = __shfl_sync(0xffffffffu, wq, 0) != 0;
           if (!ok) break;
         }
@@ -574,6 +585,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!it.run) continue;
       const bool valid = qi < it.nq;
       const int head = it.c * kG + g;
+      // whether this CTA has another item: its Q then passes through the Q
+      // buffer before this item's output may be staged there
+      bool has_next = false;
+      if constexpr (C::kQInTmem) {
+        for (int w2 = w + gridDim.x; w2 < n_work && !has_next; w2 += gridDim.x)
+          has_next = load_tile<C>(p, w2, tiles, false).run;
+      }
       const int pos = it.P0 + qi;
       const int lo_r = p.window > 0 ? pos - p.window + 1 : 0;
 
@@ -729,6 +747,34 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // per-thread stores below: a box would reach the next sequence's rows.)
         constexpr int kOutChunks = kDS / 64;
         constexpr int kOwnChunks = kOutChunks / kGroups;
+        if constexpr (C::kQInTmem) {
+          // every chunk in its own 16 KB of the Q buffer, once the next item's
+          // Q has been copied out of it
+          static_assert(kOutChunks <= C::kKChunks, "O fits the Q buffer");
+          if (ok && has_next) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.q_empty, (gt + 1) & 1));
+#pragma unroll 1
+          for (int cc = h * kOwnChunks; cc < (h + 1) * kOwnChunks; ++cc) {
+            float ov[4][16];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tmem_ld16(t_row + 64 * cc + 16 * u, ov[u]);
+            tmem_wait_ld();
+            const uint32_t row = smem_addr(s.q[cc]) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float* v = &ov[u >> 1][8 * (u & 1)];
+              st_shared_v4(row + ((u ^ (r & 7)) << 4),
+                           make_uint4(pack_bf16x2(v[0] * inv, v[1] * inv), pack_bf16x2(v[2] * inv, v[3] * inv),
+                                      pack_bf16x2(v[4] * inv, v[5] * inv), pack_bf16x2(v[6] * inv, v[7] * inv)));
+            }
+          }
+          fence_proxy_async_smem();
+          named_barrier_sync(1, C::kSoftmaxThreads);
+          if (st == 0) {
+            for (int cc = 0; cc < kOutChunks; ++cc)
+              tma_store_4d(&tm_o, s.q[cc], 0, it.slice * kOutChunks + cc, it.q0 + it.i0, it.c * kG);
+            tma_store_wait_read();
+          }
+        } else {
 #pragma unroll 1
         for (int cc = 0; cc < kOutChunks; ++cc) {
           if (cc / kOwnChunks == h) {
@@ -752,6 +798,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tma_store_wait_read();
           }
           named_barrier_sync(1, C::kSoftmaxThreads);  // the staging buffer read: the next chunk may overwrite it
+        }
         }
       } else {
       const size_t o_off = (static_cast<size_t>(it.q0 + it.i0 + qi) * kHq + head) * kD + it.slice * kDS;
@@ -785,6 +832,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.o_free);  // the next item's first P V may overwrite O
+      if (C::kQInTmem && st == 0) mbar_arrive(&s.ost_free);  // (its stores, if any, have read the Q buffer)
       gs += it.n_steps;
       ++gt;
     }
