@@ -214,6 +214,33 @@ struct Config {
   static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM within the 227 KB a CTA may have");
 };
 
+// Maximum and sum of v[0 .. N) by pairwise halving: log2 N dependent steps
+// instead of N - 1 (N a power of two).
+template <int N>
+__device__ __forceinline__ float tree_max(const float* v) {
+  static_assert((N & (N - 1)) == 0, "a power of two");
+  float t[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) t[k] = v[k];
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+  return t[0];
+}
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+  static_assert((N & (N - 1)) == 0, "a power of two");
+  float t[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) t[k] = v[k];
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int k = 0; k < w; ++k) t[k] += t[k + w];
+  return t[0];
+}
+
 constexpr float kSlack = 64.f;     // log2 units
 constexpr float kHeadroom = 48.f;  // a moved reference max sits this far above the row's max
 constexpr int kRoundTrip = 4;     // 16-column TMEM loads per wait when O is rescaled or written
@@ -627,12 +654,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!valid || key < lo_r || key > pos) sv[k] = -INFINITY;
           }
         }
-        float mx = sv[0];
-#pragma unroll
-        for (int k = 1; k < kHalf; ++k) mx = fmaxf(mx, sv[k]);
+        float mx = tree_max<kHalf>(sv);
         if constexpr (kGroups > 1) {
+          // only the warps holding the same 32 rows exchange: one barrier per
+          // set of them (ids 2-5), so a warp waits for its partners alone
           s.half_max[xb][h][r] = mx;
-          named_barrier_sync(1, C::kSoftmaxThreads);
+          named_barrier_sync(2 + (warp & 3), 32 * kGroups);
 #pragma unroll
           for (int o = 1; o < kGroups; ++o) mx = fmaxf(mx, s.half_max[xb][(h + o) % kGroups][r]);
         }
@@ -663,13 +690,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         if (move) m = m_new + kHeadroom;
         const float m_use = m == -INFINITY ? 0.f : m;
-        float ls = 0.f;
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
-          sv[k] = ex2_approx(fmaf(sv[k], kLog2e, -m_use));
-          ls += sv[k];
-        }
-        l += ls;
+        for (int k = 0; k < kHalf; ++k) sv[k] = ex2_approx(fmaf(sv[k], kLog2e, -m_use));
+        l += tree_sum<kHalf>(sv);
 
         // P row into buffer pb (K-major core matrices of 8 rows x 8 keys) once
         // P V of step gj - kPBufs has read it
