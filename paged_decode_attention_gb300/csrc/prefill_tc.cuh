@@ -875,8 +875,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   }
 }
 
-// Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per block, D = 256,
-// 2-page steps in 4 stages of 32 KB, two S issuers, two softmax warpgroups.
+// Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per work item, D = 256,
+// 2-page steps, K and V tiles in rings of 4 x 16 KB each, Q in tensor memory,
+// one S issuer and a P V issuer, three S buffers, two softmax warpgroups.
 // Global: 8 queries x 16 heads per block, D = 512 split into two blocks of
 // 256 output dims (both compute S), 2-page steps in 2 stages of 48 KB, two S
 // issuers, one softmax warpgroup; every block of a KV head reads the same
@@ -884,7 +885,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // one time then read different pages: 8 % faster than all in step).
 using SlidingConfig =
     Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 4, 2, true, 1, 2, 0,
-           2, 2, true>;
+           3, 2, true>;
 using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2, 1, 7>;
 
 }  // namespace prefill_tc
