@@ -112,7 +112,7 @@ __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bu
 
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kPPS_, bool kPInTmem_, int kIssuers_ = 1,
           int kSoftmaxGroups_ = 1, int kRotate_ = 0, int kSBufs_ = 2, int kPBufs_ = 2, bool kQInTmem_ = false,
-          int kVStages_ = kStages_>
+          int kVStages_ = kStages_, bool kPInS_ = false>
 struct Config {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per block
@@ -170,10 +170,18 @@ struct Config {
   static constexpr uint32_t kQCol = kDS;  // Q (bf16 pairs): kD / 2 columns
   static constexpr uint32_t kSCol = kDS + (kQInTmem ? kD / 2 : 0);  // S buffers: column kSCol + kKeys (kIssuers buffer + part)
   static constexpr uint32_t kPCol = kSCol + kSBufs * kIssuers * kKeys;  // P buffers (bf16 pairs), kKeys / 2 columns each
+  // P written over its own S buffer (the first kKeys / 2 columns): no P
+  // buffers, and an S buffer is free again once the P V product of its step
+  // is done (committed by the P V issuer) instead of once S is read.
+  static constexpr bool kPInS = kPInS_;
+  __device__ static constexpr uint32_t p_col(int b) {
+    return kPInS ? kSCol + kKeys * b : kPCol + (kKeys / 2) * b;
+  }
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 64 == 0 && kDS <= 256, "tile shapes");
-  static_assert(kPCol + (kPInTmem ? kPBufs * kKeys / 2 : 0) <= kTmemCols,
+  static_assert(!kPInS || (kPInTmem && kIssuers == 1 && kPBufs == kSBufs), "P over S: one S part per buffer");
+  static_assert(kPCol + (kPInTmem && !kPInS ? kPBufs * kKeys / 2 : 0) <= kTmemCols,
                 "O, Q, the S buffers and P fit in tensor memory");
   static_assert(kPInTmem || kPBufs == 2, "P in shared memory: two buffers");
   static_assert(kKeys % 16 == 0 && kKeys <= 256, "N of S");
@@ -196,7 +204,7 @@ struct Config {
     alignas(8) uint64_t v_full[kVStages];   // V tile landed (TMA)
     alignas(8) uint64_t v_empty[kVStages];  // its P V product done (commit)
     alignas(8) uint64_t s_full[kSBufs];   // S buffer written (commit)
-    alignas(8) uint64_t s_free[kSBufs];   // S buffer read (the softmax warps)
+    alignas(8) uint64_t s_free[kSBufs];   // S buffer read (the softmax warps), or with P over S its P V done (commit)
     alignas(8) uint64_t p_full[kPBufs];   // P buffer written, O rescaled, V edges zeroed (the softmax warps)
     alignas(8) uint64_t p_empty[kPBufs];  // P V of the buffer's step done (commit)
     alignas(8) uint64_t q_ready;         // the item's Q tile landed (TMA)
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&s.s_full[i], C::kIssuers);
-      mbar_init(&s.s_free[i], 4 * C::kSoftmaxGroups);
+      mbar_init(&s.s_free[i], C::kPInS ? 1 : 4 * C::kSoftmaxGroups);
     }
     for (int i = 0; i < C::kPBufs; ++i) {
       mbar_init(&s.p_full[i], 4 * C::kSoftmaxGroups);
@@ -568,7 +576,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int kk = 0; kk < kPPS; ++kk) {
           const uint64_t b_desc = umma_desc(v_base + kk * C::kVPage, C::kChunkBytes, 1024, 2);
           if constexpr (C::kPInTmem) {
-            umma_bf16_ts_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * pb + 8 * kk, b_desc, C::kIdescPV,
+            umma_bf16_ts_warp(tmem, tmem + C::p_col(pb) + 8 * kk, b_desc, C::kIdescPV,
                               (j > 0 || kk > 0) ? 1u : 0u);
           } else {
             const uint64_t a_desc = umma_desc(smem_addr(s.p[pb]) + kk * 256, 128, C::kKeys * 16, 0);
@@ -576,7 +584,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         umma_commit_warp(&s.v_empty[pst]);  // the V tile read
-        umma_commit_warp(&s.p_empty[pb]);
+        umma_commit_warp(C::kPInS ? &s.s_free[pb] : &s.p_empty[pb]);  // P read
         if (++pst == C::kVStages) pst = 0, pst_ph ^= 1;
         if (++pb == C::kPBufs) pb = 0, pb_ph ^= 1;
       }
@@ -645,7 +653,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.s_free[bs]);
+        if (!C::kPInS && lane == 0) mbar_arrive(&s.s_free[bs]);
 
         if (!valid || pos0 < lo_r || pos0 + kHalf - 1 > pos) {
 #pragma unroll
@@ -669,7 +677,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (__any_sync(0xffffffffu, rescale)) {
           // O's row holds P V up to step j-1: wait for that product, then scale in place
           if (ok && j >= 1)
-            ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[(gj - 1) % C::kPBufs], ((gj - 1) / C::kPBufs) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait_fast(C::kPInS ? &s.s_free[(gj - 1) % C::kPBufs]
+                                                                 : &s.p_empty[(gj - 1) % C::kPBufs],
+                                                        ((gj - 1) / C::kPBufs) & 1));
           tc_fence_after_sync();
           const float f = rescale ? ex2_approx(m - (m_new + kHeadroom)) : 1.f;
 #pragma unroll 1
@@ -696,23 +706,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
         // P row into buffer pb (K-major core matrices of 8 rows x 8 keys) once
         // P V of step gj - kPBufs has read it
-        if (ok && gj >= C::kPBufs)
+        // (P over S: the buffer's previous P V finished before this S was computed)
+        if (!C::kPInS && ok && gj >= C::kPBufs)
           ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[pb], ((gj / C::kPBufs) - 1) & 1));
         if constexpr (C::kPInTmem) {
-          // this row's keys into its lane: column kPCol + (kKeys / 2) pb + k / 2 holds keys k, k + 1
+          // this row's keys into its lane: column p_col(pb) + k / 2 holds keys k, k + 1
           if constexpr (kHalf % 16 == 0) {
 #pragma unroll
             for (int kc = 0; kc < kHalf / 16; ++kc) {
               uint32_t wv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) wv[e] = pack_bf16x2(sv[16 * kc + 2 * e], sv[16 * kc + 2 * e + 1]);
-              tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, wv);
+              tmem_st8(t_row + C::p_col(pb) + kc0 / 2 + 8 * kc, wv);
             }
           } else {  // 8 keys: 4 columns
             uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) wv[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
-            tmem_st4(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2, wv);
+            tmem_st4(t_row + C::p_col(pb) + kc0 / 2, wv);
           }
           tmem_wait_st();
         } else {
@@ -861,7 +872,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     // the last P V products' commits (not all waited for above)
     for (int gj = gs >= C::kPBufs ? gs - C::kPBufs : 0; gj < gs; ++gj)
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.p_empty[gj % C::kPBufs], (gj / C::kPBufs) & 1));
+      if (ok)
+        ok = __all_sync(0xffffffffu, mbar_wait_fast(C::kPInS ? &s.s_free[gj % C::kPBufs] : &s.p_empty[gj % C::kPBufs],
+                                                    (gj / C::kPBufs) & 1));
     if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     if (st == 0) tma_store_wait_all();  // the output stores complete before the CTA retires
   }
@@ -876,16 +889,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 }
 
 // Gemma-4-12B shapes.  Sliding: 64 queries x 2 heads per work item, D = 256,
-// 2-page steps, K and V tiles in rings of 4 x 16 KB each, Q in tensor memory,
-// one S issuer and a P V issuer, three S buffers, two softmax warpgroups.
+// 4-page steps (N = 64), K and V tiles in rings of 2 x 32 KB each, Q in
+// tensor memory, two S buffers with P written over them (O 256 + Q 128 +
+// S 2 x 64 columns), one S issuer and a P V issuer, two softmax warpgroups.
 // Global: 8 queries x 16 heads per block, D = 512 split into two blocks of
 // 256 output dims (both compute S), 2-page steps in 2 stages of 48 KB, two S
 // issuers, one softmax warpgroup; every block of a KV head reads the same
 // pages, so tile t starts 7 t steps into its range (the blocks resident at
 // one time then read different pages: 8 % faster than all in step).
 using SlidingConfig =
-    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 4, 2, true, 1, 2, 0,
-           3, 2, true>;
+    Config<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 2, 4, true, 1, 2, 0,
+           2, 2, true, 2, true>;
 using GlobalConfig = Config<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 2, true, 2, 1, 7>;
 
 }  // namespace prefill_tc
