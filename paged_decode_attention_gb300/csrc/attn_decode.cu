@@ -675,11 +675,13 @@ int32_t run_prefill(Kernel kernel, int32_t kind, const void* q, const void* k_po
   static bool smem_set[2][kMaxDevices] = {{false}};
   if ((st = ensure_smem(kernel, C::kSmemBytes, dev, smem_set[kind]))) return st;
 
-  // K: a CTA pair holds one page of all D dims per CTA (one box); a single
-  // CTA one 64-dim chunk of a page per box.  V: a page's output dims of the
-  // CTA (half of kDS in a pair).
+  // K: a CTA pair with one page per CTA and step copies all D dims of it in
+  // one box; otherwise a box is one 64-dim chunk of a page.  V: a page's
+  // output dims of the CTA (half of kDS in a pair).
+  int k_box_chunks = 1;
+  if constexpr (kPair) k_box_chunks = C::kKBoxChunks;
   CUtensorMap tm_k, tm_v;
-  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, kPair ? C::kKChunks : 1))) return st;
+  if ((st = encode_chunk_map(&tm_k, k_pool, num_pages, C::kHkv * C::kD, k_box_chunks))) return st;
   if ((st = encode_chunk_map(&tm_v, v_pool, num_pages, C::kHkv * C::kD, kPair ? C::kDS / 128 : C::kDS / 64)))
     return st;
 

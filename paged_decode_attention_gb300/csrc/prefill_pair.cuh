@@ -6,29 +6,34 @@
 // A cluster of two CTAs takes two adjacent query tiles of one sequence and KV
 // head: CTA rank r holds tile 2t + r, 128 rows (kQ = 128 / G queries times
 // the G query heads), and its Q in shared memory.  The pair walks the union
-// of its two tiles' key ranges in steps of two pages (32 keys):
-//   S   = Q K^T   one M = 256, N = 32 MMA per 16 dims of D, issued by rank 0:
-//                 A = each CTA's own Q rows, B = the step's keys, page 2i + r
-//                 of the step held by CTA r (one TMA box per page: all D/64
-//                 chunks, [chunk][16 rows][128 B]); D = each CTA's own S rows
-//                 in its tensor memory;
+// of its two tiles' key ranges in steps of kPPS pages (16 kPPS keys, kPPS =
+// 2 or 4):
+//   S   = Q K^T   one M = 256, N = 16 kPPS MMA per 16 dims of D, issued by
+//                 rank 0: A = each CTA's own Q rows, B = the step's keys,
+//                 CTA r holding pages r kPPS/2 .. (r+1) kPPS/2 - 1 of the
+//                 step, chunk-major ([chunk][kPPS/2 x 16 rows][128 B]); D =
+//                 each CTA's own S rows in its tensor memory;
 //   P   = softmax as in prefill_tc.cuh, each CTA on its own rows;
 //   O  += P V     M = 256, N = kDS, K = 16 per page: A = P in each CTA's
 //                 tensor memory, B = V with CTA r holding output dims
-//                 [r kDS/2, (r+1) kDS/2) of both pages.
+//                 [r kDS/2, (r+1) kDS/2) of every page of the step.
 // So each SM copies half of every K and V tile, and one instruction does
 // the work of two.
 //
-// Handshakes.  Each CTA's copies complete on its own `full` barrier; rank
-// 1's idle issuing warp forwards each completed stage to rank 0's
-// `peer_full`.  The softmax warps of each CTA arrive on their own CTA's
+// Handshakes.  K and V tiles sit in two rings with a producer warp each; a
+// K tile is free again when its S products are done, a V tile when its P V
+// product is.  Each CTA's copies complete on its own `k_full` / `v_full`
+// barriers; rank 1's idle issuing warp forwards each landed K tile to rank
+// 0's `k_peer`.  The softmax warps of each CTA arrive on their own CTA's
 // `s_free`, `p_full` and `q_ready`, and two warps of rank 1 forward each
-// completed phase to rank 0's (which count one arrival more): an arrival
-// with release at cluster scope cost a softmax warp about 400 cycles, twice
-// per step, so no softmax warp makes one.  Rank 0 commits every product to
-// both CTAs' barriers (`s_full`, `p_empty`, `empty`, `mma_done`, multicast).
-// Every arrival a CTA receives is waited for before the final cluster
-// barrier, so none can land after a CTA has left; every wait is bounded.
+// completed phase to rank 0's (which count one arrival more), the p_full
+// forward only once rank 1's V tile of the step has landed: an arrival with
+// release at cluster scope cost a softmax warp about 400 cycles, twice per
+// step, so no softmax warp makes one.  Rank 0 commits every product to both
+// CTAs' barriers (`s_full`, `p_empty`, `k_empty`, `v_empty`, `mma_done`,
+// multicast).  Every arrival a CTA receives is waited for before the final
+// cluster barrier, so none can land after a CTA has left; every wait is
+// bounded.
 #pragma once
 
 #include "prefill_tc.cuh"
@@ -39,7 +44,7 @@ namespace prefill_pair {
 using prefill_tc::PrefillParams;
 
 template <int kD_, int kDS_, int kG_, int kHkv_, int kStages_, int kSoftmaxGroups_, int kRotate_, int kSBufs_ = 2,
-          int kPBufs_ = 2, int kSIssuers_ = 1>
+          int kPBufs_ = 2, int kSIssuers_ = 1, int kPPS_ = 2>
 struct PairConfig {
   static constexpr int kD = kD_;    // head dim (the contraction of S)
   static constexpr int kDS = kDS_;  // output dims per pair (each CTA holds V for half of them)
@@ -47,7 +52,10 @@ struct PairConfig {
   static constexpr int kHkv = kHkv_;
   static constexpr int kHq = kG * kHkv;
   static constexpr int kStages = kStages_;
-  static constexpr int kPPS = 2;                 // pages per step: one per CTA for S
+  // Pages per step: 2 (one page of K per CTA) or 4 (two per CTA).  S has
+  // N = 16 kPPS, and each CTA supplies the B rows of its kKPages pages.
+  static constexpr int kPPS = kPPS_;
+  static constexpr int kKPages = kPPS / 2;       // pages of K per CTA per step
   static constexpr int kKeys = kPPS * kPage;     // N of S, K of P V
   static constexpr int kSlices = kD / kDS;
   static constexpr int kRows = 128;               // rows per CTA
@@ -56,20 +64,28 @@ struct PairConfig {
   static constexpr int kVChunksHalf = kDS / 128;  // 64-dim chunks of V per CTA
   static constexpr int kQChunkBytes = kRows * 128;
   static constexpr int kPageChunk = kPage * 128;  // one 64-dim chunk of one page: [16 rows][128 B]
-  static constexpr int kKTile = kKChunks * kPageChunk;  // this CTA's page of K
+  // This CTA's K of a step, chunk-major: [chunk][kKPages * 16 rows][128 B],
+  // so that the B operand of S has its 8-row groups 1 KB apart.  One page
+  // per CTA is one TMA box of all chunks; two pages take one 2 KB box per
+  // page and chunk (a box lands densely, so two pages cannot interleave).
+  static constexpr int kKChunkBytes = kKPages * kPageChunk;
+  static constexpr int kKTile = kKChunks * kKChunkBytes;
+  static constexpr int kKBoxChunks = kKPages == 1 ? kKChunks : 1;  // 64-dim chunks per K box
   static constexpr int kVPage = kVChunksHalf * kPageChunk;
   static constexpr int kVTile = kPPS * kVPage;
   static constexpr int kSoftmaxGroups = kSoftmaxGroups_;
   static constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
   static constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
-  // + producer (warp 4) + two more warps in each CTA.  Rank 0: warp 5
-  // issues the S products, warp kFwdSWarp the P V products (separate
-  // threads, so that S runs ahead of the softmax whatever P waits for).
-  // Rank 1: warp 5 forwards its stages, kFwdSWarp its s_free and q_ready
-  // phases, kFwdPWarp its p_full phases to rank 0.
-  static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
+  // + the K producer (warp 4), two more warps and the V producer in each
+  // CTA.  Rank 0: warp 5 issues the S products, warp kFwdSWarp the P V
+  // products (separate threads, so that S runs ahead of the softmax whatever
+  // P waits for).  Rank 1: warp 5 forwards its landed K tiles, kFwdSWarp
+  // its s_free and q_ready phases, kFwdPWarp its p_full phases (each once
+  // its V tile of the step has landed too) to rank 0.
+  static constexpr int kThreads = (kSoftmaxWarps + 5) * 32;
   static constexpr int kFwdSWarp = kSoftmaxWarps + 2;
   static constexpr int kFwdPWarp = kSoftmaxWarps + 3;
+  static constexpr int kVProdWarp = kSoftmaxWarps + 4;
   static constexpr int kRotate = kRotate_;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSBufs = kSBufs_;                  // S buffers: S runs up to kSBufs steps ahead
@@ -85,6 +101,7 @@ struct PairConfig {
   static constexpr uint32_t kIdescS = umma_idesc_bf16(256, kKeys, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(256, kDS, 0, 1);
   static_assert(kRows % kG == 0 && kD % 64 == 0 && kDS % 128 == 0 && kDS <= 256, "tile shapes");
+  static_assert(kPPS == 2 || kPPS == 4, "two or four pages per step");
   static_assert(kPCol + kPBufs * kKeys / 2 <= kTmemCols, "O, the S buffers and the P buffers fit in tensor memory");
   static_assert(kSoftmaxGroups == 1 || (kSoftmaxGroups == 2 && (kKeys / 2) % 16 == 0 && kDS % 32 == 0),
                 "two softmax warpgroups: halves of whole 16-key blocks");
@@ -93,9 +110,15 @@ struct PairConfig {
     alignas(1024) uint8_t q[kKChunks][kQChunkBytes];
     alignas(1024) uint8_t k[kStages][kKTile];
     alignas(1024) uint8_t v[kStages][kVTile];
-    alignas(8) uint64_t full[kStages];       // this CTA's copies of the stage landed (TMA)
-    alignas(8) uint64_t peer_full[kStages];  // rank 0: rank 1's copies landed (forwarded)
-    alignas(8) uint64_t empty[kStages];      // S and P V of the stage done (two commits, both CTAs)
+    // K and V tiles in two rings, each filled by its own producer warp: a K
+    // tile is released when its S products are done, a V tile when its P V
+    // product is, so that K is copied a step earlier than a shared stage
+    // would allow.
+    alignas(8) uint64_t k_full[kStages];   // this CTA's K tile landed (TMA)
+    alignas(8) uint64_t k_peer[kStages];   // rank 0: rank 1's K tile landed (forwarded)
+    alignas(8) uint64_t k_empty[kStages];  // S products of the tile done (commits, both CTAs)
+    alignas(8) uint64_t v_full[kStages];   // this CTA's V tile landed (TMA)
+    alignas(8) uint64_t v_empty[kStages];  // P V of the tile done (commit, both CTAs)
     alignas(8) uint64_t s_full[kSBufs];      // S buffer written (commit, both CTAs)
     alignas(8) uint64_t s_free[kSBufs];      // S buffer read by this CTA's softmax warps (rank 0: and rank 1's)
     alignas(8) uint64_t p_full[kPBufs];      // P written, O rescaled, V edges zeroed (rank 0: both CTAs)
@@ -136,9 +159,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
-      mbar_init(&s.full[st], 1);
-      mbar_init(&s.peer_full[st], 1);
-      mbar_init(&s.empty[st], C::kSIssuers + 1);  // the S issuers and the P V issuer
+      mbar_init(&s.k_full[st], 1);
+      mbar_init(&s.k_peer[st], 1);
+      mbar_init(&s.k_empty[st], C::kSIssuers);  // the S issuers
+      mbar_init(&s.v_full[st], 1);
+      mbar_init(&s.v_empty[st], 1);  // the P V issuer
     }
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&s.s_full[i], C::kSIssuers);
@@ -205,11 +230,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
     const auto logical_step = [&](int j) { return j + rot < n_steps ? j + rot : j + rot - n_steps; };
     const auto logical_page = [&](int gp) { return logical_step(gp / kPPS) * kPPS + gp % kPPS; };
 
-    if (warp == 4) {
-      // ---------------- producer: this CTA's half of every step ----------------
-      // Lane pg < 2 copies this CTA's output dims of V for page pg of the
-      // step; lane `rank` also copies all of K of page `rank`.  Pages past the
-      // range and bad page ids are copied from a fully out-of-range row: zeros.
+    if (warp == 4 || warp == C::kVProdWarp) {
+      // ---------------- producers: this CTA's half of every step, K (warp 4) and V ----------------
+      // V: lane pg < kPPS copies this CTA's output dims of V for page pg of
+      // the step.  K: lanes kKPages rank .. kKPages (rank + 1) - 1 copy all of
+      // K of their page (the CTA's B rows of S).  Pages past the range and
+      // bad page ids are copied from a fully out-of-range row: zeros.
+      const bool is_k = warp == 4;
+      uint64_t* const full = is_k ? s.k_full : s.v_full;
+      uint64_t* const empty = is_k ? s.k_empty : s.v_empty;
       const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
       bool ok = true;
       int issued = 0;
@@ -229,14 +258,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         const int phys = __shfl_sync(0xffffffffu, cur, (gp0 + (lane < kPPS ? lane : 0)) & 31);
         const int stage = i % kStages;
         if (i >= kStages) {
-          const int w = lane == 0 ? static_cast<int>(mbar_wait_fast(&s.empty[stage], ((i / kStages) - 1) & 1)) : 0;
+          const int w = lane == 0 ? static_cast<int>(mbar_wait_fast(&empty[stage], ((i / kStages) - 1) & 1)) : 0;
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         }
         if (!ok) {
           if (lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], C::kKTile + C::kVTile);
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], is_k ? C::kKTile : C::kVTile);
         __syncwarp();
         if (lane < kPPS) {
           const int gp = logical_page(gp0 + lane);
@@ -247,9 +276,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
             else
               y = phys * kPage;
           }
-          prefill_tc::tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, v_z, &s.full[stage]);
-          if (lane == static_cast<int>(rank))
-            prefill_tc::tma_load_3d(s.k[stage], &tm_k, 0, y, c * C::kKChunks, &s.full[stage]);
+          if (!is_k) {
+            prefill_tc::tma_load_3d(s.v[stage] + lane * C::kVPage, &tm_v, 0, y, v_z, &full[stage]);
+          } else if (lane / C::kKPages == static_cast<int>(rank)) {
+            if constexpr (C::kKPages == 1) {
+              prefill_tc::tma_load_3d(s.k[stage], &tm_k, 0, y, c * C::kKChunks, &full[stage]);
+            } else {
+              const int pc = lane % C::kKPages;  // the page's place among this CTA's keys
+#pragma unroll
+              for (int ch = 0; ch < C::kKChunks; ++ch)
+                prefill_tc::tma_load_3d(s.k[stage] + ch * C::kKChunkBytes + pc * C::kPageChunk, &tm_k, 0, y,
+                                        c * C::kKChunks + ch, &full[stage]);
+            }
+          }
         }
         ++issued;
         __syncwarp();
@@ -257,8 +296,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       if (lane == 0) {  // no copy may still be landing, nor a commit arriving, when the CTA retires
         for (int st = 0; st < kStages && st < issued; ++st) {
           const int uses = (issued - 1 - st) / kStages + 1;
-          if (!mbar_wait(&s.full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
-          if (ok && !mbar_wait(&s.empty[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+          if (!mbar_wait(&full[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
+          if (ok && !mbar_wait(&empty[st], (uses - 1) & 1)) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
         }
       }
     } else if ((warp == 5 || (C::kSIssuers == 2 && warp == C::kFwdPWarp)) && rank == 0) {
@@ -270,21 +309,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
         const int bs = j % C::kSBufs;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.peer_full[st], (j / kStages) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.k_full[st], (j / kStages) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.k_peer[st], (j / kStages) & 1));
         if (ok && j >= C::kSBufs)
           ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.s_free[bs], ((j / C::kSBufs) - 1) & 1));
         tc_fence_after_sync();
-        const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kPageChunk;
+        const uint32_t k_base = smem_addr(s.k[st]) + (part * kPart / 4) * C::kKChunkBytes;
 #pragma unroll
         for (int kk = 0; kk < kPart; ++kk) {
           const uint64_t a_desc = umma_desc(q_base + (kk >> 2) * C::kQChunkBytes + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kPageChunk + (kk & 3) * 32, 16, 1024, 2);
+          const uint64_t b_desc = umma_desc(k_base + (kk >> 2) * C::kKChunkBytes + (kk & 3) * 32, 16, 1024, 2);
           umma_bf16_pair_warp(tmem + C::kSCol + C::kKeys * (C::kSIssuers * bs + part), a_desc, b_desc, C::kIdescS,
                               kk > 0 ? 1u : 0u);
         }
         umma_commit_pair_warp(&s.s_full[bs]);
-        umma_commit_pair_warp(&s.empty[st]);  // K of the stage read
+        umma_commit_pair_warp(&s.k_empty[st]);  // the K tile read
       }
       // the softmax warps' last arrivals on s_free (they are not waited for above)
       for (int j = n_steps >= C::kSBufs ? n_steps - C::kSBufs : 0; j < n_steps; ++j)
@@ -294,12 +333,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     } else if (warp == C::kFwdSWarp && rank == 0) {
       // ---------------- rank 0: the pair's P V products, one of K = 16 per page ----------------
-      // V of step j landed before S(j) was issued, and P(j) exists only after S(j).
+      // P(j) is complete in both CTAs once p_full completes; rank 1 forwards
+      // its arrival only after its own V tile of step j has landed, and this
+      // CTA's V tile is waited for here.
       bool ok = true;
       for (int j = 0; j < n_steps; ++j) {
         const int bp = j % C::kPBufs;
         const int st = j % kStages;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&s.p_full[bp], (j / C::kPBufs) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.v_full[st], (j / kStages) & 1));
         tc_fence_after_sync();
         const uint32_t v_base = smem_addr(s.v[st]);
 #pragma unroll
@@ -308,20 +350,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
           umma_bf16_ts_pair_warp(tmem, tmem + C::kPCol + (C::kKeys / 2) * bp + 8 * kk, b_desc, C::kIdescPV,
                                  (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit_pair_warp(&s.empty[st]);  // V of the stage read
+        umma_commit_pair_warp(&s.v_empty[st]);  // the V tile read
         umma_commit_pair_warp(&s.p_empty[bp]);
       }
       umma_commit_pair_warp(&s.mma_done);
       if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
     } else if (warp == 5) {
-      // ---------------- rank 1: tell rank 0 when each stage of this CTA has landed ----------------
+      // ---------------- rank 1: tell rank 0 when each K tile of this CTA has landed ----------------
       bool ok = true;
-      const uint32_t peer_full0 = at_rank0(&s.peer_full[0]);
+      const uint32_t k_peer0 = at_rank0(&s.k_peer[0]);
       for (int j = 0; j < n_steps; ++j) {
         const int st = j % kStages;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.full[st], (j / kStages) & 1));
-        if (lane == 0) mbar_arrive_cluster_relaxed(peer_full0 + 8 * st);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.k_full[st], (j / kStages) & 1));
+        if (lane == 0) mbar_arrive_cluster_relaxed(k_peer0 + 8 * st);
       }
       if (!__all_sync(0xffffffffu, mbar_wait_fast(&s.mma_done, 0))) ok = false;  // rank 0's last product
       if (!ok && lane == 0) report(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -339,6 +381,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
         for (int j = 0; j < n_steps; ++j) {
           const int bs = j % nbuf;
           if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(fwd_s ? &s.s_free[bs] : &s.p_full[bs], (j / nbuf) & 1));
+          // p_full(j) also tells rank 0 that this CTA's V tile of step j has
+          // landed (P V reads it); the tile is refilled only after P V(j)
+          if (!fwd_s && ok)
+            ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.v_full[j % kStages], (j / kStages) & 1));
           if (lane == 0) {
             // s_free relays finished tensor-memory loads and p_full finished
             // tensor-memory stores (tcgen05.wait::ld / ::st): no data to
@@ -479,8 +525,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
           tmem_st8(t_row + C::kPCol + (C::kKeys / 2) * pb + kc0 / 2 + 8 * kc, w);
         }
         tmem_wait_st();
-        // zero this CTA's V rows outside [k_lo, k_hi] (the first and last steps)
+        // zero this CTA's V rows outside [k_lo, k_hi] (the first and last
+        // steps) once its V tile has landed
         if (step0 < k_lo || step0 + C::kKeys - 1 > k_hi) {
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait_fast(&s.v_full[j % kStages], (j / kStages) & 1));
           const uint32_t v_base = smem_addr(s.v[j % kStages]);
 #pragma unroll 1
           for (int it = st; it < C::kKeys * 8; it += C::kSoftmaxThreads) {
@@ -552,14 +600,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreads, 1)
 // Gemma-4-12B shapes.  Sliding: each CTA 64 queries x 2 heads, D = 256, its
 // stage 8 KB of K (one page) and 8 KB of V (128 dims of two pages), 8
 // stages, two softmax warpgroups.  Global: each CTA 8 queries x 16 heads, D
-// = 512 split into two slices of 256 output dims (both compute S), its stage
-// 16 KB of K and 8 KB of V, 4 stages, one softmax warpgroup, the step order
-// rotated by pair, two S issuers each with two S buffers (768 against 756
-// TFLOP/s with one issuer and three buffers, on one box).
+// = 512 split into two slices of 256 output dims (both compute S), 4-page
+// steps (N = 64), K and V rings of 2 tiles (32 KB and 16 KB per CTA), one
+// softmax warpgroup, the step order rotated by pair, one S issuer, two S
+// buffers of 64 columns and three P buffers of 32 (O 256 + 128 + 96 of the
+// 512 tensor-memory columns).  On a 4096-token chunk of a 32768-token
+// context: 1023-1026 TFLOP/s, against 1018-1020 with two P buffers and
+// 789-791 with 2-page steps (two S issuers, 4 stages) on one box.
 using SlidingPairConfig =
     PairConfig<ATTN_SLIDING_D, ATTN_SLIDING_D, ATTN_SLIDING_HQ / ATTN_SLIDING_HKV, ATTN_SLIDING_HKV, 8, 2, 0>;
 using GlobalPairConfig =
-    PairConfig<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 4, 1, 7, 2, 2, 2>;
+    PairConfig<ATTN_GLOBAL_D, 256, ATTN_GLOBAL_HQ / ATTN_GLOBAL_HKV, ATTN_GLOBAL_HKV, 2, 1, 7, 2, 3, 1, 4>;
 
 }  // namespace prefill_pair
 }  // namespace pda
