@@ -311,11 +311,24 @@ def workload_calls(cfg, device, seed_offset=0):
     """The calls (DecodeCase) of one step of workload `cfg`."""
     from workloads import config_case, N_LAYERS
     if cfg == "5":
-        return [config_case(5, device=device, layer=i, poison=False, seed_offset=seed_offset)
-                for i in range(N_LAYERS)]
+        calls = [config_case(5, device=device, layer=i, poison=False, seed_offset=seed_offset)
+                 for i in range(N_LAYERS)]
+        # the layers of one type share one page layout: one block-table tensor per type
+        first = {}
+        for c in calls:
+            f = first.setdefault(c.kind, c)
+            if f is not c:
+                assert torch_equal(f.block_table, c.block_table), "layers of one type share a page layout"
+                c.block_table = f.block_table
+        return calls
     if cfg == "4b":
         return [config_case(4, device=device, variant="b", poison=False, seed_offset=seed_offset)]
     return [config_case(int(cfg), device=device, poison=False, seed_offset=seed_offset)]
+
+
+def torch_equal(a, b):
+    import torch
+    return bool(torch.equal(a, b))
 
 
 def workload_name(cfg):
@@ -793,14 +806,13 @@ def time_append(calls0, stream, status, dev, rounds=20):
     return out
 
 
-def _packed_inputs(c, dev):
-    """One pinned host buffer and one device buffer holding q, block_table and
-    seq_lens back to back (256-byte aligned), with device views of each part."""
+def _packed_inputs(parts, dev):
+    """One pinned host buffer and one device buffer holding the tensors `parts`
+    back to back (256-byte aligned), with device views of each part."""
     import torch
 
     def a256(n):
         return (n + 255) // 256 * 256
-    parts = [c.q, c.block_table, c.seq_lens]
     sizes = [t.numel() * t.element_size() for t in parts]
     offs, total = [], 0
     for n in sizes:
@@ -816,10 +828,11 @@ def _packed_inputs(c, dev):
 
 
 def run_e2e(args, plans, n_sets, stream, status, dev, batch=4):
-    """End to end through the public binding.  Every step, for every call: an
-    H2D copy of its packed q, block_table and seq_lens from pinned memory, the
-    call (a PreparedDecode of the binding), and a D2H copy of o into pinned
-    memory; the KV cache stays resident.  Steps are pipelined as a serving
+    """End to end through the public binding.  Every step: an H2D copy from
+    pinned memory of each block table the step's calls use (once per table:
+    the layers of one type share one) and, for every call, of its packed q
+    and seq_lens; the call (a PreparedDecode of the binding); and a D2H copy
+    of o into pinned memory.  The KV cache stays resident.  Steps are pipelined as a serving
     loop runs them, `batch` steps at a time: a batch's input copies run on
     their own stream while the compute stream works on the previous batch,
     its output copies on a third stream once its calls are done, and 2*batch
@@ -836,8 +849,14 @@ def run_e2e(args, plans, n_sets, stream, status, dev, batch=4):
         key = (i % n_sets, i % slots)
         if key not in staged:
             calls = []
+            tables = {}  # id of a case's block table -> its device view in this slot
             for c, ws, o in plans[key[0]]:
-                hbuf, dbuf, (qv, btv, slv) = _packed_inputs(c, dev)
+                if id(c.block_table) not in tables:
+                    hbuf, dbuf, (btv,) = _packed_inputs([c.block_table], dev)
+                    tables[id(c.block_table)] = btv
+                    calls.append((hbuf, dbuf, None, None, None))
+                btv = tables[id(c.block_table)]
+                hbuf, dbuf, (qv, slv) = _packed_inputs([c.q, c.seq_lens], dev)
                 o_dev = torch.empty_like(o)
                 prep = pda.PreparedDecode(pda.KIND_SLIDING if c.kind == "sliding" else pda.KIND_GLOBAL,
                                           qv, c.k_pool, c.v_pool, btv, slv, o_dev, window=c.window,
@@ -852,7 +871,7 @@ def run_e2e(args, plans, n_sets, stream, status, dev, batch=4):
         stage(i)
     first = staged[(0, 0)]
     h2d = sum(hbuf.numel() for hbuf, _, _, _, _ in first)
-    d2h = sum(oh.numel() * oh.element_size() for _, _, _, _, oh in first)
+    d2h = sum(oh.numel() * oh.element_size() for _, _, _, _, oh in first if oh is not None)
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]    # a batch's inputs copied
@@ -880,13 +899,15 @@ def run_e2e(args, plans, n_sets, stream, status, dev, batch=4):
                 stream.wait_event(ev_out[par])  # batch nb-2's outputs have been read back
             for i in idx:
                 for _, _, prep, _, _ in stage(i):
-                    prep.run(stream)
+                    if prep is not None:
+                        prep.run(stream)
             ev_comp[par].record(stream)
             s_out.wait_event(ev_comp[par])
             with torch.cuda.stream(s_out):
                 for i in idx:
                     for _, _, _, o_dev, oh in stage(i):
-                        oh.copy_(o_dev, non_blocking=True)
+                        if oh is not None:
+                            oh.copy_(o_dev, non_blocking=True)
             ev_out[par].record(s_out)
             nb += 1
         for par in range(min(nb, 2)):  # join

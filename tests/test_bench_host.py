@@ -129,3 +129,23 @@ def test_source_hash_ignores_comments_only():
     code = "int f(int x) {\n  return x + 1;  // one more\n}\n"
     assert bench._code_only(code) == bench._code_only("/* header */\n" + code.replace("// one more", "// changed"))
     assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))
+
+
+def test_step_layers_of_one_type_share_a_page_layout():
+    # The 48-layer step: each layer has its own cache and queries, and the
+    # layers of one type share one page layout (one block table per type),
+    # so the end-to-end loop copies each table once per step.
+    from workloads import config_case, make_case
+    a = config_case(5, layer=0, poison=False)
+    b = config_case(5, layer=6, poison=False)
+    assert a.kind == b.kind == "sliding"
+    assert a.block_table.equal(b.block_table)
+    assert not a.q.equal(b.q) and not a.k_pool.equal(b.k_pool)
+    # the layout follows layout_seed alone; without it, the case seed
+    lens = [3, 40, 100]
+    c1 = make_case("global", lens, seed=1, layout_seed=9)
+    c2 = make_case("global", lens, seed=2, layout_seed=9)
+    c3 = make_case("global", lens, seed=9)
+    assert c1.block_table.equal(c2.block_table) and c1.block_table.equal(c3.block_table)
+    assert not c1.q.equal(c2.q)
+    assert not make_case("global", lens, seed=1).block_table.equal(c1.block_table)

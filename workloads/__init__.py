@@ -145,7 +145,7 @@ def _allocated_pages(L, window, window_only):
 
 def make_case(kind, seq_lens, seed, device="cpu", window=None, window_only=False,
               k_eq_v=None, poison=True, max_blocks=None, Hq=None, Hkv=None, D=None,
-              chunk_rows=1 << 22):
+              chunk_rows=1 << 22, layout_seed=None):
     """Build one decode case.
 
     kind        "sliding" (16/8 heads, D=256, window 1024) or "global" (16/1, D=512, no window)
@@ -156,6 +156,9 @@ def make_case(kind, seq_lens, seed, device="cpu", window=None, window_only=False
     poison      NaN-fill every slot the decode query must not read
     max_blocks  block-table width (default ceil(max(seq_lens)/16), at least 1)
     Hq/Hkv/D    override the head shape (tests of the oracle only)
+    layout_seed seeds the page layout (block table) instead of `seed`: cases
+                with the same lengths, window rule and layout_seed share one
+                block table, as the layers of one cache layout do in a step
     """
     shape = dict(SLIDING if kind == "sliding" else GLOBAL)
     if window is not None:
@@ -180,7 +183,8 @@ def make_case(kind, seq_lens, seed, device="cpu", window=None, window_only=False
     alloc = [_allocated_pages(L, window, window_only) for L in seq_lens]
     n_alloc = sum(len(a) for a in alloc)
     num_pages = n_alloc + 2
-    perm = torch.randperm(n_alloc, generator=torch.Generator().manual_seed(int(seed) + 7)) + 1
+    lseed = int(seed if layout_seed is None else layout_seed)
+    perm = torch.randperm(n_alloc, generator=torch.Generator().manual_seed(lseed + 7)) + 1
     block_table = torch.full((B, max_blocks), -1, dtype=torch.int32)
     i = 0
     for b, pages in enumerate(alloc):
@@ -278,9 +282,14 @@ def config_case(cfg, device="cpu", variant=None, layer=0, poison=True, seed_offs
     if cfg == 4:
         return make_case("global", L, seed, device, poison=poison)
     if cfg == 5:
+        # every layer of one type has its own cache and queries but the same
+        # page layout (one block table per layer type, the layout of the
+        # type's first layer: 0 sliding, 5 global)
+        first = 5 if is_global_layer(layer) else 0
+        layout = 1000 * cfg + first + seed_offset
         if is_global_layer(layer):
-            return make_case("global", L, seed, device, poison=poison)
-        return make_case("sliding", L, seed, device, window_only=True, poison=poison)
+            return make_case("global", L, seed, device, poison=poison, layout_seed=layout)
+        return make_case("sliding", L, seed, device, window_only=True, poison=poison, layout_seed=layout)
     raise ValueError("unknown workload %r" % (cfg,))
 
 
