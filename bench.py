@@ -184,7 +184,7 @@ def load_bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def time_prefill(stream, dev, reps=5):
+def time_prefill(stream, dev, reps=20):
     """attn_prefill_* on PREFILL_WORKLOADS: TFLOP/s of the algorithmic flops,
     CUDA events on the launching stream around `reps` back-to-back calls."""
     import torch
